@@ -1,0 +1,181 @@
+"""CPU oracle for the 2:4 sparse FP8 path (numpy front end to ``sp24_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA path (``semi_structured_sparse_gb300``) and never imports it.
+
+Every function cites the passage it follows; ``sp24_oracle.c`` holds the
+step-by-step definitions.  Arrays are numpy: bf16 tensors travel as their
+``uint16`` bit patterns, e4m3 tensors as ``uint8`` codes.
+"""
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        I = ctypes.c_int
+        L.ora_e4m3_from_f32.argtypes = [ctypes.c_float]
+        L.ora_e4m3_from_f32.restype = ctypes.c_uint8
+        L.ora_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.ora_e4m3_to_f64.restype = ctypes.c_double
+        L.ora_e4m3_encode_array.argtypes = [P, I64, P]
+        L.ora_keep2.argtypes = [P, P]
+        L.ora_prune.argtypes = [P, I64, I64, I64, P]
+        L.ora_weight_scales.argtypes = [P, I64, I64, I64, I, I, P]
+        L.ora_compress.argtypes = [P, I64, I64, I64, I, I, P, P, P]
+        L.ora_decompress.argtypes = [P, P, I64, I64, P]
+        L.ora_quantize_act.argtypes = [P, I64, I64, I64, I, P, P]
+        L.ora_gemm.argtypes = [P, P, I64, I64, I64, I, P, P, P, I64, I, I,
+                               P, P, I64, I, P]
+        L.ora_num_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return int(lib().ora_num_threads())
+
+
+# ----------------------------------------------------------------- e4m3 codec
+def e4m3_encode(x) -> np.ndarray:
+    """RNE + satfinite fp32 -> e4m3 codes (OCP E4M3, the float8_e4m3fn type of
+    torchao PR #3258).  Output has the input's shape."""
+    x = _c(x, np.float32)
+    q = np.empty(x.shape, dtype=np.uint8)
+    lib().ora_e4m3_encode_array(_p(x), x.size, _p(q))
+    return q
+
+
+def e4m3_decode(q) -> np.ndarray:
+    """e4m3 codes -> exact float64 values (NaN for S.1111.111)."""
+    q = _c(q, np.uint8)
+    table = np.array([lib().ora_e4m3_to_f64(i) for i in range(256)], dtype=np.float64)
+    return table[q]
+
+
+# -------------------------------------------------------------------- prune
+def keep2(group) -> tuple:
+    """Kept positions (i0 < i1) of one group of four bf16 bit patterns
+    (torchao PR #3258, jcaip's review: drop the two smallest |w| of each 4)."""
+    v = _c(group, np.uint16)
+    out = np.zeros(2, dtype=np.int32)
+    lib().ora_keep2(_p(v), _p(out))
+    return int(out[0]), int(out[1])
+
+
+def prune(W_bits: np.ndarray) -> np.ndarray:
+    """Pruned copy of W (bf16 bits [N,K]); dropped positions set to +0."""
+    W = _c(W_bits, np.uint16)
+    N, K = W.shape
+    out = np.empty_like(W)
+    lib().ora_prune(_p(W), N, K, K, _p(out))
+    return out
+
+
+# ------------------------------------------------------------------- scales
+def weight_scales(W_bits, gN: int, gK: int) -> np.ndarray:
+    """amax/448 per (gN x gK) block, layout [K/gK][ceil(N/gN)]."""
+    W = _c(W_bits, np.uint16)
+    N, K = W.shape
+    nG = (N + gN - 1) // gN
+    s = np.empty((K // gK, nG), dtype=np.float32)
+    lib().ora_weight_scales(_p(W), N, K, K, gN, gK, _p(s))
+    return s
+
+
+# ------------------------------------------------------------------ compress
+def compress(W_bits, gN: int = 1, gK: int = None):
+    """Prune + scale + e4m3 + pack (logical metadata layout).
+
+    Returns (values uint8 [N,K/2], meta uint8 [N,K/8], scales fp32 [K/gK,ceil(N/gN)]).
+    """
+    W = _c(W_bits, np.uint16)
+    N, K = W.shape
+    gK = K if gK is None else gK
+    nG = (N + gN - 1) // gN
+    values = np.empty((N, K // 2), dtype=np.uint8)
+    meta = np.empty((N, K // 8), dtype=np.uint8)
+    scales = np.empty((K // gK, nG), dtype=np.float32)
+    lib().ora_compress(_p(W), N, K, K, gN, gK, _p(values), _p(meta), _p(scales))
+    return values, meta, scales
+
+
+def decompress(values, meta) -> np.ndarray:
+    """Dense e4m3 codes [N,K] from (values, meta); dropped positions are 0x00."""
+    values = _c(values, np.uint8)
+    meta = _c(meta, np.uint8)
+    N = values.shape[0]
+    K = values.shape[1] * 2
+    dense = np.empty((N, K), dtype=np.uint8)
+    lib().ora_decompress(_p(values), _p(meta), N, K, _p(dense))
+    return dense
+
+
+# ------------------------------------------------------- activation quantize
+def quantize_act(X, gK: int = None):
+    """Per-token (gK = K) or 1 x gK activation quantization.
+    Returns (xq uint8 [M,K], sx fp32 [K/gK, M])."""
+    X = _c(X, np.float32)
+    M, K = X.shape
+    gK = K if gK is None else gK
+    xq = np.empty((M, K), dtype=np.uint8)
+    sx = np.empty((K // gK, M), dtype=np.float32)
+    lib().ora_quantize_act(_p(X), M, K, K, gK, _p(xq), _p(sx))
+    return xq, sx
+
+
+# ---------------------------------------------------------------------- GEMM
+def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None,
+         X2=None, W2=None, acc_fp64: bool = False) -> np.ndarray:
+    """Group-wise scaled 2:4 sparse GEMM Y[M,N] = X.W^T (+ X2.W2^T), as float64.
+
+    xq [M,K] e4m3; sx [K/gK, ceil(M/gM)]; values [N,K/2]; meta [N,K/8] logical;
+    sw [K/gK, ceil(N/gN)]; X2 [M,r], W2 [N,r] bf16 bits or None.
+    acc_fp64=False accumulates in fp32 (the reference the path is held to);
+    True accumulates in double (used to bound the fp32 reference's own error).
+    """
+    xq = _c(xq, np.uint8)
+    M, K = xq.shape
+    gK = K if gK is None else gK
+    values = _c(values, np.uint8)
+    meta = _c(meta, np.uint8)
+    N = values.shape[0]
+    sx = _c(sx, np.float32)
+    sw = _c(sw, np.float32)
+    assert sx.size == (K // gK) * ((M + gM - 1) // gM)
+    assert sw.size == (K // gK) * ((N + gN - 1) // gN)
+    r = 0
+    if X2 is not None:
+        X2 = _c(X2, np.uint16)
+        W2 = _c(W2, np.uint16)
+        r = X2.shape[1]
+        assert X2.shape == (M, r) and W2.shape == (N, r)
+    Y = np.empty((M, N), dtype=np.float64)
+    lib().ora_gemm(_p(xq), _p(sx), M, K, K, gM, _p(values), _p(meta), _p(sw), N, gN, gK,
+                   _p(X2), _p(W2), r, 1 if acc_fp64 else 0, _p(Y))
+    return Y
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32."""
+    b = _c(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32)

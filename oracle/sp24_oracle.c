@@ -1,0 +1,331 @@
+/*
+ * sp24_oracle.c -- plain CPU oracle for the 2:4 sparse FP8 linear-layer path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the test suite, the package smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table or
+ * constant generator with the CUDA implementation.
+ *
+ * What it computes, and where each step comes from:
+ *   - magnitude 2:4 pruning along K: in every group of four consecutive K
+ *     elements of a weight row, the two smallest magnitudes are zeroed
+ *     (pytorch/ao PR #3258 "Introduce new W8A8-FP-CSR quantization API",
+ *     jcaip's review of the pruning code: argsort of |w| over each group of
+ *     four, the first two indices scattered to zero);
+ *   - weight scale amax/448 per output channel or per 128x128 block, strictly
+ *     positive (same PR, review thread on the positive-scale check; block
+ *     granularity from CUTLASS PR #2095 "Improvements for: Groupwise scaling
+ *     along M for FP8 gemm", ScaleGranularityM/N description);
+ *   - e4m3 quantization q = e4m3(x / scale) (same PR, activation path that
+ *     casts the scaled tensor to float8_e4m3fn), written here from the OCP
+ *     FP8 E4M3 format definition (1 sign, 4 exponent bits with bias 7, 3
+ *     mantissa bits, no infinities, S.1111.111 = NaN, max finite 448);
+ *   - packing into kept values plus 2-bit position metadata, and nothing
+ *     dense (same PR, jcaip: store specified values and sparsity metadata);
+ *   - the group-wise scaled GEMM Y = X.W^T, each K block of length gK
+ *     summed, then multiplied by sx*sw and added to the running sum (CUTLASS
+ *     PR #2095, promotion of per-K-tile partial sums), plus an optional
+ *     bf16 side GEMM X2.W2^T added into the same output (CUTLASS issue
+ *     #2058 "How to implement a fused mixed precision matrix multiplication
+ *     such as w4a4 + w16a16?", hyx1999's statement of Y = X1 W1^T + X2 W2^T).
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - ties in the pruning argsort: the lower index wins;
+ *   - amax == 0 (all-zero group, which must be accepted): scale = 1;
+ *   - quantization divides by the scale (IEEE fp32, correctly rounded),
+ *     then rounds to nearest-even with saturation to +-448; the sign of a
+ *     value that rounds to zero is kept (0x80);
+ *   - metadata nibble of a group = i0 | i1 << 2 with i0 < i1 the kept
+ *     positions; two groups per byte, the even group in the low nibble.
+ *
+ * Build: plain C11, no intrinsics, -ffp-contract=off so that every fp32
+ * operation rounds on its own on any host ISA.  OpenMP (optional) splits the
+ * outer loop over rows only; every output element is computed by one thread
+ * in the order written.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define E4M3_MAX_FINITE 448.0
+
+/* ---------------------------------------------------------------- helpers */
+
+/* bf16 is the upper half of an IEEE binary32: widening is exact. */
+float ora_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Value of an e4m3 code, straight from the format definition. */
+double ora_e4m3_to_f64(uint8_t q)
+{
+    int s = (q >> 7) & 1;
+    int e = (q >> 3) & 0xF;
+    int m = q & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);           /* subnormal: (m/8) * 2^(1-7) */
+    else
+        v = ldexp(8.0 + (double)m, e - 10); /* normal: (1+m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* Nearest e4m3 code to x: round to nearest, ties to the even code (the code's
+ * lowest bit is the mantissa's lowest bit); |x| >= 448 saturates to 448; the
+ * sign bit is always copied, so small negatives give -0 (0x80).
+ * Finds the bracketing pair of non-negative codes by bisection over the
+ * ordered code range 0x00..0x7E, then compares the two distances exactly in
+ * double (fp32 inputs and e4m3 values are both exact there). */
+uint8_t ora_e4m3_from_f32(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    int lo, hi;
+    double dlo, dhi;
+    if (isnan(x)) return (uint8_t)(sign | 0x7F);
+    if (a >= E4M3_MAX_FINITE) return (uint8_t)(sign | 0x7E);
+    lo = 0x00;  /* value(lo) <= a */
+    hi = 0x7E;  /* value(hi) >  a */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (ora_e4m3_to_f64((uint8_t)mid) <= a) lo = mid; else hi = mid;
+    }
+    dlo = a - ora_e4m3_to_f64((uint8_t)lo);
+    dhi = ora_e4m3_to_f64((uint8_t)hi) - a;
+    if (dlo < dhi) return (uint8_t)(sign | lo);
+    if (dhi < dlo) return (uint8_t)(sign | hi);
+    return (uint8_t)(sign | ((lo & 1) == 0 ? lo : hi));
+}
+
+/* Elementwise ora_e4m3_from_f32 over an array. */
+void ora_e4m3_encode_array(const float *x, int64_t n, uint8_t *q)
+{
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < n; ++i) q[i] = ora_e4m3_from_f32(x[i]);
+}
+
+/* --------------------------------------------------------------- pruning */
+
+/* Kept positions of one group of four bf16 values.  The magnitude of a finite
+ * bf16 orders like its bit pattern with the sign cleared (which also makes
+ * +0 and -0 equal).  rank_i = number of elements that beat element i, where
+ * j beats i if |v_j| > |v_i|, or |v_j| == |v_i| and j < i.  The two elements
+ * of rank 0 and 1 are kept; keep[0] < keep[1]. */
+void ora_keep2(const uint16_t v[4], int keep[2])
+{
+    unsigned a[4];
+    int i, j, n = 0;
+    for (i = 0; i < 4; ++i) a[i] = v[i] & 0x7FFFu;
+    for (i = 0; i < 4; ++i) {
+        int rank = 0;
+        for (j = 0; j < 4; ++j)
+            if (a[j] > a[i] || (j < i && a[j] == a[i])) ++rank;
+        if (rank < 2) keep[n++] = i;
+    }
+}
+
+/* Pruned copy of W (bf16 bits): the two dropped positions of every group set
+ * to +0.  W is [N][K] with row stride ldw; out is [N][K] packed. */
+void ora_prune(const uint16_t *W, int64_t N, int64_t K, int64_t ldw, uint16_t *out)
+{
+    int64_t n;
+#pragma omp parallel for schedule(static)
+    for (n = 0; n < N; ++n) {
+        int64_t g;
+        for (g = 0; g < K / 4; ++g) {
+            const uint16_t *v = W + n * ldw + 4 * g;
+            int keep[2], i;
+            ora_keep2(v, keep);
+            for (i = 0; i < 4; ++i)
+                out[n * K + 4 * g + i] = (i == keep[0] || i == keep[1]) ? v[i] : 0;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- scales */
+
+/* Scale of one block: amax over the block (fp32), divided by 448 in fp32;
+ * 1 for an all-zero block. */
+static float block_scale(const uint16_t *W, int64_t ldw, int64_t r0, int64_t r1,
+                         int64_t c0, int64_t c1)
+{
+    float amax = 0.0f;
+    int64_t r, c;
+    for (r = r0; r < r1; ++r)
+        for (c = c0; c < c1; ++c) {
+            float a = fabsf(ora_bf16_to_f32(W[r * ldw + c]));
+            if (a > amax) amax = a;
+        }
+    if (amax == 0.0f) return 1.0f;
+    return amax / (float)E4M3_MAX_FINITE;
+}
+
+/* Weight scales for granularity (gN, gK): layout [K/gK][ceil(N/gN)], the
+ * N-group index fastest (the "M-major" scale layout of CUTLASS PR #2095
+ * applied to the weight, which sits in the GEMM's M slot). */
+void ora_weight_scales(const uint16_t *W, int64_t N, int64_t K, int64_t ldw,
+                       int gN, int gK, float *scales)
+{
+    int64_t nG = (N + gN - 1) / gN, kB = K / gK, ng;
+#pragma omp parallel for schedule(static)
+    for (ng = 0; ng < nG; ++ng) {
+        int64_t kb;
+        int64_t r1 = (ng + 1) * gN < N ? (ng + 1) * gN : N;
+        for (kb = 0; kb < kB; ++kb)
+            scales[kb * nG + ng] = block_scale(W, ldw, ng * gN, r1, kb * gK, (kb + 1) * gK);
+    }
+}
+
+/* ----------------------------------------------------------- compression */
+
+/* Prune, scale, quantize and pack.
+ *   values[n][K/2]: kept e4m3 codes, two per group, in ascending k;
+ *   meta[n][K/8]:   one nibble per group (i0 | i1<<2), group 2j in the low
+ *                   nibble of byte j, group 2j+1 in the high nibble;
+ *   scales:         as ora_weight_scales.
+ * The scale of an element's block is computed from the unpruned W; pruning
+ * never removes a group's largest magnitude, so this equals the amax of the
+ * pruned block. */
+void ora_compress(const uint16_t *W, int64_t N, int64_t K, int64_t ldw, int gN, int gK,
+                  uint8_t *values, uint8_t *meta, float *scales)
+{
+    int64_t nG = (N + gN - 1) / gN, n;
+    ora_weight_scales(W, N, K, ldw, gN, gK, scales);
+#pragma omp parallel for schedule(static)
+    for (n = 0; n < N; ++n) {
+        int64_t g;
+        for (g = 0; g < K / 8; ++g) meta[n * (K / 8) + g] = 0;
+        for (g = 0; g < K / 4; ++g) {
+            const uint16_t *v = W + n * ldw + 4 * g;
+            float s = scales[((4 * g) / gK) * nG + n / gN];
+            int keep[2], t;
+            ora_keep2(v, keep);
+            for (t = 0; t < 2; ++t) {
+                float q = ora_bf16_to_f32(v[keep[t]]) / s;
+                values[n * (K / 2) + 2 * g + t] = ora_e4m3_from_f32(q);
+            }
+            meta[n * (K / 8) + g / 2] |= (uint8_t)((keep[0] | (keep[1] << 2)) << (4 * (g & 1)));
+        }
+    }
+}
+
+/* Dense [N][K] e4m3 codes from the packed form; dropped positions are +0. */
+void ora_decompress(const uint8_t *values, const uint8_t *meta, int64_t N, int64_t K,
+                    uint8_t *dense)
+{
+    int64_t n;
+#pragma omp parallel for schedule(static)
+    for (n = 0; n < N; ++n) {
+        int64_t g;
+        for (g = 0; g < K; ++g) dense[n * K + g] = 0;
+        for (g = 0; g < K / 4; ++g) {
+            int nib = (meta[n * (K / 8) + g / 2] >> (4 * (g & 1))) & 0xF;
+            int i0 = nib & 3, i1 = (nib >> 2) & 3;
+            dense[n * K + 4 * g + i0] = values[n * (K / 2) + 2 * g];
+            dense[n * K + 4 * g + i1] = values[n * (K / 2) + 2 * g + 1];
+        }
+    }
+}
+
+/* ------------------------------------------------- activation quantization */
+
+/* Dynamic activation quantization (pytorch/ao PR #3258, the activation path:
+ * divide by the scale, then cast to e4m3).  X fp32 [M][K] (row stride ldx);
+ * one scale per token and K block of length gK: sx[K/gK][M], M fastest;
+ * sx = amax/448 (1 for an all-zero block); xq[m][k] = e4m3(x / sx). */
+void ora_quantize_act(const float *X, int64_t M, int64_t K, int64_t ldx, int gK,
+                      uint8_t *xq, float *sx)
+{
+    int64_t m;
+#pragma omp parallel for schedule(static)
+    for (m = 0; m < M; ++m) {
+        int64_t kb, k;
+        for (kb = 0; kb < K / gK; ++kb) {
+            float amax = 0.0f, s;
+            for (k = kb * gK; k < (kb + 1) * gK; ++k) {
+                float a = fabsf(X[m * ldx + k]);
+                if (a > amax) amax = a;
+            }
+            s = amax == 0.0f ? 1.0f : amax / (float)E4M3_MAX_FINITE;
+            sx[kb * M + m] = s;
+            for (k = kb * gK; k < (kb + 1) * gK; ++k)
+                xq[m * K + k] = ora_e4m3_from_f32(X[m * ldx + k] / s);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------- GEMM */
+
+/* Group-wise scaled sparse GEMM, Y[m][n] for every token m and channel n:
+ *   for each K block kb of length gK (kb ascending):
+ *       P  = sum over kept k in the block, k ascending, of wq[n][k] * xq[m][k]
+ *       acc = acc + (sx[kb][m/gM] * sw[kb][n/gN]) * P
+ *   acc = acc + sum_{j<r} X2[m][j] * W2[n][j]          (bf16 side GEMM)
+ * Only kept weights are multiplied (the sparse loop); wq comes from values
+ * and the metadata nibbles.  Every product of two e4m3 values, and of two
+ * bf16 values, is exact in fp32.  acc_fp64 = 0 accumulates in fp32 (each
+ * operation rounded, as written above); 1 accumulates in double.
+ * Layouts: xq [M][K] row stride ldx; sx [K/gK][ceil(M/gM)]; values [N][K/2];
+ * meta [N][K/8]; sw [K/gK][ceil(N/gN)]; X2 [M][r]; W2 [N][r]; Y [M][N]. */
+void ora_gemm(const uint8_t *xq, const float *sx, int64_t M, int64_t K, int64_t ldx, int gM,
+              const uint8_t *values, const uint8_t *meta, const float *sw, int64_t N,
+              int gN, int gK, const uint16_t *X2, const uint16_t *W2, int64_t r,
+              int acc_fp64, double *Y)
+{
+    int64_t ldsx = (M + gM - 1) / gM, ldsw = (N + gN - 1) / gN, kB = K / gK;
+    double dec[256];
+    int64_t m;
+    int i;
+    for (i = 0; i < 256; ++i) dec[i] = ora_e4m3_to_f64((uint8_t)i);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (m = 0; m < M; ++m) {
+        int64_t n;
+        for (n = 0; n < N; ++n) {
+            float accf = 0.0f;
+            double accd = 0.0;
+            int64_t kb, g, j;
+            for (kb = 0; kb < kB; ++kb) {
+                float pf = 0.0f;
+                double pd = 0.0;
+                for (g = kb * gK / 4; g < (kb + 1) * gK / 4; ++g) {
+                    int nib = (meta[n * (K / 8) + g / 2] >> (4 * (g & 1))) & 0xF;
+                    int i0 = nib & 3, i1 = (nib >> 2) & 3;
+                    double p0 = dec[values[n * (K / 2) + 2 * g]] * dec[xq[m * ldx + 4 * g + i0]];
+                    double p1 = dec[values[n * (K / 2) + 2 * g + 1]] * dec[xq[m * ldx + 4 * g + i1]];
+                    if (acc_fp64) { pd += p0; pd += p1; }
+                    else { pf += (float)p0; pf += (float)p1; }
+                }
+                if (acc_fp64) {
+                    accd += ((double)sx[kb * ldsx + m / gM] * (double)sw[kb * ldsw + n / gN]) * pd;
+                } else {
+                    float s = sx[kb * ldsx + m / gM] * sw[kb * ldsw + n / gN];
+                    accf += s * pf;
+                }
+            }
+            for (j = 0; j < r; ++j) {
+                double p = (double)ora_bf16_to_f32(X2[m * r + j]) * (double)ora_bf16_to_f32(W2[n * r + j]);
+                if (acc_fp64) accd += p; else accf += (float)p;
+            }
+            Y[m * N + n] = acc_fp64 ? accd : (double)accf;
+        }
+    }
+}
+
+/* Threads the OpenMP loops above use (1 without OpenMP). */
+int ora_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
