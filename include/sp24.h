@@ -1,0 +1,158 @@
+/*
+ * sp24.h -- C ABI of libsp24: 2:4 semi-structured sparse FP8 (e4m3) linear
+ * layer on a GB300 (sm_103a).
+ *
+ *   Y[M,N] (bf16) = X[M,K] . W[N,K]^T  with W pruned 2:4 along K,
+ *   both operands e4m3 with group-wise fp32 scales, plus an optional bf16
+ *   side term X2[M,r] . W2[N,r]^T added into the same output.
+ *
+ * General conventions
+ *   - Pointers marked (device) are CUDA device pointers owned by the caller;
+ *     the library never allocates, frees or retains them.  Pointers marked
+ *     (host) are ordinary host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is stream-ordered and asynchronous; none
+ *     synchronises except sp24_last_device_error().
+ *   - Every entry point checks its arguments before launching anything and
+ *     returns an sp24_status; nothing throws across the ABI.  On an error
+ *     no kernel has been launched and no output has been written.
+ *   - Row-major storage; "ld" arguments are row strides in elements.
+ *   - Scale tensors use the layout [K/gK][ceil(rows/g)] with the row-group
+ *     index fastest (the "M-major" scale layout of CUTLASS PR #2095,
+ *     "Improvements for: Groupwise scaling along M for FP8 gemm", PR
+ *     description).  gK = K means one block along K.
+ *
+ * The pages this follows are cited by title and comment thread:
+ *   [2029] CUTLASS issue #2029, "[QST] CUTLASS support for fp8 sparse
+ *          matrix(for W) multiplication ... sparse tensor core";
+ *   [2095] CUTLASS PR #2095, "Improvements for: Groupwise scaling along M
+ *          for FP8 gemm";
+ *   [2058] CUTLASS issue #2058, "[QST] How to implement a fused mixed
+ *          precision matrix multiplication such as w4a4 + w16a16?";
+ *   [3258] pytorch/ao PR #3258, "Introduce new W8A8-FP-CSR quantization API".
+ */
+#ifndef SP24_H
+#define SP24_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SP24_OK = 0,
+  SP24_ERR_INVALID_ARG = 1,    /* null pointer, bad size or stride            */
+  SP24_ERR_UNSUPPORTED = 2,    /* valid but not implemented (granularity ...) */
+  SP24_ERR_ALIGNMENT = 3,      /* pointer or row stride not 16-byte aligned   */
+  SP24_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed           */
+  SP24_ERR_ARCH = 5,           /* current device is not sm_103                */
+  SP24_ERR_WORKSPACE = 6,      /* workspace missing or too small              */
+  SP24_ERR_DEVICE_TIMEOUT = 7  /* a kernel gave up waiting (device error word)*/
+} sp24_status;
+
+/* Human-readable name of a status code (static string). */
+const char* sp24_status_string(sp24_status s);
+
+/* Bytes of sparsity metadata for an N x K weight: N * K / 8 (one 4-bit
+ * entry per group of four along K).  K must be a multiple of 8. */
+size_t sp24_meta_bytes(int64_t N, int64_t K);
+
+/*
+ * sp24_fp8_compress -- magnitude 2:4 prune + e4m3 quantize + pack.
+ * Follows [3258] (jcaip's review: drop the two smallest |w| of each group of
+ * four along K; positive amax-based scales; keep only the specified values
+ * and the sparsity metadata, nothing dense; an all-zero weight is legal) and
+ * [2095] for the 128x128 block scale granularity.
+ *
+ *   W       (device) bf16 [N][K], row stride ldw >= K elements.
+ *   gN, gK  weight scale granularity: (1, K) per output channel,
+ *           (1, 128) per channel and 128-wide K block, or (128, 128) blocks.
+ *   values  (device, out) uint8 e4m3 [N][K/2]: for group g of row n the two
+ *           kept elements, in ascending k, at values[n][2g], values[n][2g+1].
+ *   meta    (device, out) sp24_meta_bytes(N, K) bytes: row n holds K/8 bytes;
+ *           byte j carries group 2j in its low nibble and group 2j+1 in its
+ *           high nibble; a nibble is i0 | (i1 << 2), i0 < i1 the kept
+ *           positions within the group.  This is also the layout the GEMM
+ *           reads.
+ *   scales  (device, out) fp32 [K/gK][ceil(N/gN)]: amax/448 of the block
+ *           (1.0 for an all-zero block).
+ * Each kept element is q = e4m3_rn_satfinite(w / scale) with a correctly
+ * rounded fp32 division.  Ties in |w| keep the lower index.
+ * Preconditions: N >= 1; K a positive multiple of 128; N % 128 == 0 when
+ * gN == 128; W, values and meta 16-byte aligned, ldw*2 a multiple of 16.
+ */
+sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, int64_t ldw, int gN, int gK,
+                              void* values, void* meta, float* scales, void* stream);
+
+/*
+ * sp24_fp8_quantize_act -- dynamic activation quantization to e4m3.
+ * Follows [3258] (the activation path divides by the scale, then casts to
+ * e4m3) with the per-token / 1x128 granularities of [2095].
+ *
+ *   X   (device) fp32 [M][K], row stride ldx >= K.
+ *   gK  K or 128 (scales per token, or per token and 128-wide K block).
+ *   xq  (device, out) uint8 e4m3 [M][K] (row stride K).
+ *   sx  (device, out) fp32 [K/gK][M]: amax/448 (1.0 for an all-zero block).
+ * Preconditions: M >= 1; K a positive multiple of 128; X and xq 16-byte
+ * aligned; ldx*4 a multiple of 16.
+ */
+sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
+                                  float* sx, void* stream);
+
+/*
+ * sp24_fp8_gemm -- group-wise scaled 2:4 sparse FP8 GEMM with an optional
+ * fused bf16 side GEMM:
+ *
+ *   Y[m][n] = bf16( sum_kb sx[kb][m/gM] * sw[kb][n/gN] * P_kb[m][n]
+ *                   + sum_{j<r} X2[m][j] * W2[n][j] )
+ *   P_kb[m][n] = sum over k in K block kb of xq[m][k] * wq[n][k]  (fp32)
+ *
+ * where wq is the dense weight that (values, meta) encode.  Internally the
+ * product is computed as Y^T = W . X^T so that the sparse weight is the
+ * row-major sparse A operand of the tensor core ([2029], klevzoff's
+ * swap+transpose answer); no data is moved for that.  Per-K-block partial
+ * sums are scaled and added to the running fp32 sum ([2095], promotion per K
+ * tile).  Token rows beyond M in the last tile are computed on zero fill and
+ * not stored ([2095], predication of partial tiles).  The side GEMM is the
+ * small w16a16 term of [2058] (hyx1999: Y = X1 W1^T + X2 W2^T in one kernel).
+ *
+ *   Xq      (device) uint8 e4m3 [M][K], row stride ldx (ldx % 16 == 0).
+ *   sx      (device) fp32 [K/gK][ceil(M/gM)].
+ *   gM      1 or 128.
+ *   values, meta (device) as produced by sp24_fp8_compress for [N][K].
+ *   sw      (device) fp32 [K/gK][ceil(N/gN)].
+ *   gN      1 or 128; gK: K or 128.
+ *   X2, W2  (device) bf16 [M][r] and [N][r] (row stride r), or NULL with
+ *           r = 0 for no side GEMM; r a multiple of 16, at most 64.
+ *   Y       (device, out) bf16 [M][N], row stride ldy (ldy % 8 == 0).
+ *   workspace, workspace_bytes: device scratch of at least
+ *           sp24_fp8_gemm_workspace_size(M, N, K, r) bytes (may be NULL when
+ *           that size is 0).
+ * Preconditions: M >= 1; N a positive multiple of 128; K a positive multiple
+ * of 128; all scales finite and > 0; device pointers 16-byte aligned.
+ * Errors: SP24_ERR_* as above; device-side wait timeouts are reported by
+ * sp24_last_device_error().
+ */
+sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
+                          const void* values, const void* meta, const float* sw, int64_t N, int gN, int gK,
+                          const void* X2, const void* W2, int64_t r, void* Y, int64_t ldy, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Device scratch bytes sp24_fp8_gemm needs for this problem (0 = none). */
+size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r);
+
+/*
+ * sp24_last_device_error -- synchronise `stream`, then read and clear the
+ * library's device error word on the current device.  Returns SP24_OK, or
+ * SP24_ERR_DEVICE_TIMEOUT if any kernel of this library gave up on a bounded
+ * wait since the last call (its results are then invalid), or SP24_ERR_CUDA.
+ */
+sp24_status sp24_last_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SP24_H */
