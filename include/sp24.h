@@ -37,6 +37,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(SP24_BUILD) && defined(__GNUC__)
+#define SP24_API __attribute__((visibility("default")))
+#else
+#define SP24_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -53,11 +59,11 @@ typedef enum {
 } sp24_status;
 
 /* Human-readable name of a status code (static string). */
-const char* sp24_status_string(sp24_status s);
+SP24_API const char* sp24_status_string(sp24_status s);
 
 /* Bytes of sparsity metadata for an N x K weight: N * K / 8 (one 4-bit
  * entry per group of four along K).  K must be a multiple of 8. */
-size_t sp24_meta_bytes(int64_t N, int64_t K);
+SP24_API size_t sp24_meta_bytes(int64_t N, int64_t K);
 
 /*
  * sp24_fp8_compress -- magnitude 2:4 prune + e4m3 quantize + pack.
@@ -83,7 +89,7 @@ size_t sp24_meta_bytes(int64_t N, int64_t K);
  * Preconditions: N >= 1; K a positive multiple of 128; N % 128 == 0 when
  * gN == 128; W, values and meta 16-byte aligned, ldw*2 a multiple of 16.
  */
-sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, int64_t ldw, int gN, int gK,
+SP24_API sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, int64_t ldw, int gN, int gK,
                               void* values, void* meta, float* scales, void* stream);
 
 /*
@@ -98,7 +104,7 @@ sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, int64_t ldw, 
  * Preconditions: M >= 1; K a positive multiple of 128; X and xq 16-byte
  * aligned; ldx*4 a multiple of 16.
  */
-sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
+SP24_API sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
                                   float* sx, void* stream);
 
 /*
@@ -126,7 +132,7 @@ sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K, int64_t 
  *   gN      1 or 128; gK: K or 128.
  *   X2, W2  (device) bf16 [M][r] and [N][r] (row stride r), or NULL with
  *           r = 0 for no side GEMM; r a multiple of 16, at most 64.
- *   Y       (device, out) bf16 [M][N], row stride ldy (ldy % 8 == 0).
+ *   Y       (device, out) bf16 [M][N], row stride ldy >= N.
  *   workspace, workspace_bytes: device scratch of at least
  *           sp24_fp8_gemm_workspace_size(M, N, K, r) bytes (may be NULL when
  *           that size is 0).
@@ -135,13 +141,13 @@ sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K, int64_t 
  * Errors: SP24_ERR_* as above; device-side wait timeouts are reported by
  * sp24_last_device_error().
  */
-sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
+SP24_API sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
                           const void* values, const void* meta, const float* sw, int64_t N, int gN, int gK,
                           const void* X2, const void* W2, int64_t r, void* Y, int64_t ldy, void* workspace,
                           size_t workspace_bytes, void* stream);
 
 /* Device scratch bytes sp24_fp8_gemm needs for this problem (0 = none). */
-size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r);
+SP24_API size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r);
 
 /*
  * sp24_last_device_error -- synchronise `stream`, then read and clear the
@@ -149,7 +155,7 @@ size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r);
  * SP24_ERR_DEVICE_TIMEOUT if any kernel of this library gave up on a bounded
  * wait since the last call (its results are then invalid), or SP24_ERR_CUDA.
  */
-sp24_status sp24_last_device_error(void* stream);
+SP24_API sp24_status sp24_last_device_error(void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,171 @@
+"""semi_structured_sparse_gb300 -- Python binding of libsp24 (2:4 sparse FP8 GEMM on GB300).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+torch supplies device memory and the current stream; the library itself never
+allocates.  There is no CPU fallback: if the library is missing or the device
+is not an sm_103 GPU, every call raises.
+
+    values, meta, sw = compress(w_bf16, gN=1, gK=None)        # prune + e4m3 + pack
+    xq, sx          = quantize_act(x_fp32, gK=None)            # per-token / 1x128 e4m3
+    y               = gemm(xq, sx, values, meta, sw, gM=1, gN=1, gK=None, x2=None, w2=None)
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+SP24_STATUS = {
+    0: "SP24_OK", 1: "SP24_ERR_INVALID_ARG", 2: "SP24_ERR_UNSUPPORTED", 3: "SP24_ERR_ALIGNMENT",
+    4: "SP24_ERR_CUDA", 5: "SP24_ERR_ARCH", 6: "SP24_ERR_WORKSPACE", 7: "SP24_ERR_DEVICE_TIMEOUT",
+}
+
+# Every entry point the C header declares, with its ctypes signature.
+_P, _I64, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "sp24_status_string": ([_I], ctypes.c_char_p),
+    "sp24_meta_bytes": ([_I64, _I64], _SZ),
+    "sp24_fp8_compress": ([_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P], _I),
+    "sp24_fp8_quantize_act": ([_P, _I64, _I64, _I64, _I, _P, _P, _P], _I),
+    "sp24_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _I64,
+                       _P, _SZ, _P], _I),
+    "sp24_fp8_gemm_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
+    "sp24_last_device_error": ([_P], _I),
+}
+
+
+class Sp24Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s" % (where, SP24_STATUS.get(status, "status %d" % status)))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libsp24.so (building it first if asked and it is absent or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError("libsp24.so is not built (run semi_structured_sparse_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        if status in (1, 2, 3):
+            raise ValueError("%s: %s" % (where, SP24_STATUS.get(status, status)))
+        raise Sp24Error(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_tensor(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.stride(-1) != 1:
+        raise ValueError("%s must have unit stride in its last dimension" % name)
+    return t
+
+
+def meta_bytes(N: int, K: int) -> int:
+    return int(load().sp24_meta_bytes(N, K))
+
+
+def compress(w: torch.Tensor, gN: int = 1, gK: int = None, out=None, stream=None):
+    """Magnitude 2:4 prune + e4m3 + pack of a bf16 weight [N, K].
+
+    Returns (values uint8 [N, K/2], meta uint8 [N, K/8], scales fp32 [K/gK, ceil(N/gN)]).
+    ``out`` may supply those three tensors (no allocation then)."""
+    lib = load()
+    _dev_tensor(w, torch.bfloat16, "w")
+    N, K = w.shape
+    gK = K if gK is None else gK
+    if out is None:
+        values = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+        meta = torch.empty((N, K // 8), dtype=torch.uint8, device=w.device)
+        scales = torch.empty((K // gK, (N + gN - 1) // gN), dtype=torch.float32, device=w.device)
+    else:
+        values, meta, scales = out
+    _check(lib.sp24_fp8_compress(_ptr(w), N, K, w.stride(0), gN, gK, _ptr(values), _ptr(meta), _ptr(scales),
+                                 _stream(stream)), "sp24_fp8_compress")
+    return values, meta, scales
+
+
+def quantize_act(x: torch.Tensor, gK: int = None, out=None, stream=None):
+    """Dynamic e4m3 quantization of fp32 activations [M, K]: returns (xq uint8 [M, K], sx fp32 [K/gK, M])."""
+    lib = load()
+    _dev_tensor(x, torch.float32, "x")
+    M, K = x.shape
+    gK = K if gK is None else gK
+    if out is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+        sx = torch.empty((K // gK, M), dtype=torch.float32, device=x.device)
+    else:
+        xq, sx = out
+    _check(lib.sp24_fp8_quantize_act(_ptr(x), M, K, x.stride(0), gK, _ptr(xq), _ptr(sx), _stream(stream)),
+           "sp24_fp8_quantize_act")
+    return xq, sx
+
+
+def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None, x2=None, w2=None,
+         out=None, workspace=None, stream=None):
+    """Y[M, N] (bf16) = scaled 2:4 sparse e4m3 GEMM of xq [M, K] with the packed weight
+    (values [N, K/2], meta [N, K/8]) plus x2 [M, r] . w2 [N, r]^T when given."""
+    lib = load()
+    _dev_tensor(xq, torch.uint8, "xq")
+    _dev_tensor(values, torch.uint8, "values")
+    _dev_tensor(meta, torch.uint8, "meta")
+    _dev_tensor(sx, torch.float32, "sx")
+    _dev_tensor(sw, torch.float32, "sw")
+    M, K = xq.shape
+    N = values.shape[0]
+    gK = K if gK is None else gK
+    r = 0
+    if x2 is not None:
+        _dev_tensor(x2, torch.bfloat16, "x2")
+        _dev_tensor(w2, torch.bfloat16, "w2")
+        r = x2.shape[1]
+        if not (x2.is_contiguous() and w2.is_contiguous()):
+            raise ValueError("x2 and w2 must be contiguous")
+    if not (sx.is_contiguous() and sw.is_contiguous() and values.is_contiguous() and meta.is_contiguous()):
+        raise ValueError("scales, values and meta must be contiguous")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if out is None else out
+    ws_bytes = int(lib.sp24_fp8_gemm_workspace_size(M, N, K, r))
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=xq.device)
+    _check(lib.sp24_fp8_gemm(_ptr(xq), _ptr(sx), M, K, xq.stride(0), gM, _ptr(values), _ptr(meta), _ptr(sw), N,
+                             gN, gK, _ptr(x2), _ptr(w2), r, _ptr(y), y.stride(0), _ptr(workspace),
+                             0 if workspace is None else workspace.numel() * workspace.element_size(),
+                             _stream(stream)), "sp24_fp8_gemm")
+    return y
+
+
+def last_device_error(stream=None):
+    """Synchronise and raise if any library kernel gave up on a bounded wait."""
+    _check(load().sp24_last_device_error(_stream(stream)), "device")

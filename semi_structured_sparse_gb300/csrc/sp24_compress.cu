@@ -1,0 +1,291 @@
+// sp24_compress.cu -- weight compression (magnitude 2:4 prune + e4m3 +
+// pack) and dynamic activation quantization.  Both are HBM-bound streaming
+// kernels: 16-byte vector loads, warp-level reductions, register-held rows,
+// one pass over the input.
+//
+// Weight path: pytorch/ao PR #3258 ("Introduce new W8A8-FP-CSR quantization
+// API", jcaip's review): drop the two smallest |w| of every group of four
+// along K, positive amax-based scale, store only the kept values and the
+// 2-bit metadata; all-zero weights are legal.  Scale granularities 1 x K,
+// 1 x 128 and 128 x 128 follow CUTLASS PR #2095 ("Improvements for:
+// Groupwise scaling along M for FP8 gemm", ScaleGranularity description).
+// Activation path: same PR #3258, the activation is divided by its scale and
+// cast to e4m3.
+#include <cuda_fp8.h>
+#include "sp24_internal.cuh"
+
+namespace sp24 {
+namespace {
+
+constexpr float kE4M3Max = 448.0f;
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint32_t to_e4m3(float x) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Scale for a block whose largest |w| has bf16 magnitude bits `amax_bits`:
+// amax / 448 (correctly rounded), or 1 when the block is all zeros.
+__device__ __forceinline__ float weight_scale(uint32_t amax_bits) {
+  return amax_bits == 0 ? 1.0f : __fdiv_rn(bf16_bits_to_float(amax_bits), kE4M3Max);
+}
+
+// Largest bf16 magnitude (sign cleared) among the 8 values of a 16-byte chunk.
+__device__ __forceinline__ uint32_t chunk_amax_bits(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = max(m, w[i] & 0x7FFFu);
+    m = max(m, (w[i] >> 16) & 0x7FFFu);
+  }
+  return m;
+}
+
+// Select, quantize and pack one group of four bf16 values (bit patterns).
+// Element j beats element i when |w_j| > |w_i|, or when they are equal and
+// j < i; the two elements beaten by fewer than two others are kept.
+// Returns the two e4m3 codes (kept in ascending position) in bits [15:0] and
+// the metadata nibble i0 | i1 << 2 in bits [19:16].
+__device__ __forceinline__ uint32_t pack_group(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3, float s) {
+  const uint32_t a0 = e0 & 0x7FFFu, a1 = e1 & 0x7FFFu, a2 = e2 & 0x7FFFu, a3 = e3 & 0x7FFFu;
+  const int c01 = a0 >= a1, c02 = a0 >= a2, c03 = a0 >= a3;
+  const int c12 = a1 >= a2, c13 = a1 >= a3, c23 = a2 >= a3;
+  const int r0 = (1 - c01) + (1 - c02) + (1 - c03);
+  const int r1 = c01 + (1 - c12) + (1 - c13);
+  const int r2 = c02 + c12 + (1 - c23);
+  const int r3 = c03 + c13 + c23;
+  const uint32_t keep = (r0 < 2 ? 1u : 0u) | (r1 < 2 ? 2u : 0u) | (r2 < 2 ? 4u : 0u) | (r3 < 2 ? 8u : 0u);
+  const uint32_t i0 = __ffs(keep) - 1;
+  const uint32_t i1 = 31 - __clz(keep);
+  const uint32_t v0 = i0 == 0 ? e0 : (i0 == 1 ? e1 : e2);
+  const uint32_t v1 = i1 == 3 ? e3 : (i1 == 2 ? e2 : e1);
+  const uint32_t q0 = to_e4m3(__fdiv_rn(bf16_bits_to_float(v0), s));
+  const uint32_t q1 = to_e4m3(__fdiv_rn(bf16_bits_to_float(v1), s));
+  return q0 | (q1 << 8) | ((i0 | (i1 << 2)) << 16);
+}
+
+// Two groups (8 bf16 in a 16-byte chunk) -> 4 value bytes and 1 meta byte.
+__device__ __forceinline__ void pack_chunk(const uint4& v, float s, uint32_t& vals, uint32_t& metab) {
+  const uint32_t g0 = pack_group(v.x & 0xFFFFu, v.x >> 16, v.y & 0xFFFFu, v.y >> 16, s);
+  const uint32_t g1 = pack_group(v.z & 0xFFFFu, v.z >> 16, v.w & 0xFFFFu, v.w >> 16, s);
+  vals = (g0 & 0xFFFFu) | ((g1 & 0xFFFFu) << 16);
+  metab = (g0 >> 16) | ((g1 >> 16) << 4);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+constexpr int kRowsPerCta = 8;   // one warp per weight row
+constexpr int kHeldChunks = 16;  // a row of up to 16 x 256 elements stays in registers
+
+// gN = 1: one warp per row.  GK128 = false: one scale per row (gK = K);
+// true: one scale per row and 128-wide K block (each half-warp owns a block).
+template <bool GK128>
+__global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __restrict__ W, int N, int K, int64_t ldw,
+                                                            uint8_t* __restrict__ values, uint8_t* __restrict__ meta,
+                                                            float* __restrict__ scales) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * kRowsPerCta + warp;
+  if (n >= N) return;
+  const uint16_t* row = W + static_cast<int64_t>(n) * ldw;
+  uint8_t* vrow = values + static_cast<int64_t>(n) * (K / 2);
+  uint8_t* mrow = meta + static_cast<int64_t>(n) * (K / 8);
+  const int nchunks = (K + 255) / 256;  // 256 elements per warp step, 8 per lane
+
+  if (!GK128) {
+    uint4 held[kHeldChunks];
+    uint32_t amax = 0;
+#pragma unroll
+    for (int c = 0; c < kHeldChunks; ++c) {
+      const int k = c * 256 + lane * 8;
+      if (c < nchunks && k < K) {
+        held[c] = ldg_stream(row + k);
+        amax = max(amax, chunk_amax_bits(held[c]));
+      }
+    }
+    for (int c = kHeldChunks; c < nchunks; ++c) {  // rows longer than 4096: stream once for amax
+      const int k = c * 256 + lane * 8;
+      if (k < K) amax = max(amax, chunk_amax_bits(ldg_stream(row + k)));
+    }
+    amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+    const float s = weight_scale(amax);
+    if (lane == 0) scales[n] = s;
+#pragma unroll
+    for (int c = 0; c < kHeldChunks; ++c) {
+      const int k = c * 256 + lane * 8;
+      if (c < nchunks && k < K) {
+        uint32_t vals, mb;
+        pack_chunk(held[c], s, vals, mb);
+        *reinterpret_cast<uint32_t*>(vrow + k / 2) = vals;
+        mrow[k / 8] = static_cast<uint8_t>(mb);
+      }
+    }
+    for (int c = kHeldChunks; c < nchunks; ++c) {
+      const int k = c * 256 + lane * 8;
+      if (k < K) {
+        uint32_t vals, mb;
+        pack_chunk(*reinterpret_cast<const uint4*>(row + k), s, vals, mb);
+        *reinterpret_cast<uint32_t*>(vrow + k / 2) = vals;
+        mrow[k / 8] = static_cast<uint8_t>(mb);
+      }
+    }
+  } else {
+    // lanes 0-15 cover K block 2c, lanes 16-31 block 2c+1 (when it exists)
+    for (int c = 0; c < nchunks; ++c) {
+      const int k = c * 256 + lane * 8;
+      const bool active = k < K;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (active) v = ldg_stream(row + k);
+      uint32_t amax = active ? chunk_amax_bits(v) : 0u;
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      const float s = weight_scale(amax);
+      if (active) {
+        if ((lane & 15) == 0) scales[static_cast<int64_t>(k / 128) * N + n] = s;
+        uint32_t vals, mb;
+        pack_chunk(v, s, vals, mb);
+        *reinterpret_cast<uint32_t*>(vrow + k / 2) = vals;
+        mrow[k / 8] = static_cast<uint8_t>(mb);
+      }
+    }
+  }
+}
+
+// gN = gK = 128: one CTA of 256 threads per 128 x 128 block.  Thread t owns
+// columns 8*(t%16) .. +7 of rows t/16 + 16*i, i = 0..7.
+__global__ void __launch_bounds__(256) compress_blocks_kernel(const uint16_t* __restrict__ W, int N, int K,
+                                                              int64_t ldw, uint8_t* __restrict__ values,
+                                                              uint8_t* __restrict__ meta,
+                                                              float* __restrict__ scales) {
+  __shared__ uint32_t warp_max[8];
+  const int kb = blockIdx.x, nb = blockIdx.y;
+  const int t = threadIdx.x, cseg = t & 15, r0 = t >> 4;
+  const int k = kb * 128 + cseg * 8;
+  uint4 v[8];
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int n = nb * 128 + r0 + 16 * i;
+    v[i] = ldg_stream(W + static_cast<int64_t>(n) * ldw + k);
+    amax = max(amax, chunk_amax_bits(v[i]));
+  }
+  amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+  if ((t & 31) == 0) warp_max[t >> 5] = amax;
+  __syncthreads();
+  amax = warp_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = max(amax, warp_max[w]);
+  const float s = weight_scale(amax);
+  if (t == 0) scales[static_cast<int64_t>(kb) * (N / 128) + nb] = s;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int n = nb * 128 + r0 + 16 * i;
+    uint32_t vals, mb;
+    pack_chunk(v[i], s, vals, mb);
+    *reinterpret_cast<uint32_t*>(values + static_cast<int64_t>(n) * (K / 2) + k / 2) = vals;
+    meta[static_cast<int64_t>(n) * (K / 8) + k / 8] = static_cast<uint8_t>(mb);
+  }
+}
+
+// Activation quantization: one warp per token row; 128 elements per warp
+// step (4 fp32 per lane).  GK128: each step is one scale block.
+template <bool GK128>
+__global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ X, int M, int K, int64_t ldx,
+                                                           uint8_t* __restrict__ xq, float* __restrict__ sx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x * 8 + warp;
+  if (m >= M) return;
+  const float* row = X + static_cast<int64_t>(m) * ldx;
+  uint8_t* qrow = xq + static_cast<int64_t>(m) * K;
+  const int nsteps = K / 128;
+  auto quant4 = [&](const float4& f, float s) -> uint32_t {
+    return to_e4m3(__fdiv_rn(f.x, s)) | (to_e4m3(__fdiv_rn(f.y, s)) << 8) | (to_e4m3(__fdiv_rn(f.z, s)) << 16) |
+           (to_e4m3(__fdiv_rn(f.w, s)) << 24);
+  };
+  auto amax4 = [](const float4& f) { return fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))); };
+  if (GK128) {
+    for (int c = 0; c < nsteps; ++c) {
+      const float4 f = *reinterpret_cast<const float4*>(row + c * 128 + lane * 4);
+      float a = amax4(f);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+      const float s = a == 0.0f ? 1.0f : __fdiv_rn(a, kE4M3Max);
+      if (lane == 0) sx[static_cast<int64_t>(c) * M + m] = s;
+      *reinterpret_cast<uint32_t*>(qrow + c * 128 + lane * 4) = quant4(f, s);
+    }
+  } else {
+    float a = 0.0f;
+    for (int c = 0; c < nsteps; ++c) a = fmaxf(a, amax4(*reinterpret_cast<const float4*>(row + c * 128 + lane * 4)));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+    const float s = a == 0.0f ? 1.0f : __fdiv_rn(a, kE4M3Max);
+    if (lane == 0) sx[m] = s;
+    for (int c = 0; c < nsteps; ++c) {
+      const float4 f = *reinterpret_cast<const float4*>(row + c * 128 + lane * 4);
+      *reinterpret_cast<uint32_t*>(qrow + c * 128 + lane * 4) = quant4(f, s);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace sp24
+
+extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, int64_t ldw, int gN, int gK,
+                                         void* values, void* meta, float* scales, void* stream) {
+  using namespace sp24;
+  if (!W || !values || !meta || !scales) return SP24_ERR_INVALID_ARG;
+  if (N < 1 || K < 128 || K % 128 != 0 || ldw < K || N > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
+  const bool per_channel = (gN == 1 && gK == K);
+  const bool row_k128 = (gN == 1 && gK == 128);
+  const bool block128 = (gN == 128 && gK == 128);
+  if (!per_channel && !row_k128 && !block128) return SP24_ERR_UNSUPPORTED;
+  if (block128 && N % 128 != 0) return SP24_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(values) || !aligned16(meta) || (ldw * 2) % 16 != 0) return SP24_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(scales) % 4 != 0) return SP24_ERR_ALIGNMENT;
+  const DeviceInfo* dev = nullptr;
+  sp24_status st = current_device(&dev);
+  if (st != SP24_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t* w = static_cast<const uint16_t*>(W);
+  uint8_t* v = static_cast<uint8_t*>(values);
+  uint8_t* m = static_cast<uint8_t*>(meta);
+  if (block128) {
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+    if (grid.y > 65535u) return SP24_ERR_UNSUPPORTED;
+    compress_blocks_kernel<<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
+  } else {
+    const unsigned grid = static_cast<unsigned>((N + kRowsPerCta - 1) / kRowsPerCta);
+    if (per_channel)
+      compress_rows_kernel<false><<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
+    else
+      compress_rows_kernel<true><<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
+  }
+  return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+}
+
+extern "C" sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
+                                             float* sx, void* stream) {
+  using namespace sp24;
+  if (!X || !xq || !sx) return SP24_ERR_INVALID_ARG;
+  if (M < 1 || K < 128 || K % 128 != 0 || ldx < K || M > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
+  if (gK != K && gK != 128) return SP24_ERR_UNSUPPORTED;
+  if (!aligned16(X) || !aligned16(xq) || (ldx * 4) % 16 != 0) return SP24_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(sx) % 4 != 0) return SP24_ERR_ALIGNMENT;
+  const DeviceInfo* dev = nullptr;
+  sp24_status st = current_device(&dev);
+  if (st != SP24_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>((M + 7) / 8);
+  if (gK == 128)
+    quantize_act_kernel<true><<<grid, 256, 0, s>>>(X, (int)M, (int)K, ldx, static_cast<uint8_t*>(xq), sx);
+  else
+    quantize_act_kernel<false><<<grid, 256, 0, s>>>(X, (int)M, (int)K, ldx, static_cast<uint8_t*>(xq), sx);
+  return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+}

@@ -1,0 +1,501 @@
+// sp24_gemm.cu -- 2:4 sparse e4m3 GEMM with group-wise scaling and an
+// optional fused bf16 side GEMM, for sm_103a.
+//
+// Math (user view):  Y[m][n] = bf16( sum_kb sx[kb][m/gM] sw[kb][n/gN] P_kb[m][n]
+//                                    + sum_j X2[m][j] W2[n][j] ).
+// The kernel computes the transposed product Y^T = W . X^T so that the
+// sparse weight is the row-major sparse A operand of the tensor core and the
+// token-major activations are the K-major B operand (CUTLASS issue #2029,
+// klevzoff's swap+transpose answer); a weight row is a TMEM lane and a token
+// is a TMEM column.  Row-major Y is column-major Y^T, so nothing is moved.
+//
+// Structure (one persistent CTA per SM, 6 warps):
+//   warp 0      TMA producer: per 128-wide K step, the kept-value tile
+//               (128 rows x 64 B, 64-byte swizzle), the metadata tile
+//               (128 rows x 16 B) and the activation tile (BN rows x 128 B,
+//               128-byte swizzle) into one stage of a shared-memory ring.
+//   warp 1      TMEM allocation and the single-thread MMA issuer: copies the
+//               stage's metadata into TMEM (tcgen05.cp, lane = weight row)
+//               and issues two sparse tcgen05.mma (K = 64 each) per stage.
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, scale, add the
+//               side accumulator, round to bf16, predicated stores.
+// Scale promotion (gK = 128, CUTLASS PR #2095's per-K-tile promotion): every
+// 128-wide K step is its own scale block, so each stage's partial product
+// lands in its own TMEM buffer (ring of NACC) and the epilogue folds it into
+// register accumulators with sx * sw while the tensor core fills the next.
+// Partial token tiles: TMA zero-fills rows past M and the epilogue skips them
+// (PR #2095, predication of partial tiles).
+// Side GEMM (CUTLASS issue #2058, Y = X1 W1^T + X2 W2^T in one kernel): after
+// the sparse K loop the MMA thread issues bf16 tcgen05.mma over r <= 64 into
+// a second accumulator that the epilogue adds after scaling.
+#include <cuda_bf16.h>
+#include "sp24_internal.cuh"
+#include "sp24_ptx.cuh"
+
+namespace sp24 {
+namespace {
+
+constexpr int BM = 128;                // weight rows per tile (MMA M)
+constexpr int BK = 128;                // logical K per stage (two sparse MMAs of K = 64)
+constexpr int A_STAGE = BM * BK / 2;   // kept values: 8 KB
+constexpr int META_STAGE = BM * BK / 8;  // metadata: 2 KB
+constexpr int META_COL0 = 448;         // TMEM columns 448..511: metadata ring
+constexpr int META_SLOTS = 16;         // 4 columns each
+constexpr int MAX_STAGES = 16;
+constexpr int NUM_THREADS = 192;
+constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr int BAR_BYTES = 1024;
+
+template <int BN, bool PROMOTE, bool SIDE>
+struct Cfg {
+  static constexpr int B_STAGE = BN * BK;  // e4m3 activations, 128 B per token row
+  static constexpr int STAGE = A_STAGE + META_STAGE + B_STAGE;
+  static constexpr int SIDE_BYTES = SIDE ? (BM * 128 + BN * 128) : 0;
+  static constexpr int NACC = (PROMOTE && !SIDE && 3 * BN <= META_COL0) ? 3 : 2;
+  static constexpr int CS_BYTES = PROMOTE ? 2 * BN * 4 : 0;
+  static constexpr int FIXED = 1024 + SIDE_BYTES + CS_BYTES + BAR_BYTES;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
+  static constexpr int SMEM = FIXED + STAGES * STAGE;
+  static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(STAGES >= 2, "need at least two stages");
+  static_assert(NACC * BN + (SIDE ? BN : 0) <= META_COL0, "TMEM columns");
+  static_assert(STAGES <= META_SLOTS, "metadata ring must cover the stage ring");
+};
+
+struct GemmArgs {
+  const float* sx;
+  const float* sw;
+  __nv_bfloat16* Y;
+  int64_t ldy;
+  int M, N, K;
+  int ldsx, ldsw;       // row strides (floats) of the scale tensors
+  int gM_shift, gN_shift;  // log2 of the granularities (0 or 7)
+  int m_tiles, n_tiles, k_tiles;
+  int side_ksteps;      // r / 16
+  unsigned int* err;
+};
+
+// Barrier over the 128 epilogue threads (named barrier 1) that also ORs a
+// predicate across them, so that a give-up decision is taken by all or none.
+__device__ __forceinline__ bool epilogue_bar_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+template <int BN, bool PROMOTE, bool SIDE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    sp24_gemm_kernel(const __grid_constant__ CUtensorMap tm_vals, const __grid_constant__ CUtensorMap tm_meta,
+                     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w2,
+                     const __grid_constant__ CUtensorMap tm_x2, const GemmArgs p) {
+  using C = Cfg<BN, PROMOTE, SIDE>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int NACC = C::NACC;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = sm;
+  uint8_t* side_w2 = sm + STAGES * C::STAGE;
+  uint8_t* side_x2 = side_w2 + BM * 128;
+  float* cs = reinterpret_cast<float*>(sm + STAGES * C::STAGE + C::SIDE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + STAGES * C::STAGE + C::SIDE_BYTES + C::CS_BYTES);
+  uint64_t* full = bars;                  // [STAGES] TMA -> MMA
+  uint64_t* empty = bars + MAX_STAGES;    // [STAGES] MMA -> TMA
+  uint64_t* accf = bars + 2 * MAX_STAGES; // [NACC]  MMA -> epilogue
+  uint64_t* acce = accf + 3;              // [NACC]  epilogue -> MMA
+  uint64_t* sidef = acce + 3;             // side operands loaded
+  uint64_t* sidee = sidef + 1;            // side operands consumed
+  uint64_t* saccf = sidee + 1;            // side accumulator ready
+  uint64_t* sacce = saccf + 1;            // side accumulator drained
+  uint64_t* drain = sacce + 1;            // MMA drain on abort
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(&accf[i], 1);
+      mbar_init(&acce[i], 128);
+    }
+    mbar_init(sidef, 1);
+    mbar_init(sidee, 1);
+    mbar_init(saccf, 1);
+    mbar_init(sacce, 128);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_vals);
+    tma_prefetch_desc(&tm_meta);
+    tma_prefetch_desc(&tm_x);
+    if (SIDE) {
+      tma_prefetch_desc(&tm_w2);
+      tma_prefetch_desc(&tm_x2);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const int num_tiles = p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, side_phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int n0 = (tile % p.n_tiles) * BM;
+        const int m0 = (tile / p.n_tiles) * BN;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
+          uint8_t* sA = ring + stage * C::STAGE;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE);
+          tma_load_2d(sA, &tm_vals, &full[stage], kt * (BK / 2), n0);
+          tma_load_2d(sA + A_STAGE, &tm_meta, &full[stage], kt * (BK / 8), n0);
+          tma_load_2d(sA + A_STAGE + META_STAGE, &tm_x, &full[stage], kt * BK, m0);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (SIDE && ok) {
+          if (!mbar_wait(sidee, side_phase ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(sidef, BM * 128 + BN * 128);
+          tma_load_2d(side_w2, &tm_w2, sidef, 0, n0);
+          tma_load_2d(side_x2, &tm_x2, sidef, 0, m0);
+          side_phase ^= 1;
+        }
+      }
+      if (!ok) {
+        atomicOr(p.err, DEVERR_TIMEOUT_PRODUCER);
+        // let every load already issued land before the CTA's shared memory goes away
+        const int64_t first = issued > STAGES ? issued - STAGES : 0;
+        for (int64_t i = first; i < issued; ++i)
+          (void)mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_sp = idesc_e4m3(BM, BN, true);
+      constexpr uint32_t idesc_side = idesc_bf16(BM, BN);
+      uint32_t stage = 0, phase = 0, side_cnt = 0, meta_ctr = 0;
+      uint32_t acc_cnt = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        uint32_t d = 0;
+        if (!PROMOTE) {
+          const uint32_t b = acc_cnt % NACC;
+          if (!mbar_wait(&acce[b], ((acc_cnt / NACC) & 1) ^ 1)) { ok = false; break; }
+          tc_fence_after();
+          d = tbase + b * BN;
+        }
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          uint32_t b = 0;
+          if (PROMOTE) {
+            b = acc_cnt % NACC;
+            if (!mbar_wait(&acce[b], ((acc_cnt / NACC) & 1) ^ 1)) { ok = false; break; }
+            tc_fence_after();
+            d = tbase + b * BN;
+          }
+          if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(ring + stage * C::STAGE);
+          const uint32_t sMeta = sA + A_STAGE;
+          const uint32_t sB = sMeta + META_STAGE;
+          const uint32_t mcol = tbase + META_COL0 + 4 * (meta_ctr % META_SLOTS);
+          ++meta_ctr;
+          tmem_cp_128x128b(mcol, smem_desc(sMeta, 128, 128, SWZ_NONE));
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint64_t da = smem_desc(sA + 32 * j, 16, 512, SWZ_64B);
+            const uint64_t db = smem_desc(sB + 64 * j, 16, 1024, SWZ_128B);
+            const uint32_t accumulate = PROMOTE ? (j > 0) : ((kt | j) != 0);
+            mma_sp_e4m3(d, da, db, mcol + 2 * j, idesc_sp, accumulate);
+          }
+          mma_commit(&empty[stage]);
+          if (PROMOTE) {
+            mma_commit(&accf[b]);
+            ++acc_cnt;
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        if (SIDE) {
+          if (!mbar_wait(sacce, (side_cnt & 1) ^ 1)) { ok = false; break; }
+          if (!mbar_wait(sidef, side_cnt & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ds = tbase + NACC * BN;
+          for (int j = 0; j < p.side_ksteps; ++j) {
+            const uint64_t da = smem_desc(smem_u32(side_w2) + 32 * j, 16, 1024, SWZ_128B);
+            const uint64_t db = smem_desc(smem_u32(side_x2) + 32 * j, 16, 1024, SWZ_128B);
+            mma_bf16(ds, da, db, idesc_side, j > 0);
+          }
+          mma_commit(sidee);
+          mma_commit(saccf);
+          ++side_cnt;
+        }
+        if (!PROMOTE) {
+          mma_commit(&accf[acc_cnt % NACC]);
+          ++acc_cnt;
+        }
+      }
+      if (!ok) {
+        atomicOr(p.err, DEVERR_TIMEOUT_MMA);
+        mma_commit(drain);  // every MMA issued so far must finish before TMEM is freed
+        (void)mbar_wait(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int row = 32 * q + lane;           // weight row within the tile
+    const int et = threadIdx.x - 64;         // 0..127 within the epilogue warps
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(32 * q) << 16);
+    uint32_t acc_cnt = 0, side_cnt = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const int n0 = (tile % p.n_tiles) * BM;
+      const int m0 = (tile / p.n_tiles) * BN;
+      const int n = n0 + row;
+      if (!PROMOTE) {
+        const uint32_t b = acc_cnt % NACC;
+        if (!mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) { ok = false; break; }
+        if (SIDE && !mbar_wait(saccf, side_cnt & 1)) { ok = false; break; }
+        tc_fence_after();
+        const float swr = __ldg(&p.sw[n >> p.gN_shift]);
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          uint32_t v[16], s2[16];
+          tmem_ld16(lane_base + b * BN + 16 * c, v);
+          if (SIDE) tmem_ld16(lane_base + NACC * BN + 16 * c, s2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + 16 * c + j;
+            if (m < p.M) {
+              const float s = __ldg(&p.sx[m >> p.gM_shift]) * swr;
+              const float y = SIDE ? fmaf(s, __uint_as_float(v[j]), __uint_as_float(s2[j]))
+                                   : s * __uint_as_float(v[j]);
+              p.Y[static_cast<int64_t>(m) * p.ldy + n] = __float2bfloat16_rn(y);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acce[b]);
+        ++acc_cnt;
+        if (SIDE) {
+          mbar_arrive(sacce);
+          ++side_cnt;
+        }
+      } else {
+        float acc[BN];
+#pragma unroll
+        for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+        const bool per_row_w = p.gN_shift == 0;  // gN = 1: weight scale varies by row
+        // column scale for K block kt: sx (x sw when the weight scale is uniform over the tile)
+        auto col_scale = [&](int kt) -> float {
+          const int m = m0 + et;
+          if (et >= BN || m >= p.M) return 0.0f;
+          float s = __ldg(&p.sx[static_cast<int64_t>(kt) * p.ldsx + (m >> p.gM_shift)]);
+          if (!per_row_w) s *= __ldg(&p.sw[static_cast<int64_t>(kt) * p.ldsw + (n0 >> p.gN_shift)]);
+          return s;
+        };
+        float cs_next = col_scale(0);
+        float rowf_next = per_row_w ? __ldg(&p.sw[n]) : 1.0f;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          float* csb = cs + (kt & 1) * BN;
+          if (et < BN) csb[et] = cs_next;
+          const float rowf = rowf_next;
+          if (epilogue_bar_any(!ok)) { ok = false; break; }
+          if (kt + 1 < p.k_tiles) {
+            cs_next = col_scale(kt + 1);
+            if (per_row_w) rowf_next = __ldg(&p.sw[static_cast<int64_t>(kt + 1) * p.ldsw + n]);
+          }
+          const uint32_t b = acc_cnt % NACC;
+          if (!mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) { ok = false; continue; }  // decided at the next barrier
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < BN / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld16(lane_base + b * BN + 16 * c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+              const float4 s4 = *reinterpret_cast<const float4*>(csb + 16 * c + 4 * j4);
+              const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const float s = per_row_w ? sc[t] * rowf : sc[t];
+                acc[16 * c + 4 * j4 + t] = fmaf(s, __uint_as_float(v[4 * j4 + t]), acc[16 * c + 4 * j4 + t]);
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&acce[b]);
+          ++acc_cnt;
+        }
+        if (epilogue_bar_any(!ok)) { ok = false; break; }
+        if (SIDE) {
+          if (!mbar_wait(saccf, side_cnt & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < BN / 16; ++c) {
+            uint32_t s2[16];
+            tmem_ld16(lane_base + NACC * BN + 16 * c, s2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[16 * c + j] += __uint_as_float(s2[j]);
+          }
+          tc_fence_before();
+          mbar_arrive(sacce);
+          ++side_cnt;
+        }
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const int m = m0 + i;
+          if (m < p.M) p.Y[static_cast<int64_t>(m) * p.ldy + n] = __float2bfloat16_rn(acc[i]);
+        }
+      }
+    }
+    if (!ok) atomicOr(p.err, DEVERR_TIMEOUT_EPILOGUE);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int BN, bool PROMOTE, bool SIDE>
+sp24_status launch(const DeviceInfo* dev, const CUtensorMap& a, const CUtensorMap& m, const CUtensorMap& x,
+                   const CUtensorMap& w2, const CUtensorMap& x2, const GemmArgs& args, cudaStream_t stream) {
+  using C = Cfg<BN, PROMOTE, SIDE>;
+  auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE>;
+  static bool attr_done[64] = {};
+  if (!attr_done[dev->ordinal]) {
+    if (static_cast<size_t>(C::SMEM) > dev->smem_optin) return SP24_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+      return SP24_ERR_CUDA;
+    attr_done[dev->ordinal] = true;
+  }
+  const int tiles = args.m_tiles * args.n_tiles;
+  const int grid = tiles < dev->sm_count ? tiles : dev->sm_count;
+  kern<<<grid, NUM_THREADS, C::SMEM, stream>>>(a, m, x, w2, x2, args);
+  return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+}
+
+template <bool PROMOTE, bool SIDE>
+sp24_status launch_bn(int bn, const DeviceInfo* dev, const CUtensorMap& a, const CUtensorMap& m,
+                      const CUtensorMap& x, const CUtensorMap& w2, const CUtensorMap& x2, const GemmArgs& args,
+                      cudaStream_t s) {
+  switch (bn) {
+    case 16: return launch<16, PROMOTE, SIDE>(dev, a, m, x, w2, x2, args, s);
+    case 32: return launch<32, PROMOTE, SIDE>(dev, a, m, x, w2, x2, args, s);
+    case 64: return launch<64, PROMOTE, SIDE>(dev, a, m, x, w2, x2, args, s);
+    default: return launch<128, PROMOTE, SIDE>(dev, a, m, x, w2, x2, args, s);
+  }
+}
+
+int pick_bn(int64_t M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  return 128;
+}
+
+}  // namespace
+}  // namespace sp24
+
+extern "C" size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r) {
+  (void)M; (void)N; (void)K; (void)r;
+  return 0;
+}
+
+extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
+                                     const void* values, const void* meta, const float* sw, int64_t N, int gN,
+                                     int gK, const void* X2, const void* W2, int64_t r, void* Y, int64_t ldy,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  using namespace sp24;
+  (void)workspace; (void)workspace_bytes;
+  if (!Xq || !sx || !values || !meta || !sw || !Y) return SP24_ERR_INVALID_ARG;
+  if (M < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0) return SP24_ERR_INVALID_ARG;
+  if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
+  if (ldx < K || ldy < N) return SP24_ERR_INVALID_ARG;
+  if ((gM != 1 && gM != 128) || (gN != 1 && gN != 128) || (gK != K && gK != 128)) return SP24_ERR_UNSUPPORTED;
+  if (r < 0) return SP24_ERR_INVALID_ARG;
+  const bool side = r > 0;
+  if (side) {
+    if (!X2 || !W2) return SP24_ERR_INVALID_ARG;
+    if (r % 16 != 0 || r > 64) return SP24_ERR_UNSUPPORTED;
+    if (!aligned16(X2) || !aligned16(W2)) return SP24_ERR_ALIGNMENT;
+  }
+  if (!aligned16(Xq) || !aligned16(values) || !aligned16(meta) || ldx % 16 != 0) return SP24_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(sx) | reinterpret_cast<uintptr_t>(sw)) % 4 != 0 ||
+      reinterpret_cast<uintptr_t>(Y) % 2 != 0)
+    return SP24_ERR_ALIGNMENT;
+  const DeviceInfo* dev = nullptr;
+  sp24_status st = current_device(&dev);
+  if (st != SP24_OK) return st;
+
+  const int bn = pick_bn(M);
+  CUtensorMap tm_a, tm_m, tm_x, tm_w2, tm_x2;
+  st = make_tmap_2d(&tm_a, values, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, BK / 2, BM,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+  if (st == SP24_OK)
+    st = make_tmap_2d(&tm_m, meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 8, N, K / 8, BK / 8, BM,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st == SP24_OK)
+    st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == SP24_OK && side) {
+    st = make_tmap_2d(&tm_w2, W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, N, r * 2, 64, BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == SP24_OK)
+      st = make_tmap_2d(&tm_x2, X2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, M, r * 2, 64, bn,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    tm_w2 = tm_a;
+    tm_x2 = tm_a;
+  }
+  if (st != SP24_OK) return st;
+
+  GemmArgs a;
+  a.sx = sx;
+  a.sw = sw;
+  a.Y = static_cast<__nv_bfloat16*>(Y);
+  a.ldy = ldy;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.ldsx = static_cast<int>((M + gM - 1) / gM);
+  a.ldsw = static_cast<int>((N + gN - 1) / gN);
+  a.gM_shift = gM == 128 ? 7 : 0;
+  a.gN_shift = gN == 128 ? 7 : 0;
+  a.m_tiles = static_cast<int>((M + bn - 1) / bn);
+  a.n_tiles = static_cast<int>(N / BM);
+  a.k_tiles = static_cast<int>(K / BK);
+  a.side_ksteps = static_cast<int>(r / 16);
+  a.err = dev->err_word;
+  if (static_cast<int64_t>(a.m_tiles) * a.n_tiles > (1 << 30)) return SP24_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool promote = (gK == 128 && K != 128);
+  if (promote)
+    return side ? launch_bn<true, true>(bn, dev, tm_a, tm_m, tm_x, tm_w2, tm_x2, a, s)
+                : launch_bn<true, false>(bn, dev, tm_a, tm_m, tm_x, tm_w2, tm_x2, a, s);
+  return side ? launch_bn<false, true>(bn, dev, tm_a, tm_m, tm_x, tm_w2, tm_x2, a, s)
+              : launch_bn<false, false>(bn, dev, tm_a, tm_m, tm_x, tm_w2, tm_x2, a, s);
+}

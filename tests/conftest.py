@@ -17,3 +17,14 @@ def ora():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def sp24():
+    """The CUDA path (built in-tree); GPU tests only."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import semi_structured_sparse_gb300 as s
+    s.load()
+    return s

@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every symbol include/sp24.h declares, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sp24.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import semi_structured_sparse_gb300 as s
+    return s.load()
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"SP24_API\s+[\w\s\*]*?\b(sp24_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("sp24_fp8_compress", "sp24_fp8_gemm", "sp24_fp8_quantize_act",
+                     "sp24_fp8_gemm_workspace_size", "sp24_meta_bytes", "sp24_status_string",
+                     "sp24_last_device_error"):
+        assert required in names
+
+
+def test_exports_every_declared_symbol(lib):
+    import semi_structured_sparse_gb300 as s
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in s.SIGNATURES, name
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.sp24_status_string(code).startswith(b"SP24_")
+    assert lib.sp24_status_string(99) == b"SP24_ERR_UNKNOWN"
+
+
+def test_meta_bytes(lib):
+    assert lib.sp24_meta_bytes(4096, 4096) == 4096 * 512
+    assert lib.sp24_meta_bytes(1, 8) == 1
+    assert lib.sp24_meta_bytes(0, 128) == 0
+    assert lib.sp24_meta_bytes(4, 12) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+FAKE_ODD = ctypes.c_void_p(0x10008)  # 8-byte aligned only
+
+
+def test_compress_argument_errors(lib):
+    f = lib.sp24_fp8_compress
+    ok = dict(W=FAKE, N=256, K=512, ldw=512, gN=1, gK=512, v=FAKE, m=FAKE, s=FAKE)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["W"], a["N"], a["K"], a["ldw"], a["gN"], a["gK"], a["v"], a["m"], a["s"], None)
+
+    assert call(W=None) == 1
+    assert call(v=None) == 1
+    assert call(N=0) == 1
+    assert call(K=100) == 1          # not a multiple of 128
+    assert call(ldw=256) == 1        # stride shorter than a row
+    assert call(gN=2) == 2
+    assert call(gN=128, gK=512) == 2
+    assert call(gN=128, gK=128, N=200) == 1
+    assert call(W=FAKE_ODD) == 3
+    assert call(ldw=516) == 3        # row stride not 16-byte aligned
+
+
+def test_gemm_argument_errors(lib):
+    f = lib.sp24_fp8_gemm
+    ok = dict(X=FAKE, sx=FAKE, M=64, K=512, ldx=512, gM=1, v=FAKE, m=FAKE, sw=FAKE, N=256, gN=1, gK=512,
+              X2=None, W2=None, r=0, Y=FAKE, ldy=256)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["X"], a["sx"], a["M"], a["K"], a["ldx"], a["gM"], a["v"], a["m"], a["sw"], a["N"], a["gN"],
+                 a["gK"], a["X2"], a["W2"], a["r"], a["Y"], a["ldy"], None, 0, None)
+
+    assert call(X=None) == 1
+    assert call(Y=None) == 1
+    assert call(M=0) == 1
+    assert call(N=200) == 1           # N must be a multiple of 128
+    assert call(K=200) == 1
+    assert call(ldx=256) == 1
+    assert call(ldy=128) == 1
+    assert call(gM=2) == 2
+    assert call(gK=256) == 2
+    assert call(r=64) == 1            # side rank without operands
+    assert call(r=24, X2=FAKE, W2=FAKE) == 2
+    assert call(r=128, X2=FAKE, W2=FAKE) == 2
+    assert call(X=FAKE_ODD) == 3
+    assert call(ldx=520) == 3
+
+
+def test_quantize_argument_errors(lib):
+    f = lib.sp24_fp8_quantize_act
+    assert f(None, 4, 128, 128, 128, FAKE, FAKE, None) == 1
+    assert f(FAKE, 4, 100, 128, 128, FAKE, FAKE, None) == 1
+    assert f(FAKE, 4, 256, 256, 64, FAKE, FAKE, None) == 2
+    assert f(FAKE_ODD, 4, 256, 256, 128, FAKE, FAKE, None) == 3
+
+
+def test_workspace_size(lib):
+    assert lib.sp24_fp8_gemm_workspace_size(2048, 4096, 4096, 0) >= 0
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The binding never routes through the oracle or a CPU implementation."""
+    pkg = os.path.join(ROOT, "semi_structured_sparse_gb300", "__init__.py")
+    txt = open(pkg).read()
+    assert "import oracle" not in txt and "from oracle" not in txt
+    assert "import numpy" not in txt

@@ -1,0 +1,114 @@
+"""GPU parity of the weight compression and the activation quantization:
+bit-exact against the CPU oracle (values, metadata and scales), through the
+C ABI, on every workload's weight at full size."""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+from gpu_util import dev, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _compress_both(ora, sp24, Wt, gN, gK):
+    Wb = inputs.bf16_bits(Wt)
+    ov, om, os_ = ora.compress(Wb, gN, gK)
+    gv, gm, gs = sp24.compress(dev(Wb), gN, gK)
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    return (ov, om, os_), (host_bits(gv), host_bits(gm), host_bits(gs))
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama", "groupwise", "decode"])
+def test_compress_bit_exact_full_size(ora, sp24, name):
+    w = inputs.WORKLOADS[name]
+    _, W, _, _ = inputs.generate(inputs.with_shape(w, M=1))
+    (ov, om, os_), (gv, gm, gs) = _compress_both(ora, sp24, W, w.gN, w.gk)
+    assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32)), "scales"
+    assert np.array_equal(gm, om), "metadata"
+    assert np.array_equal(gv, ov), "values"
+
+
+@pytest.mark.parametrize("gN,gK", [(1, None), (1, 128), (128, 128)])
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (384, 4352), (8, 640)])
+def test_compress_ragged_shapes(ora, sp24, N, K, gN, gK):
+    if gN == 128 and N % 128:
+        pytest.skip("block scales need N % 128 == 0")
+    _, W, _, _ = inputs.generate(inputs.Workload("t", 1, N, K, seed=N + K))
+    (ov, om, os_), (gv, gm, gs) = _compress_both(ora, sp24, W, gN, K if gK is None else gK)
+    assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(gm, om)
+    assert np.array_equal(gv, ov)
+
+
+def test_compress_edge_values(ora, sp24):
+    """Ties, signed zeros, an all-zero row, subnormal bf16 and huge values."""
+    N, K = 128, 256
+    rng = np.random.default_rng(5)
+    vals = np.array([0.0, -0.0, 1.0, -1.0, 2.0, 1e-38, -3e-39, 3e38, -1.5, 0.5], dtype=np.float32)
+    W = torch.from_numpy(rng.choice(vals, size=(N, K)).astype(np.float32)).to(torch.bfloat16)
+    W[3] = 0.0          # all-zero row: scale 1, codes 0
+    W[4] = -0.0
+    W[5, :] = 7.0       # all ties
+    (ov, om, os_), (gv, gm, gs) = _compress_both(ora, sp24, W, 1, K)
+    assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(gm, om)
+    assert np.array_equal(gv, ov)
+    assert gs[0, 3] == 1.0 and (gv[3] == 0).all()
+
+
+def test_compress_all_zero_weight(ora, sp24):
+    W = torch.zeros((256, 512), dtype=torch.bfloat16)
+    for gN, gK in [(1, 512), (1, 128), (128, 128)]:
+        (ov, om, os_), (gv, gm, gs) = _compress_both(ora, sp24, W, gN, gK)
+        assert (gs == 1.0).all() and (gv == 0).all() and (gm == 0x44).all()
+
+
+def test_compress_strided_input(ora, sp24):
+    """Row stride larger than K (a view into a wider weight)."""
+    _, Wbig, _, _ = inputs.generate(inputs.Workload("t", 1, 256, 1024, seed=12))
+    W = Wbig[:, :512]
+    Wd = dev(inputs.bf16_bits(Wbig))[:, :512]
+    gv, gm, gs = sp24.compress(Wd, 1, 512)
+    ov, om, os_ = ora.compress(inputs.bf16_bits(W), 1, 512)
+    assert np.array_equal(host_bits(gv), ov) and np.array_equal(host_bits(gm), om)
+
+
+@pytest.mark.parametrize("gK", [None, 128])
+@pytest.mark.parametrize("name", ["tiny", "llama", "groupwise"])
+def test_quantize_act_bit_exact(ora, sp24, name, gK):
+    w = inputs.WORKLOADS[name]
+    X, _, _, _ = inputs.generate(inputs.with_shape(w, N=8))
+    gk = w.K if gK is None else gK
+    oq, osx = ora.quantize_act(X.numpy(), gk)
+    gq, gsx = sp24.quantize_act(dev(X.numpy()), gk)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(gsx).view(np.uint32), osx.view(np.uint32))
+    assert np.array_equal(host_bits(gq), oq)
+
+
+def test_e4m3_rounding_boundaries_on_gpu(ora, sp24):
+    """Rows whose amax is 448 have scale exactly 1, so the GPU's e4m3 cast is
+    seen directly: every code value, every midpoint and one ulp either side,
+    both signs, must round as the oracle's encoder does."""
+    q = np.arange(0x7F, dtype=np.uint8)
+    v = ora.e4m3_decode(q).astype(np.float32)
+    mids = ((v[:-1].astype(np.float64) + v[1:]) / 2).astype(np.float32)
+    pts = np.concatenate([v, mids])
+    pts = np.concatenate([pts, np.nextafter(pts, np.float32(np.inf)), np.nextafter(pts, np.float32(-np.inf))])
+    pts = pts[(np.abs(pts) <= 448)]
+    pts = np.concatenate([pts, -pts])
+    K = 128
+    per_row = K - 1
+    rows = (pts.size + per_row - 1) // per_row
+    X = np.zeros((rows, K), dtype=np.float32)
+    flat = np.zeros(rows * per_row, dtype=np.float32)
+    flat[:pts.size] = pts
+    X[:, 1:] = flat.reshape(rows, per_row)
+    X[:, 0] = 448.0
+    oq, osx = ora.quantize_act(X, K)
+    gq, gsx = sp24.quantize_act(dev(X), K)
+    torch.cuda.synchronize()
+    assert (osx == 1.0).all()
+    assert np.array_equal(host_bits(gq), oq)

@@ -1,0 +1,181 @@
+"""GPU parity of the 2:4 sparse FP8 GEMM against the CPU oracle, through the C ABI.
+
+Inputs are the seeded synthetic workloads; both sides consume the same bytes
+(the oracle's compression and activation quantization).  Tolerance, element by
+element: |Y - ref| <= 1e-2 |ref| + 1e-3 with ref the oracle's fp32-accumulated
+result (the bf16 output rounding alone is <= 2^-9 |ref|).
+
+Small cases cover every output element (several tiles, ragged token tails,
+every granularity); the full-size workloads, run in the same launch
+configuration the benchmark times, are checked on sampled token rows that the
+oracle computes one by one (first, last, tile edges).
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+from gpu_util import assert_close, bf16_to_f64, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _prep(ora, w: inputs.Workload):
+    X, W, X2, W2 = inputs.generate(w)
+    gk = w.gk
+    xq, sx = ora.quantize_act(X.numpy(), gk)
+    if w.gM != 1:  # coarser activation scales are caller-supplied: any positive values
+        rng = np.random.default_rng(w.seed)
+        sx = rng.uniform(0.001, 0.01, (w.K // gk, (w.M + w.gM - 1) // w.gM)).astype(np.float32)
+    values, meta, sw = ora.compress(inputs.bf16_bits(W), w.gN, gk)
+    x2 = inputs.bf16_bits(X2) if w.r else None
+    w2 = inputs.bf16_bits(W2) if w.r else None
+    return xq, sx, values, meta, sw, x2, w2
+
+
+def _run_gpu(sp24, w, xq, sx, values, meta, sw, x2, w2):
+    y = sp24.gemm(dev(xq), dev(sx), dev(values), dev(meta), dev(sw), w.gM, w.gN, w.gk,
+                  None if x2 is None else dev(x2), None if w2 is None else dev(w2))
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    return bf16_to_f64(y)
+
+
+def _check_full(ora, sp24, w, what):
+    xq, sx, values, meta, sw, x2, w2 = _prep(ora, w)
+    y = _run_gpu(sp24, w, xq, sx, values, meta, sw, x2, w2)
+    ref = ora.gemm(xq, sx, values, meta, sw, w.gM, w.gN, w.gk, x2, w2)
+    assert_close(y, ref, what)
+    return y, ref
+
+
+def test_tiny_workload(ora, sp24):
+    w = inputs.WORKLOADS["tiny"]
+    y, ref = _check_full(ora, sp24, w, "tiny")
+    assert np.abs(ref).max() > 0.1  # the comparison is not vacuous
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 32, 33, 64, 65, 128, 129, 300])
+def test_token_counts_per_channel(ora, sp24, M):
+    w = inputs.Workload("pc", M, 384, 512, seed=100 + M)
+    _check_full(ora, sp24, w, "M=%d" % M)
+
+
+@pytest.mark.parametrize("gM,gN,gK", [(1, 128, 128), (1, 1, 128), (128, 128, 128), (128, 1, None),
+                                       (1, 128, None), (128, 1, 128)])
+@pytest.mark.parametrize("M", [5, 130, 300])
+def test_granularities(ora, sp24, gM, gN, gK, M):
+    w = inputs.Workload("g", M, 384, 768, gM=gM, gN=gN, gK=gK, seed=7 * M + gM + gN)
+    _check_full(ora, sp24, w, "g=(%d,%d,%s) M=%d" % (gM, gN, gK, M))
+
+
+@pytest.mark.parametrize("r", [16, 32, 64])
+@pytest.mark.parametrize("M,gK", [(40, None), (200, None), (130, 128)])
+def test_side_gemm(ora, sp24, r, M, gK):
+    w = inputs.Workload("side", M, 256, 512, gK=gK, r=r, seed=r + M)
+    _check_full(ora, sp24, w, "side r=%d M=%d" % (r, M))
+
+
+def test_k_equals_128(ora, sp24):
+    _check_full(ora, sp24, inputs.Workload("k128", 70, 128, 128, seed=3), "K=128")
+    _check_full(ora, sp24, inputs.Workload("k128g", 70, 128, 128, gN=128, gK=128, seed=4), "K=128 gK=128")
+
+
+def test_identity_dequantize(ora, sp24):
+    """X = I (e4m3 1.0 on the diagonal), unit activation scales: Y[k, n] is the
+    dequantized weight sw[n] * Wq[n, k] (pytorch/ao PR #3258, jcaip: dequantize
+    by multiplying with an identity), rounded to bf16, exactly."""
+    N, K = 256, 512
+    _, W, _, _ = inputs.generate(inputs.Workload("id", 1, N, K, seed=21))
+    values, meta, sw = ora.compress(inputs.bf16_bits(W))
+    xq = np.where(np.eye(K, dtype=bool), 0x38, 0).astype(np.uint8)
+    sx = np.ones((1, K), np.float32)
+    y = sp24.gemm(dev(xq), dev(sx), dev(values), dev(meta), dev(sw))
+    torch.cuda.synchronize()
+    Wq = ora.e4m3_decode(ora.decompress(values, meta))
+    ref = torch.from_numpy((Wq * sw[0][:, None]).astype(np.float32).T.copy()).to(torch.bfloat16)
+    assert torch.equal(y.cpu(), ref)
+
+
+def test_all_zero_weight(ora, sp24):
+    M, N, K = 64, 128, 256
+    X, _, _, _ = inputs.generate(inputs.Workload("z", M, N, K, seed=1))
+    xq, sx = ora.quantize_act(X.numpy())
+    values, meta, sw = ora.compress(np.zeros((N, K), np.uint16))
+    y = sp24.gemm(dev(xq), dev(sx), dev(values), dev(meta), dev(sw))
+    torch.cuda.synchronize()
+    assert (y.float() == 0).all()
+
+
+def test_one_hot_weight_patterns(ora, sp24):
+    """Each weight row keeps one nonzero at a known position per group of
+    four (and its partner at a zero value): checks that every metadata
+    nibble steers the right activation column, end to end."""
+    M, N, K = 64, 128, 256
+    rng = np.random.default_rng(8)
+    Wf = np.zeros((N, K), np.float32)
+    pos = rng.integers(0, 4, size=(N, K // 4))
+    Wf.reshape(N, K // 4, 4)[np.arange(N)[:, None], np.arange(K // 4)[None, :], pos] = \
+        rng.uniform(0.5, 1.5, (N, K // 4)).astype(np.float32)
+    Wb = inputs.bf16_bits(torch.from_numpy(Wf).to(torch.bfloat16))
+    X, _, _, _ = inputs.generate(inputs.Workload("oh", M, N, K, seed=2))
+    xq, sx = ora.quantize_act(X.numpy())
+    values, meta, sw = ora.compress(Wb)
+    y = _run_gpu(sp24, inputs.Workload("oh", M, N, K), xq, sx, values, meta, sw, None, None)
+    ref = ora.gemm(xq, sx, values, meta, sw)
+    assert_close(y, ref, "one-hot")
+
+
+def test_repeat_is_deterministic(ora, sp24):
+    w = inputs.Workload("det", 300, 384, 1024, gN=128, gK=128, seed=77)
+    xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+    a = [dev(t) for t in (xq, sx, values, meta, sw)]
+    y1 = sp24.gemm(*a, w.gM, w.gN, w.gk)
+    y2 = sp24.gemm(*a, w.gM, w.gN, w.gk)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+# ------------------------------------------------------------- full-size runs
+def _sample_rows(M, BN=128):
+    rows = {0, 1, M // 2, M - 1}
+    for t in (BN - 1, BN, 2 * BN - 1, (M // BN) * BN, (M // BN) * BN - 1):
+        if 0 <= t < M:
+            rows.add(t)
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["llama", "groupwise", "fused"])
+def test_full_size_sampled(ora, sp24, name):
+    w = inputs.WORKLOADS[name]
+    xq, sx, values, meta, sw, x2, w2 = _prep(ora, w)
+    y = _run_gpu(sp24, w, xq, sx, values, meta, sw, x2, w2)
+    rows = _sample_rows(w.M)
+    assert w.gM == 1
+    ref = ora.gemm(xq[rows], sx[:, rows], values, meta, sw, 1, w.gN, w.gk,
+                   None if x2 is None else x2[rows], w2)
+    assert_close(y[rows], ref, name + " sampled rows %s" % rows)
+    assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("M", inputs.DECODE_M)
+def test_decode_full_size(ora, sp24, M):
+    w = inputs.with_shape(inputs.WORKLOADS["decode"], M=M)
+    xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+    y = _run_gpu(sp24, w, xq, sx, values, meta, sw, None, None)
+    rows = sorted({0, M - 1, M // 2})
+    ref = ora.gemm(xq[rows], sx[:, rows], values, meta, sw)
+    assert_close(y[rows], ref, "decode M=%d" % M)
+
+
+def test_compress_then_gemm_on_device(ora, sp24):
+    """The whole path on the device (quantize, compress, GEMM) against the
+    whole path in the oracle."""
+    w = inputs.with_shape(inputs.WORKLOADS["llama"], M=256, N=512, K=1024)
+    X, W, _, _ = inputs.generate(w)
+    xq_d, sx_d = sp24.quantize_act(X.cuda())
+    v_d, m_d, sw_d = sp24.compress(dev(inputs.bf16_bits(W)))
+    y = bf16_to_f64(sp24.gemm(xq_d, sx_d, v_d, m_d, sw_d))
+    xq, sx = ora.quantize_act(X.numpy())
+    values, meta, sw = ora.compress(inputs.bf16_bits(W))
+    assert_close(y, ora.gemm(xq, sx, values, meta, sw), "device path")
