@@ -1,0 +1,389 @@
+"""Benchmark of the 2:4 sparse FP8 hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: compress the bf16
+weight (magnitude 2:4 prune + e4m3 + pack) and run the group-wise scaled
+sparse GEMM on e4m3 activations.  Activation quantization is input
+preparation and runs before the timed region.
+
+Prints ONE JSON line (rank 0).  ``value`` is dense-equivalent TFLOPS (2*M*N*K
+per step, the convention sparse tensor peaks are quoted in) over the whole
+step, summed over ranks; per-kernel figures and the roofline of the dominant
+kernel ride along.  ``--impl reference`` times the CPU oracle instead, on a
+bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama]
+       torchrun --nproc-per-node N bench.py --gpus N ...
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import inputs  # noqa: E402
+
+METRIC = "sparse FP8 GEMM TFLOPS & % of FP8 sparse peak; compress GB/s & % HBM peak"
+UNIT = "TFLOPS"
+FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+
+DESCR = {
+    "llama": "Llama-style FP8 linear: X[2048,4096] e4m3 per-token (N(0,1), 0.1% outliers x20), "
+             "W[4096,4096] bf16 N(0,0.02) -> 2:4 e4m3 per-channel, Y bf16",
+    "groupwise": "group-wise scaling: X[3000,4096] 1x128 scales, W[14336,4096] 128x128 block scales",
+    "fused": "fused: llama shapes + bf16 side GEMM X2[2048,64] W2[4096,64]",
+    "decode": "decode: X[M,4096] per-token, W[28672,4096] per-channel",
+    "tiny": "tiny: X[128,512], W[256,512]",
+}
+
+
+# ---------------------------------------------------------------- utilities
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------- our GPU arm
+def run_ours(args):
+    import semi_structured_sparse_gb300 as sp24
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    sp24.load(build_if_missing=(world == 1))
+    w = inputs.WORKLOADS[args.workload]
+    if args.workload == "decode":
+        w = inputs.with_shape(w, M=args.decode_m)
+    w = inputs.with_shape(w, seed=w.seed + 1000 * rank)  # each replica its own batch
+    gk = w.gk
+    X, W, X2, W2 = inputs.generate(w)
+    dev = torch.device("cuda", local)
+
+    # rotating input sets so that the working set exceeds L2 between reuses
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = (w.N * w.K * 2 + w.M * w.K + w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.N * 2)
+    nsets = max(2, -(-3 * l2 // set_bytes))
+    Wd = W.to(dev)
+    xq0, sx0 = sp24.quantize_act(X.to(dev), gk)
+    sets = []
+    for i in range(nsets):
+        s = {
+            "W": Wd.clone(), "xq": xq0.clone(), "sx": sx0.clone(),
+            "v": torch.empty((w.N, w.K // 2), dtype=torch.uint8, device=dev),
+            "m": torch.empty((w.N, w.K // 8), dtype=torch.uint8, device=dev),
+            "sw": torch.empty((w.K // gk, (w.N + w.gN - 1) // w.gN), dtype=torch.float32, device=dev),
+            "y": torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev),
+            "x2": None if X2 is None else X2.to(dev), "w2": None if W2 is None else W2.to(dev),
+        }
+        sets.append(s)
+    stream = torch.cuda.current_stream()
+
+    def step(s, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sp24.compress(s["W"], w.gN, gk, out=(s["v"], s["m"], s["sw"]))
+        if ev is not None:
+            ev[1].record(stream)
+        sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"])
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(sets[i % nsets])
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        # keep the GPU busy ~1 s so the clock samples see it under load, untimed
+        t_end = time.time() + 1.0
+        i = 0
+        while time.time() < t_end:
+            step(sets[i % nsets])
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(sets[i % nsets], evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+    sp24.last_device_error()
+    ms = start.elapsed_time(stop)
+    t_comp = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    t_gemm = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+
+    # end to end through the public API with host buffers: H2D inputs, D2H output
+    pin_W = W.pin_memory()
+    pin_xq = xq0.cpu().pin_memory()
+    pin_sx = sx0.cpu().pin_memory()
+    pin_x2 = None if X2 is None else X2.pin_memory()
+    pin_w2 = None if W2 is None else W2.pin_memory()
+    pin_y = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    s0 = sets[0]
+
+    def e2e_step():
+        s0["W"].copy_(pin_W, non_blocking=True)
+        s0["xq"].copy_(pin_xq, non_blocking=True)
+        s0["sx"].copy_(pin_sx, non_blocking=True)
+        if pin_x2 is not None:
+            s0["x2"].copy_(pin_x2, non_blocking=True)
+            s0["w2"].copy_(pin_w2, non_blocking=True)
+        step(s0)
+        pin_y.copy_(s0["y"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    if pg:
+        pg.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (pin_W.numel() * 2 + pin_xq.numel() + pin_sx.numel() * 4
+           + (0 if pin_x2 is None else pin_x2.numel() * 2 + pin_w2.numel() * 2))
+    d2h = pin_y.numel() * 2
+
+    flops = w.dense_flops()
+    alg_flops = flops / 2  # only kept weights are multiplied
+    pk = peaks()
+    fp8_dense_peak = pk["bf16_tflops"] * FP8_OVER_BF16
+    comp_bytes = w.N * w.K * 2 + w.N * w.K // 2 + w.N * w.K // 8 + 4 * (w.K // gk) * ((w.N + w.gN - 1) // w.gN)
+    gemm_bytes = (w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.K + 2 * w.M * w.N
+                  + 4 * (w.K // gk) * (w.M + (w.N + w.gN - 1) // w.gN))
+    gemm_tflops_alg = alg_flops / (t_gemm * 1e-3) / 1e12
+    comp_gbs = comp_bytes / (t_comp * 1e-3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "M": w.M, "N": w.N, "K": w.K,
+                   "scales": {"gM": w.gM, "gN": w.gN, "gK": gk}, "side_r": w.r,
+                   "step": "compress(W) + sparse GEMM", "flops_per_step": "2*M*N*K dense-equivalent",
+                   "l2": "rotating %d input sets of %.1f MB (> L2 %.0f MB)" % (nsets, set_bytes / 1e6, l2 / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "kernels": {
+            "gemm": {"ms": round(t_gemm, 5), "tflops_dense_equiv": round(2 * gemm_tflops_alg, 1),
+                     "frac_fp8_sparse_peak": round(gemm_tflops_alg / fp8_dense_peak, 4)},
+            "compress": {"ms": round(t_comp, 5), "gbs": round(comp_gbs, 1),
+                         "frac_hbm": round(comp_gbs / pk["hbm_gbs"], 4)},
+        },
+        "roofline": {"kernel": "sp24_gemm_kernel", "bound": "tensor", "achieved": round(gemm_tflops_alg, 1),
+                     "peak": round(fp8_dense_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops_alg / fp8_dense_peak, 4), "traffic": None,
+                     "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16), of %s" % (
+                         pk["source"], FP8_OVER_BF16, pk["source"]),
+                     "achieved_counts": "algorithmic 2*M*N*K/2 (kept weights only)"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if pg:
+        pg.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------ oracle (CPU)
+def cpu_step_estimate(w: inputs.Workload, budget_s: float):
+    """Time the oracle on a bounded sample of the workload and scale it to one
+    whole step (compress all of W + GEMM of all M tokens).
+    Returns (seconds per step, description, threads)."""
+    import numpy as np
+
+    import oracle
+    X, W, X2, W2 = inputs.generate(w)
+    gk = w.gk
+    Wb = inputs.bf16_bits(W)
+    # compress sample: whole 128-row blocks
+    n_rows = min(w.N, 512)
+    t0 = time.perf_counter()
+    values, meta, sw = oracle.compress(Wb[:n_rows], w.gN, gk)
+    t_comp = (time.perf_counter() - t0) * (w.N / n_rows)
+    values, meta, sw = oracle.compress(Wb, w.gN, gk)
+    xq, sx = oracle.quantize_act(X.numpy(), gk)
+    # GEMM sample: the first m_s tokens, sized to the time budget
+    m_s = 1
+    t_g = 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm(xq[:m_s], sx[:, :m_s], values, meta, sw, 1, w.gN, gk,
+                    None if X2 is None else inputs.bf16_bits(X2)[:m_s], None if W2 is None else inputs.bf16_bits(W2))
+        t_g = time.perf_counter() - t0
+        if t_g > budget_s / 8 or m_s >= w.M:
+            break
+        m_s = min(w.M, m_s * 4)
+    t_gemm = t_g * (w.M / m_s)
+    descr = ("oracle compress of %d of %d weight rows and GEMM of %d of %d token rows (all N, K), "
+             "scaled to the full step" % (n_rows, w.N, m_s, w.M))
+    return t_comp + t_gemm, descr, oracle.num_threads()
+
+
+def cpu_baseline(w, budget_s=20.0):
+    sec, descr, threads = cpu_step_estimate(w, budget_s)
+    return {"value": round(w.dense_flops() / sec / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": descr, "seconds_per_step": round(sec, 3)}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return  # the CPU reference arm runs on rank 0 only
+    w = inputs.WORKLOADS[args.workload]
+    if args.workload == "decode":
+        w = inputs.with_shape(w, M=args.decode_m)
+    budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    secs = []
+    descr, threads = "", 1
+    for i in range(args.warmup + args.steps):
+        s, descr, threads = cpu_step_estimate(w, budget)
+        if i >= args.warmup:
+            secs.append(s)
+    sec = sum(secs) / len(secs)
+    value = w.dense_flops() / sec / 1e12
+    out = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "impl": "reference",
+        "config": {"workload": DESCR[args.workload], "M": w.M, "N": w.N, "K": w.K,
+                   "scales": {"gM": w.gM, "gN": w.gN, "gK": w.gk}, "side_r": w.r,
+                   "step": "compress(W) + sparse GEMM", "parallelism": "single"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": descr},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(inputs.WORKLOADS), default="llama")
+    ap.add_argument("--decode-m", type=int, default=16)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
