@@ -176,7 +176,7 @@ def run_ours(args):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         # keep the GPU busy ~1 s so the clock samples see it under load, untimed
-        t_end = time.time() + 1.0
+        t_end = time.time() + (0.0 if args.quick else 1.0)
         i = 0
         while time.time() < t_end:
             step(sets[i % nsets])
@@ -222,11 +222,11 @@ def run_ours(args):
         step(s0)
         pin_y.copy_(s0["y"], non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(0 if args.quick else max(3, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, min(args.steps, 50))
+    e2e_steps = 1 if args.quick else max(3, min(args.steps, 50))
     if pg:
         pg.barrier()
     e0.record(stream)
@@ -287,7 +287,7 @@ def run_ours(args):
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.quick):
         out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if pg:
         pg.destroy_process_group()
@@ -376,6 +376,8 @@ def main():
     ap.add_argument("--decode-m", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling runs: no clock soak, no e2e pass, no CPU baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -75,19 +75,27 @@ SP24_API size_t sp24_meta_bytes(int64_t N, int64_t K);
  *   W       (device) bf16 [N][K], row stride ldw >= K elements.
  *   gN, gK  weight scale granularity: (1, K) per output channel,
  *           (1, 128) per channel and 128-wide K block, or (128, 128) blocks.
- *   values  (device, out) uint8 e4m3 [N][K/2]: for group g of row n the two
- *           kept elements, in ascending k, at values[n][2g], values[n][2g+1].
- *   meta    (device, out) sp24_meta_bytes(N, K) bytes: row n holds K/8 bytes;
- *           byte j carries group 2j in its low nibble and group 2j+1 in its
- *           high nibble; a nibble is i0 | (i1 << 2), i0 < i1 the kept
- *           positions within the group.  This is also the layout the GEMM
- *           reads.
+ *   values  (device, out) N*K/2 bytes of kept e4m3 codes in tiled storage:
+ *           the weight is cut into 128-row x 128-K tiles; tile
+ *           t = (n/128)*(K/128) + k/128 occupies bytes [8192 t, 8192 t + 8192).
+ *           Inside a tile, row r = n % 128 owns 64 bytes at 64 r: the two kept
+ *           codes of each group of four, in ascending k (kept index j = 2g + t
+ *           for group g), with the 16-byte chunk c = (j % 64) / 16 stored at
+ *           chunk position c XOR ((r / 2) mod 4) (the 64-byte swizzle the
+ *           tensor core reads).  A whole tile is one contiguous copy.
+ *   meta    (device, out) sp24_meta_bytes(N, K) = N*K/8 bytes, tiled the same
+ *           way: tile t occupies [2048 t, 2048 t + 2048); row r owns 16 bytes
+ *           at 16 r; byte b carries group 2b of the tile row in its low nibble
+ *           and group 2b+1 in its high nibble; a nibble is i0 | (i1 << 2),
+ *           i0 < i1 the kept positions within the group.  This is the layout
+ *           the tensor core's sparse metadata takes in tensor memory (lane =
+ *           row), so the GEMM copies it without rearranging.
  *   scales  (device, out) fp32 [K/gK][ceil(N/gN)]: amax/448 of the block
  *           (1.0 for an all-zero block).
  * Each kept element is q = e4m3_rn_satfinite(w / scale) with a correctly
  * rounded fp32 division.  Ties in |w| keep the lower index.
- * Preconditions: N >= 1; K a positive multiple of 128; N % 128 == 0 when
- * gN == 128; W, values and meta 16-byte aligned, ldw*2 a multiple of 16.
+ * Preconditions: N a positive multiple of 128; K a positive multiple of 128;
+ * W, values and meta 16-byte aligned, ldw*2 a multiple of 16.
  */
 SP24_API sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, int64_t ldw, int gN, int gK,
                               void* values, void* meta, float* scales, void* stream);
@@ -132,7 +140,8 @@ SP24_API sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K,
  *   gN      1 or 128; gK: K or 128.
  *   X2, W2  (device) bf16 [M][r] and [N][r] (row stride r), or NULL with
  *           r = 0 for no side GEMM; r a multiple of 16, at most 64.
- *   Y       (device, out) bf16 [M][N], row stride ldy >= N.
+ *   Y       (device, out) bf16 [M][N], row stride ldy >= N, ldy % 8 == 0,
+ *           16-byte aligned.
  *   workspace, workspace_bytes: device scratch of at least
  *           sp24_fp8_gemm_workspace_size(M, N, K, r) bytes (may be NULL when
  *           that size is 0).

@@ -38,6 +38,8 @@ def lib():
         L.ora_quantize_act.argtypes = [P, I64, I64, I64, I, P, P]
         L.ora_gemm.argtypes = [P, P, I64, I64, I64, I, P, P, P, I64, I, I,
                                P, P, I64, I, P]
+        for f in ("ora_tile_values", "ora_untile_values", "ora_tile_meta", "ora_untile_meta"):
+            getattr(L, f).argtypes = [P, I64, I64, P]
         L.ora_num_threads.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -128,6 +130,47 @@ def decompress(values, meta) -> np.ndarray:
     dense = np.empty((N, K), dtype=np.uint8)
     lib().ora_decompress(_p(values), _p(meta), N, K, _p(dense))
     return dense
+
+
+# ----------------------------------------------------------- storage layout
+def tile_values(values) -> np.ndarray:
+    """Logical kept values [N, K/2] -> the ABI's tiled storage (N*K/2 bytes):
+    contiguous 128-row x 64-byte tiles with the 64-byte swizzle inside."""
+    values = _c(values, np.uint8)
+    N, K = values.shape[0], values.shape[1] * 2
+    out = np.empty(N * K // 2, dtype=np.uint8)
+    lib().ora_tile_values(_p(values), N, K, _p(out))
+    return out
+
+
+def untile_values(tiled, N: int, K: int) -> np.ndarray:
+    tiled = _c(tiled, np.uint8).ravel()
+    out = np.empty((N, K // 2), dtype=np.uint8)
+    lib().ora_untile_values(_p(tiled), N, K, _p(out))
+    return out
+
+
+def tile_meta(meta) -> np.ndarray:
+    """Logical metadata [N, K/8] -> the ABI's tiled storage: contiguous
+    128-row x 16-byte tiles."""
+    meta = _c(meta, np.uint8)
+    N, K = meta.shape[0], meta.shape[1] * 8
+    out = np.empty(N * K // 8, dtype=np.uint8)
+    lib().ora_tile_meta(_p(meta), N, K, _p(out))
+    return out
+
+
+def untile_meta(tiled, N: int, K: int) -> np.ndarray:
+    tiled = _c(tiled, np.uint8).ravel()
+    out = np.empty((N, K // 8), dtype=np.uint8)
+    lib().ora_untile_meta(_p(tiled), N, K, _p(out))
+    return out
+
+
+def compress_abi(W_bits, gN: int = 1, gK: int = None):
+    """compress() in the storage layout the C ABI produces and consumes."""
+    values, meta, scales = compress(W_bits, gN, gK)
+    return tile_values(values), tile_meta(meta), scales
 
 
 # ------------------------------------------------------- activation quantize

@@ -236,6 +236,59 @@ void ora_decompress(const uint8_t *values, const uint8_t *meta, int64_t N, int64
     }
 }
 
+/* ------------------------------------------------------- storage layout */
+
+/* The packed weight as the C ABI stores it: 128-row x 128-K tiles, each tile
+ * contiguous, tiles of one 128-row band consecutive along K.
+ *   values: tile t = (n/128)*(K/128) + j/64 holds 128 rows x 64 kept bytes
+ *           (8192 B); kept byte j of row n sits at row r = n % 128, byte
+ *           b = j % 64, whose 16-byte chunk b/16 is stored at chunk position
+ *           (b/16) XOR ((r/2) mod 4) -- the 64-byte swizzle -- so a tile
+ *           offset is r*64 + 16*((b/16) ^ ((r/2)%4)) + b%16.
+ *   meta:   tile t = (n/128)*(K/128) + jb/16 holds 128 rows x 16 bytes
+ *           (2048 B); logical meta byte jb of row n sits at r*16 + jb%16.
+ * N must be a multiple of 128 and K of 128. */
+static int64_t values_tiled_offset(int64_t n, int64_t j, int64_t K)
+{
+    int64_t t = (n / 128) * (K / 128) + j / 64;
+    int64_t r = n % 128, b = j % 64;
+    return t * 8192 + r * 64 + 16 * ((b / 16) ^ ((r / 2) % 4)) + b % 16;
+}
+
+static int64_t meta_tiled_offset(int64_t n, int64_t jb, int64_t K)
+{
+    int64_t t = (n / 128) * (K / 128) + jb / 16;
+    return t * 2048 + (n % 128) * 16 + jb % 16;
+}
+
+void ora_tile_values(const uint8_t *values, int64_t N, int64_t K, uint8_t *tiled)
+{
+    int64_t n, j;
+    for (n = 0; n < N; ++n)
+        for (j = 0; j < K / 2; ++j) tiled[values_tiled_offset(n, j, K)] = values[n * (K / 2) + j];
+}
+
+void ora_untile_values(const uint8_t *tiled, int64_t N, int64_t K, uint8_t *values)
+{
+    int64_t n, j;
+    for (n = 0; n < N; ++n)
+        for (j = 0; j < K / 2; ++j) values[n * (K / 2) + j] = tiled[values_tiled_offset(n, j, K)];
+}
+
+void ora_tile_meta(const uint8_t *meta, int64_t N, int64_t K, uint8_t *tiled)
+{
+    int64_t n, jb;
+    for (n = 0; n < N; ++n)
+        for (jb = 0; jb < K / 8; ++jb) tiled[meta_tiled_offset(n, jb, K)] = meta[n * (K / 8) + jb];
+}
+
+void ora_untile_meta(const uint8_t *tiled, int64_t N, int64_t K, uint8_t *meta)
+{
+    int64_t n, jb;
+    for (n = 0; n < N; ++n)
+        for (jb = 0; jb < K / 8; ++jb) meta[n * (K / 8) + jb] = tiled[meta_tiled_offset(n, jb, K)];
+}
+
 /* ------------------------------------------------- activation quantization */
 
 /* Dynamic activation quantization (pytorch/ao PR #3258, the activation path:

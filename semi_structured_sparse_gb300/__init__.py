@@ -101,6 +101,8 @@ def compress(w: torch.Tensor, gN: int = 1, gK: int = None, out=None, stream=None
     """Magnitude 2:4 prune + e4m3 + pack of a bf16 weight [N, K].
 
     Returns (values uint8 [N, K/2], meta uint8 [N, K/8], scales fp32 [K/gK, ceil(N/gN)]).
+    values and meta hold the library's tiled storage (128 x 128 weight tiles,
+    each contiguous; see include/sp24.h), which is what gemm() reads.
     ``out`` may supply those three tensors (no allocation then)."""
     lib = load()
     _dev_tensor(w, torch.bfloat16, "w")

@@ -11,7 +11,6 @@
 // Groupwise scaling along M for FP8 gemm", ScaleGranularity description).
 // Activation path: same PR #3258, the activation is divided by its scale and
 // cast to e4m3.
-#include <cuda_fp8.h>
 #include "sp24_internal.cuh"
 
 namespace sp24 {
@@ -21,49 +20,52 @@ constexpr float kE4M3Max = 448.0f;
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
-__device__ __forceinline__ uint32_t to_e4m3(float x) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
-}
-
 // Scale for a block whose largest |w| has bf16 magnitude bits `amax_bits`:
 // amax / 448 (correctly rounded), or 1 when the block is all zeros.
 __device__ __forceinline__ float weight_scale(uint32_t amax_bits) {
   return amax_bits == 0 ? 1.0f : __fdiv_rn(bf16_bits_to_float(amax_bits), kE4M3Max);
 }
 
-// Largest bf16 magnitude (sign cleared) among the 8 values of a 16-byte chunk.
+// Largest bf16 magnitude (sign cleared) among the 8 values of a 16-byte
+// chunk, with packed 16-bit unsigned max.
 __device__ __forceinline__ uint32_t chunk_amax_bits(const uint4& v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = max(m, w[i] & 0x7FFFu);
-    m = max(m, (w[i] >> 16) & 0x7FFFu);
-  }
-  return m;
+  const uint32_t m2 = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                               __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  return max(m2 & 0xFFFFu, m2 >> 16);
 }
 
-// Select, quantize and pack one group of four bf16 values (bit patterns).
-// Element j beats element i when |w_j| > |w_i|, or when they are equal and
-// j < i; the two elements beaten by fewer than two others are kept.
-// Returns the two e4m3 codes (kept in ascending position) in bits [15:0] and
-// the metadata nibble i0 | i1 << 2 in bits [19:16].
+// Two fp32 -> e4m3 conversions in one instruction (round to nearest even,
+// saturate to +-448); `lo` lands in bits [7:0], `hi` in bits [15:8].
+__device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Select, quantize and pack one group of four bf16 values (bit patterns
+// e0..e3).  Each element gets the key  |w| bits << 3 | (3 - i) << 1 | sign:
+// a larger key is a larger magnitude, and among equal magnitudes the lower
+// index (the sign bit never decides because indices differ), so the two
+// largest keys are exactly the two kept elements.  Found with a 4-input
+// max/min network.  Returns the two e4m3 codes in ascending position in bits
+// [15:0] and the metadata nibble i0 | i1 << 2 in bits [19:16].
+__device__ __forceinline__ uint32_t group_key(uint32_t e, uint32_t i) {
+  return ((e & 0x7FFFu) << 3) | ((3u - i) << 1) | (e >> 15);
+}
 __device__ __forceinline__ uint32_t pack_group(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3, float s) {
-  const uint32_t a0 = e0 & 0x7FFFu, a1 = e1 & 0x7FFFu, a2 = e2 & 0x7FFFu, a3 = e3 & 0x7FFFu;
-  const int c01 = a0 >= a1, c02 = a0 >= a2, c03 = a0 >= a3;
-  const int c12 = a1 >= a2, c13 = a1 >= a3, c23 = a2 >= a3;
-  const int r0 = (1 - c01) + (1 - c02) + (1 - c03);
-  const int r1 = c01 + (1 - c12) + (1 - c13);
-  const int r2 = c02 + c12 + (1 - c23);
-  const int r3 = c03 + c13 + c23;
-  const uint32_t keep = (r0 < 2 ? 1u : 0u) | (r1 < 2 ? 2u : 0u) | (r2 < 2 ? 4u : 0u) | (r3 < 2 ? 8u : 0u);
-  const uint32_t i0 = __ffs(keep) - 1;
-  const uint32_t i1 = 31 - __clz(keep);
-  const uint32_t v0 = i0 == 0 ? e0 : (i0 == 1 ? e1 : e2);
-  const uint32_t v1 = i1 == 3 ? e3 : (i1 == 2 ? e2 : e1);
-  const uint32_t q0 = to_e4m3(__fdiv_rn(bf16_bits_to_float(v0), s));
-  const uint32_t q1 = to_e4m3(__fdiv_rn(bf16_bits_to_float(v1), s));
-  return q0 | (q1 << 8) | ((i0 | (i1 << 2)) << 16);
+  const uint32_t k0 = group_key(e0, 0), k1 = group_key(e1, 1), k2 = group_key(e2, 2), k3 = group_key(e3, 3);
+  const uint32_t hi01 = max(k0, k1), lo01 = min(k0, k1);
+  const uint32_t hi23 = max(k2, k3), lo23 = min(k2, k3);
+  const uint32_t first = max(hi01, hi23);
+  const uint32_t second = max(min(hi01, hi23), max(lo01, lo23));
+  const uint32_t ia = 3u - ((first >> 1) & 3u), ib = 3u - ((second >> 1) & 3u);
+  // bf16 bits back from a key: sign in bit 0, magnitude in bits [17:3]
+  const uint32_t va = ((first & 1u) << 15) | (first >> 3), vb = ((second & 1u) << 15) | (second >> 3);
+  const bool a_first = ia < ib;
+  const uint32_t i0 = a_first ? ia : ib, i1 = a_first ? ib : ia;
+  const uint32_t v0 = a_first ? va : vb, v1 = a_first ? vb : va;
+  const uint32_t q = to_e4m3x2(__fdiv_rn(bf16_bits_to_float(v0), s), __fdiv_rn(bf16_bits_to_float(v1), s));
+  return q | ((i0 | (i1 << 2)) << 16);
 }
 
 // Two groups (8 bf16 in a 16-byte chunk) -> 4 value bytes and 1 meta byte.
@@ -74,6 +76,20 @@ __device__ __forceinline__ void pack_chunk(const uint4& v, float s, uint32_t& va
   metab = (g0 >> 16) | ((g1 >> 16) << 4);
 }
 
+// Storage the GEMM reads (see sp24.h): 128-row x 128-K tiles, tile-contiguous,
+// consecutive along K within a 128-row band; kept values with the 64-byte
+// swizzle applied inside a tile.  Offsets of 4 kept bytes starting at kept
+// index j (j % 4 == 0) of row n, and of meta byte jb of row n.
+__device__ __forceinline__ int64_t values_offset(int n, int j, int K) {
+  const int64_t t = static_cast<int64_t>(n >> 7) * (K >> 7) + (j >> 6);
+  const int r = n & 127, b = j & 63;
+  return t * 8192 + r * 64 + (((b >> 4) ^ ((r >> 1) & 3)) << 4) + (b & 15);
+}
+__device__ __forceinline__ int64_t meta_offset(int n, int jb, int K) {
+  const int64_t t = static_cast<int64_t>(n >> 7) * (K >> 7) + (jb >> 4);
+  return t * 2048 + (n & 127) * 16 + (jb & 15);
+}
+
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -82,62 +98,72 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
-constexpr int kRowsPerCta = 8;   // one warp per weight row
-constexpr int kHeldChunks = 16;  // a row of up to 16 x 256 elements stays in registers
+constexpr int kRowsPerCta = 8;   // gK = 128: one warp per weight row
+constexpr int kPairRowsPerCta = 4;  // gK = K: two warps per weight row
+constexpr int kHeldChunks = 8;   // per warp: 8 x 16 bytes per lane stay in registers
 
-// gN = 1: one warp per row.  GK128 = false: one scale per row (gK = K);
-// true: one scale per row and 128-wide K block (each half-warp owns a block).
+// gN = 1.  GK128 = false: one scale per row (gK = K); two warps share a row,
+// warp h of the pair owning the 256-element chunks c = h, h+2, h+4, ...; the
+// row's amax is combined through shared memory.  GK128 = true: one scale per
+// row and 128-wide K block; one warp per row, each half-warp owns a block.
 template <bool GK128>
 __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __restrict__ W, int N, int K, int64_t ldw,
                                                             uint8_t* __restrict__ values, uint8_t* __restrict__ meta,
                                                             float* __restrict__ scales) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.x * kRowsPerCta + warp;
-  if (n >= N) return;
-  const uint16_t* row = W + static_cast<int64_t>(n) * ldw;
-  uint8_t* vrow = values + static_cast<int64_t>(n) * (K / 2);
-  uint8_t* mrow = meta + static_cast<int64_t>(n) * (K / 8);
   const int nchunks = (K + 255) / 256;  // 256 elements per warp step, 8 per lane
 
   if (!GK128) {
+    __shared__ uint32_t pair_amax[8];
+    const int h = warp & 1;
+    const int n = blockIdx.x * kPairRowsPerCta + (warp >> 1);
+    const bool valid = n < N;
+    const uint16_t* row = W + static_cast<int64_t>(valid ? n : 0) * ldw;
     uint4 held[kHeldChunks];
     uint32_t amax = 0;
 #pragma unroll
-    for (int c = 0; c < kHeldChunks; ++c) {
-      const int k = c * 256 + lane * 8;
-      if (c < nchunks && k < K) {
-        held[c] = ldg_stream(row + k);
-        amax = max(amax, chunk_amax_bits(held[c]));
+    for (int i = 0; i < kHeldChunks; ++i) {
+      const int c = 2 * i + h, k = c * 256 + lane * 8;
+      if (valid && c < nchunks && k < K) {
+        held[i] = ldg_stream(row + k);
+        amax = max(amax, chunk_amax_bits(held[i]));
       }
     }
-    for (int c = kHeldChunks; c < nchunks; ++c) {  // rows longer than 4096: stream once for amax
+    for (int c = 2 * kHeldChunks + h; valid && c < nchunks; c += 2) {  // rows longer than 4096: stream for amax
       const int k = c * 256 + lane * 8;
       if (k < K) amax = max(amax, chunk_amax_bits(ldg_stream(row + k)));
     }
     amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+    if (lane == 0) pair_amax[warp] = amax;
+    __syncthreads();
+    if (!valid) return;
+    amax = max(pair_amax[warp & ~1], pair_amax[warp | 1]);
     const float s = weight_scale(amax);
-    if (lane == 0) scales[n] = s;
+    if (lane == 0 && h == 0) scales[n] = s;
 #pragma unroll
-    for (int c = 0; c < kHeldChunks; ++c) {
-      const int k = c * 256 + lane * 8;
+    for (int i = 0; i < kHeldChunks; ++i) {
+      const int c = 2 * i + h, k = c * 256 + lane * 8;
       if (c < nchunks && k < K) {
         uint32_t vals, mb;
-        pack_chunk(held[c], s, vals, mb);
-        *reinterpret_cast<uint32_t*>(vrow + k / 2) = vals;
-        mrow[k / 8] = static_cast<uint8_t>(mb);
+        pack_chunk(held[i], s, vals, mb);
+        *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
+        meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
       }
     }
-    for (int c = kHeldChunks; c < nchunks; ++c) {
+    for (int c = 2 * kHeldChunks + h; c < nchunks; c += 2) {
       const int k = c * 256 + lane * 8;
       if (k < K) {
         uint32_t vals, mb;
         pack_chunk(*reinterpret_cast<const uint4*>(row + k), s, vals, mb);
-        *reinterpret_cast<uint32_t*>(vrow + k / 2) = vals;
-        mrow[k / 8] = static_cast<uint8_t>(mb);
+        *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
+        meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
       }
     }
   } else {
     // lanes 0-15 cover K block 2c, lanes 16-31 block 2c+1 (when it exists)
+    const int n = blockIdx.x * kRowsPerCta + warp;
+    if (n >= N) return;
+    const uint16_t* row = W + static_cast<int64_t>(n) * ldw;
     for (int c = 0; c < nchunks; ++c) {
       const int k = c * 256 + lane * 8;
       const bool active = k < K;
@@ -151,8 +177,8 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
         if ((lane & 15) == 0) scales[static_cast<int64_t>(k / 128) * N + n] = s;
         uint32_t vals, mb;
         pack_chunk(v, s, vals, mb);
-        *reinterpret_cast<uint32_t*>(vrow + k / 2) = vals;
-        mrow[k / 8] = static_cast<uint8_t>(mb);
+        *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
+        meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
       }
     }
   }
@@ -189,8 +215,8 @@ __global__ void __launch_bounds__(256) compress_blocks_kernel(const uint16_t* __
     const int n = nb * 128 + r0 + 16 * i;
     uint32_t vals, mb;
     pack_chunk(v[i], s, vals, mb);
-    *reinterpret_cast<uint32_t*>(values + static_cast<int64_t>(n) * (K / 2) + k / 2) = vals;
-    meta[static_cast<int64_t>(n) * (K / 8) + k / 8] = static_cast<uint8_t>(mb);
+    *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
+    meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
   }
 }
 
@@ -206,8 +232,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
   uint8_t* qrow = xq + static_cast<int64_t>(m) * K;
   const int nsteps = K / 128;
   auto quant4 = [&](const float4& f, float s) -> uint32_t {
-    return to_e4m3(__fdiv_rn(f.x, s)) | (to_e4m3(__fdiv_rn(f.y, s)) << 8) | (to_e4m3(__fdiv_rn(f.z, s)) << 16) |
-           (to_e4m3(__fdiv_rn(f.w, s)) << 24);
+    return to_e4m3x2(__fdiv_rn(f.x, s), __fdiv_rn(f.y, s)) | (to_e4m3x2(__fdiv_rn(f.z, s), __fdiv_rn(f.w, s)) << 16);
   };
   auto amax4 = [](const float4& f) { return fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))); };
   if (GK128) {
@@ -246,7 +271,7 @@ extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, in
   const bool row_k128 = (gN == 1 && gK == 128);
   const bool block128 = (gN == 128 && gK == 128);
   if (!per_channel && !row_k128 && !block128) return SP24_ERR_UNSUPPORTED;
-  if (block128 && N % 128 != 0) return SP24_ERR_INVALID_ARG;
+  if (N % 128 != 0) return SP24_ERR_INVALID_ARG;  // tiled storage: whole 128-row bands
   if (!aligned16(W) || !aligned16(values) || !aligned16(meta) || (ldw * 2) % 16 != 0) return SP24_ERR_ALIGNMENT;
   if (reinterpret_cast<uintptr_t>(scales) % 4 != 0) return SP24_ERR_ALIGNMENT;
   const DeviceInfo* dev = nullptr;
@@ -261,11 +286,13 @@ extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, in
     if (grid.y > 65535u) return SP24_ERR_UNSUPPORTED;
     compress_blocks_kernel<<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
   } else {
-    const unsigned grid = static_cast<unsigned>((N + kRowsPerCta - 1) / kRowsPerCta);
-    if (per_channel)
+    if (per_channel) {
+      const unsigned grid = static_cast<unsigned>((N + kPairRowsPerCta - 1) / kPairRowsPerCta);
       compress_rows_kernel<false><<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
-    else
+    } else {
+      const unsigned grid = static_cast<unsigned>((N + kRowsPerCta - 1) / kRowsPerCta);
       compress_rows_kernel<true><<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
+    }
   }
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }

@@ -35,14 +35,16 @@
 namespace sp24 {
 namespace {
 
-constexpr int BM = 128;                // weight rows per tile (MMA M)
-constexpr int BK = 128;                // logical K per stage (two sparse MMAs of K = 64)
-constexpr int A_STAGE = BM * BK / 2;   // kept values: 8 KB
-constexpr int META_STAGE = BM * BK / 8;  // metadata: 2 KB
-constexpr int META_COL0 = 448;         // TMEM columns 448..511: metadata ring
-constexpr int META_SLOTS = 16;         // 4 columns each
+constexpr int BM = 128;                  // weight rows per tile (MMA M)
+constexpr int BK = 128;                  // logical K per stage (two sparse MMAs of K = 64)
+constexpr int A_STAGE = BM * BK / 2;     // kept values: one 8 KB storage tile
+constexpr int META_STAGE = BM * BK / 8;  // metadata: one 2 KB storage tile
+constexpr int META_COL0 = 448;           // TMEM columns 448..511: metadata ring
+constexpr int META_SLOTS = 16;           // 4 columns each
 constexpr int MAX_STAGES = 16;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;             // two per TMEM lane quadrant, each half of the columns
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int NUM_THREADS = 64 + EPI_THREADS;
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr int BAR_BYTES = 1024;
 
@@ -51,68 +53,87 @@ struct Cfg {
   static constexpr int B_STAGE = BN * BK;  // e4m3 activations, 128 B per token row
   static constexpr int STAGE = A_STAGE + META_STAGE + B_STAGE;
   static constexpr int SIDE_BYTES = SIDE ? (BM * 128 + BN * 128) : 0;
+  static constexpr int OUT_BYTES = BN * BM * 2;  // bf16 output tile staged for the TMA store
   static constexpr int NACC = (PROMOTE && !SIDE && 3 * BN <= META_COL0) ? 3 : 2;
-  static constexpr int CS_BYTES = PROMOTE ? 2 * BN * 4 : 0;
-  static constexpr int FIXED = 1024 + SIDE_BYTES + CS_BYTES + BAR_BYTES;
+  static constexpr int SCALE_BYTES = 4 * BN * (PROMOTE ? 2 : 1);
+  static constexpr int FIXED = 1024 + SIDE_BYTES + OUT_BYTES + SCALE_BYTES + BAR_BYTES;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE;
   static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
   static constexpr int SMEM = FIXED + STAGES * STAGE;
+  static constexpr int COLS = BN / 2;  // accumulator columns (tokens) per epilogue warp
   static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(STAGES >= 2, "need at least two stages");
   static_assert(NACC * BN + (SIDE ? BN : 0) <= META_COL0, "TMEM columns");
   static_assert(STAGES <= META_SLOTS, "metadata ring must cover the stage ring");
+  static_assert(COLS % 8 == 0, "epilogue chunking");
 };
 
 struct GemmArgs {
+  const uint8_t* values;  // tiled kept values
+  const uint8_t* meta;    // tiled metadata
   const float* sx;
   const float* sw;
-  __nv_bfloat16* Y;
-  int64_t ldy;
   int M, N, K;
-  int ldsx, ldsw;       // row strides (floats) of the scale tensors
+  int ldsx, ldsw;          // row strides (floats) of the scale tensors
   int gM_shift, gN_shift;  // log2 of the granularities (0 or 7)
   int m_tiles, n_tiles, k_tiles;
-  int side_ksteps;      // r / 16
+  int side_ksteps;  // r / 16
   unsigned int* err;
 };
 
-// Barrier over the 128 epilogue threads (named barrier 1) that also ORs a
+// Barrier over the epilogue threads (named barrier 1) that also ORs a
 // predicate across them, so that a give-up decision is taken by all or none.
 __device__ __forceinline__ bool epilogue_bar_any(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred ? 1u : 0u)
+      : "r"(pred ? 1u : 0u), "n"(EPI_THREADS)
       : "memory");
   return r != 0;
+}
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
+
+// Loads `N8 * 8` consecutive accumulator columns of this warp's lanes.
+template <int N8>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
+  if constexpr (N8 % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N8 / 2; ++i) tmem_ld16(taddr + 16 * i, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * i));
+  } else {
+#pragma unroll
+    for (int i = 0; i < N8; ++i) tmem_ld8(taddr + 8 * i, r + 8 * i);
+  }
 }
 
 template <int BN, bool PROMOTE, bool SIDE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    sp24_gemm_kernel(const __grid_constant__ CUtensorMap tm_vals, const __grid_constant__ CUtensorMap tm_meta,
-                     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w2,
-                     const __grid_constant__ CUtensorMap tm_x2, const GemmArgs p) {
+    sp24_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w2,
+                     const __grid_constant__ CUtensorMap tm_x2, const __grid_constant__ CUtensorMap tm_y,
+                     const GemmArgs p) {
   using C = Cfg<BN, PROMOTE, SIDE>;
   constexpr int STAGES = C::STAGES;
   constexpr int NACC = C::NACC;
+  constexpr int COLS = C::COLS;
+  constexpr int CH = COLS >= 16 ? 16 : COLS;  // columns per TMEM load
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = sm;
   uint8_t* side_w2 = sm + STAGES * C::STAGE;
   uint8_t* side_x2 = side_w2 + BM * 128;
-  float* cs = reinterpret_cast<float*>(sm + STAGES * C::STAGE + C::SIDE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + STAGES * C::STAGE + C::SIDE_BYTES + C::CS_BYTES);
-  uint64_t* full = bars;                  // [STAGES] TMA -> MMA
-  uint64_t* empty = bars + MAX_STAGES;    // [STAGES] MMA -> TMA
-  uint64_t* accf = bars + 2 * MAX_STAGES; // [NACC]  MMA -> epilogue
-  uint64_t* acce = accf + 3;              // [NACC]  epilogue -> MMA
-  uint64_t* sidef = acce + 3;             // side operands loaded
-  uint64_t* sidee = sidef + 1;            // side operands consumed
-  uint64_t* saccf = sidee + 1;            // side accumulator ready
-  uint64_t* sacce = saccf + 1;            // side accumulator drained
-  uint64_t* drain = sacce + 1;            // MMA drain on abort
+  uint8_t* out_tile = sm + STAGES * C::STAGE + C::SIDE_BYTES;      // [2 halves][BN tokens][64 channels] bf16
+  float* scl = reinterpret_cast<float*>(out_tile + C::OUT_BYTES);  // token scales, [1 or 2][BN]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_tile + C::OUT_BYTES + C::SCALE_BYTES);
+  uint64_t* full = bars;                   // [STAGES] loads -> MMA
+  uint64_t* empty = bars + MAX_STAGES;     // [STAGES] MMA -> loads
+  uint64_t* accf = bars + 2 * MAX_STAGES;  // [NACC]  MMA -> epilogue
+  uint64_t* acce = accf + 3;               // [NACC]  epilogue -> MMA
+  uint64_t* sidef = acce + 3;              // side operands loaded
+  uint64_t* sidee = sidef + 1;             // side operands consumed
+  uint64_t* saccf = sidee + 1;             // side accumulator ready
+  uint64_t* sacce = saccf + 1;             // side accumulator drained
+  uint64_t* drain = sacce + 1;             // MMA drain on abort
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,19 +144,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], 128);
+      mbar_init(&acce[i], EPI_THREADS);
     }
     mbar_init(sidef, 1);
     mbar_init(sidee, 1);
     mbar_init(saccf, 1);
-    mbar_init(sacce, 128);
+    mbar_init(sacce, EPI_THREADS);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_vals);
-    tma_prefetch_desc(&tm_meta);
     tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_y);
     if (SIDE) {
       tma_prefetch_desc(&tm_w2);
       tma_prefetch_desc(&tm_x2);
@@ -158,14 +178,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int64_t issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int n0 = (tile % p.n_tiles) * BM;
+        const int n_tile = tile % p.n_tiles;
         const int m0 = (tile / p.n_tiles) * BN;
+        const uint8_t* vsrc = p.values + static_cast<int64_t>(n_tile) * p.k_tiles * A_STAGE;
+        const uint8_t* msrc = p.meta + static_cast<int64_t>(n_tile) * p.k_tiles * META_STAGE;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
           uint8_t* sA = ring + stage * C::STAGE;
           mbar_arrive_expect_tx(&full[stage], C::STAGE);
-          tma_load_2d(sA, &tm_vals, &full[stage], kt * (BK / 2), n0);
-          tma_load_2d(sA + A_STAGE, &tm_meta, &full[stage], kt * (BK / 8), n0);
+          bulk_load(sA, vsrc + static_cast<int64_t>(kt) * A_STAGE, A_STAGE, &full[stage]);
+          bulk_load(sA + A_STAGE, msrc + static_cast<int64_t>(kt) * META_STAGE, META_STAGE, &full[stage]);
           tma_load_2d(sA + A_STAGE + META_STAGE, &tm_x, &full[stage], kt * BK, m0);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -173,7 +195,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (SIDE && ok) {
           if (!mbar_wait(sidee, side_phase ^ 1)) { ok = false; break; }
           mbar_arrive_expect_tx(sidef, BM * 128 + BN * 128);
-          tma_load_2d(side_w2, &tm_w2, sidef, 0, n0);
+          tma_load_2d(side_w2, &tm_w2, sidef, 0, n_tile * BM);
           tma_load_2d(side_x2, &tm_x2, sidef, 0, m0);
           side_phase ^= 1;
         }
@@ -260,36 +282,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------- epilogue
-    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int row = 32 * q + lane;           // weight row within the tile
-    const int et = threadIdx.x - 64;         // 0..127 within the epilogue warps
+    const int ew = warp - 2;                  // 0..7
+    const int q = warp & 3;                   // TMEM lane quadrant this warp may access
+    const int half = ew >> 2;                 // which half of the tile's columns
+    const int row = 32 * q + lane;            // weight row (channel) within the tile
+    const int et = threadIdx.x - 64;          // 0..EPI_THREADS-1
+    const int c0 = half * COLS;               // first accumulator column (token) of this warp
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(32 * q) << 16);
+    // staged output: channel half (row / 64) x BN tokens x 64 channels
+    uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (BN * 64) + (row & 63);
     uint32_t acc_cnt = 0, side_cnt = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const int n0 = (tile % p.n_tiles) * BM;
       const int m0 = (tile / p.n_tiles) * BN;
       const int n = n0 + row;
+      if (et == 0) bulk_wait_read_all();  // the previous tile's store has read the staging buffer
       if (!PROMOTE) {
         const uint32_t b = acc_cnt % NACC;
-        if (!mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) { ok = false; break; }
-        if (SIDE && !mbar_wait(saccf, side_cnt & 1)) { ok = false; break; }
+        if (et < BN) {
+          const int m = m0 + et;
+          scl[et] = m < p.M ? __ldg(&p.sx[m >> p.gM_shift]) : 0.0f;
+        }
+        if (!mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
+        if (SIDE && ok && !mbar_wait(saccf, side_cnt & 1)) ok = false;
+        if (epilogue_bar_any(!ok)) { ok = false; break; }
         tc_fence_after();
         const float swr = __ldg(&p.sw[n >> p.gN_shift]);
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          uint32_t v[16], s2[16];
-          tmem_ld16(lane_base + b * BN + 16 * c, v);
-          if (SIDE) tmem_ld16(lane_base + NACC * BN + 16 * c, s2);
-          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = m0 + 16 * c + j;
-            if (m < p.M) {
-              const float s = __ldg(&p.sx[m >> p.gM_shift]) * swr;
-              const float y = SIDE ? fmaf(s, __uint_as_float(v[j]), __uint_as_float(s2[j]))
-                                   : s * __uint_as_float(v[j]);
-              p.Y[static_cast<int64_t>(m) * p.ldy + n] = __float2bfloat16_rn(y);
+        for (int c = 0; c < COLS; c += CH) {
+          uint32_t v[CH];
+          tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
+          if (SIDE) {
+            uint32_t s2[CH];
+            tmem_load_cols<CH / 8>(lane_base + NACC * BN + c0 + c, s2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const float y = fmaf(scl[c0 + c + j] * swr, __uint_as_float(v[j]), __uint_as_float(s2[j]));
+              out_row[(c0 + c + j) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            }
+          } else {
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const float y = (scl[c0 + c + j] * swr) * __uint_as_float(v[j]);
+              out_row[(c0 + c + j) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
             }
           }
         }
@@ -301,22 +339,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++side_cnt;
         }
       } else {
-        float acc[BN];
+        float acc[COLS];
 #pragma unroll
-        for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < COLS; ++i) acc[i] = 0.0f;
         const bool per_row_w = p.gN_shift == 0;  // gN = 1: weight scale varies by row
         // column scale for K block kt: sx (x sw when the weight scale is uniform over the tile)
         auto col_scale = [&](int kt) -> float {
           const int m = m0 + et;
           if (et >= BN || m >= p.M) return 0.0f;
-          float s = __ldg(&p.sx[static_cast<int64_t>(kt) * p.ldsx + (m >> p.gM_shift)]);
-          if (!per_row_w) s *= __ldg(&p.sw[static_cast<int64_t>(kt) * p.ldsw + (n0 >> p.gN_shift)]);
-          return s;
+          float sc = __ldg(&p.sx[static_cast<int64_t>(kt) * p.ldsx + (m >> p.gM_shift)]);
+          if (!per_row_w) sc *= __ldg(&p.sw[static_cast<int64_t>(kt) * p.ldsw + (n0 >> p.gN_shift)]);
+          return sc;
         };
         float cs_next = col_scale(0);
         float rowf_next = per_row_w ? __ldg(&p.sw[n]) : 1.0f;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          float* csb = cs + (kt & 1) * BN;
+          float* csb = scl + (kt & 1) * BN;
           if (et < BN) csb[et] = cs_next;
           const float rowf = rowf_next;
           if (epilogue_bar_any(!ok)) { ok = false; break; }
@@ -328,48 +366,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) { ok = false; continue; }  // decided at the next barrier
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < BN / 16; ++c) {
-            uint32_t v[16];
-            tmem_ld16(lane_base + b * BN + 16 * c, v);
+          for (int c = 0; c < COLS; c += CH) {
+            uint32_t v[CH];
+            tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int j4 = 0; j4 < 4; ++j4) {
-              const float4 s4 = *reinterpret_cast<const float4*>(csb + 16 * c + 4 * j4);
-              const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const float s = per_row_w ? sc[t] * rowf : sc[t];
-                acc[16 * c + 4 * j4 + t] = fmaf(s, __uint_as_float(v[4 * j4 + t]), acc[16 * c + 4 * j4 + t]);
+            for (int j = 0; j < CH; j += 4) {
+              const float4 s4 = *reinterpret_cast<const float4*>(csb + c0 + c + j);
+              float s0 = s4.x, s1 = s4.y, s2 = s4.z, s3 = s4.w;
+              if (per_row_w) {
+                s0 *= rowf; s1 *= rowf; s2 *= rowf; s3 *= rowf;
               }
+              ffma2(acc[c + j], acc[c + j + 1], __uint_as_float(v[j]), __uint_as_float(v[j + 1]), s0, s1);
+              ffma2(acc[c + j + 2], acc[c + j + 3], __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), s2, s3);
             }
           }
           tc_fence_before();
-          mbar_arrive(&acce[b]);
+          mbar_arrive(&acce[b]);  // partial folded into registers: the MMA may overwrite it
           ++acc_cnt;
         }
         if (epilogue_bar_any(!ok)) { ok = false; break; }
         if (SIDE) {
-          if (!mbar_wait(saccf, side_cnt & 1)) { ok = false; break; }
+          if (!mbar_wait(saccf, side_cnt & 1)) ok = false;
+          if (epilogue_bar_any(!ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < BN / 16; ++c) {
-            uint32_t s2[16];
-            tmem_ld16(lane_base + NACC * BN + 16 * c, s2);
+          for (int c = 0; c < COLS; c += CH) {
+            uint32_t s2[CH];
+            tmem_load_cols<CH / 8>(lane_base + NACC * BN + c0 + c, s2);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[16 * c + j] += __uint_as_float(s2[j]);
+            for (int j = 0; j < CH; ++j) acc[c + j] += __uint_as_float(s2[j]);
           }
           tc_fence_before();
           mbar_arrive(sacce);
           ++side_cnt;
         }
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          const int m = m0 + i;
-          if (m < p.M) p.Y[static_cast<int64_t>(m) * p.ldy + n] = __float2bfloat16_rn(acc[i]);
-        }
+        for (int j = 0; j < COLS; ++j) out_row[(c0 + j) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+      }
+      // hand the staged tile to the TMA engine: rows past M are clipped by it
+      fence_proxy_async_smem();
+      epilogue_bar();
+      if (et == 0) {
+        tma_store_2d(&tm_y, out_tile, n0, m0);
+        tma_store_2d(&tm_y, out_tile + BN * 128, n0 + 64, m0);
+        bulk_commit();
       }
     }
+    if (et == 0) bulk_wait_all();
     if (!ok) atomicOr(p.err, DEVERR_TIMEOUT_EPILOGUE);
   }
 
@@ -382,8 +427,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <int BN, bool PROMOTE, bool SIDE>
-sp24_status launch(const DeviceInfo* dev, const CUtensorMap& a, const CUtensorMap& m, const CUtensorMap& x,
-                   const CUtensorMap& w2, const CUtensorMap& x2, const GemmArgs& args, cudaStream_t stream) {
+sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2, const CUtensorMap& x2,
+                   const CUtensorMap& y, const GemmArgs& args, cudaStream_t stream) {
   using C = Cfg<BN, PROMOTE, SIDE>;
   auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE>;
   static bool attr_done[64] = {};
@@ -395,19 +440,18 @@ sp24_status launch(const DeviceInfo* dev, const CUtensorMap& a, const CUtensorMa
   }
   const int tiles = args.m_tiles * args.n_tiles;
   const int grid = tiles < dev->sm_count ? tiles : dev->sm_count;
-  kern<<<grid, NUM_THREADS, C::SMEM, stream>>>(a, m, x, w2, x2, args);
+  kern<<<grid, NUM_THREADS, C::SMEM, stream>>>(x, w2, x2, y, args);
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }
 
 template <bool PROMOTE, bool SIDE>
-sp24_status launch_bn(int bn, const DeviceInfo* dev, const CUtensorMap& a, const CUtensorMap& m,
-                      const CUtensorMap& x, const CUtensorMap& w2, const CUtensorMap& x2, const GemmArgs& args,
-                      cudaStream_t s) {
+sp24_status launch_bn(int bn, const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2,
+                      const CUtensorMap& x2, const CUtensorMap& y, const GemmArgs& args, cudaStream_t s) {
   switch (bn) {
-    case 16: return launch<16, PROMOTE, SIDE>(dev, a, m, x, w2, x2, args, s);
-    case 32: return launch<32, PROMOTE, SIDE>(dev, a, m, x, w2, x2, args, s);
-    case 64: return launch<64, PROMOTE, SIDE>(dev, a, m, x, w2, x2, args, s);
-    default: return launch<128, PROMOTE, SIDE>(dev, a, m, x, w2, x2, args, s);
+    case 16: return launch<16, PROMOTE, SIDE>(dev, x, w2, x2, y, args, s);
+    case 32: return launch<32, PROMOTE, SIDE>(dev, x, w2, x2, y, args, s);
+    case 64: return launch<64, PROMOTE, SIDE>(dev, x, w2, x2, y, args, s);
+    default: return launch<128, PROMOTE, SIDE>(dev, x, w2, x2, y, args, s);
   }
 }
 
@@ -445,22 +489,17 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
     if (!aligned16(X2) || !aligned16(W2)) return SP24_ERR_ALIGNMENT;
   }
   if (!aligned16(Xq) || !aligned16(values) || !aligned16(meta) || ldx % 16 != 0) return SP24_ERR_ALIGNMENT;
-  if ((reinterpret_cast<uintptr_t>(sx) | reinterpret_cast<uintptr_t>(sw)) % 4 != 0 ||
-      reinterpret_cast<uintptr_t>(Y) % 2 != 0)
-    return SP24_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(sx) | reinterpret_cast<uintptr_t>(sw)) % 4 != 0) return SP24_ERR_ALIGNMENT;
+  if (!aligned16(Y) || ldy % 8 != 0) return SP24_ERR_ALIGNMENT;
   const DeviceInfo* dev = nullptr;
   sp24_status st = current_device(&dev);
   if (st != SP24_OK) return st;
 
   const int bn = pick_bn(M);
-  CUtensorMap tm_a, tm_m, tm_x, tm_w2, tm_x2;
-  st = make_tmap_2d(&tm_a, values, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, BK / 2, BM,
-                    CU_TENSOR_MAP_SWIZZLE_64B);
+  CUtensorMap tm_x, tm_w2, tm_x2, tm_y;
+  st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == SP24_OK)
-    st = make_tmap_2d(&tm_m, meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 8, N, K / 8, BK / 8, BM,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st == SP24_OK)
-    st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+    st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, bn, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st == SP24_OK && side) {
     st = make_tmap_2d(&tm_w2, W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, N, r * 2, 64, BM,
                       CU_TENSOR_MAP_SWIZZLE_128B);
@@ -468,16 +507,16 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
       st = make_tmap_2d(&tm_x2, X2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, M, r * 2, 64, bn,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    tm_w2 = tm_a;
-    tm_x2 = tm_a;
+    tm_w2 = tm_x;
+    tm_x2 = tm_x;
   }
   if (st != SP24_OK) return st;
 
   GemmArgs a;
+  a.values = static_cast<const uint8_t*>(values);
+  a.meta = static_cast<const uint8_t*>(meta);
   a.sx = sx;
   a.sw = sw;
-  a.Y = static_cast<__nv_bfloat16*>(Y);
-  a.ldy = ldy;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
@@ -494,8 +533,8 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool promote = (gK == 128 && K != 128);
   if (promote)
-    return side ? launch_bn<true, true>(bn, dev, tm_a, tm_m, tm_x, tm_w2, tm_x2, a, s)
-                : launch_bn<true, false>(bn, dev, tm_a, tm_m, tm_x, tm_w2, tm_x2, a, s);
-  return side ? launch_bn<false, true>(bn, dev, tm_a, tm_m, tm_x, tm_w2, tm_x2, a, s)
-              : launch_bn<false, false>(bn, dev, tm_a, tm_m, tm_x, tm_w2, tm_x2, a, s);
+    return side ? launch_bn<true, true>(bn, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
+                : launch_bn<true, false>(bn, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
+  return side ? launch_bn<false, true>(bn, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
+              : launch_bn<false, false>(bn, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
 }

@@ -70,6 +70,7 @@ def test_compress_argument_errors(lib):
     assert call(gN=2) == 2
     assert call(gN=128, gK=512) == 2
     assert call(gN=128, gK=128, N=200) == 1
+    assert call(N=100) == 1          # tiled storage: whole 128-row bands
     assert call(W=FAKE_ODD) == 3
     assert call(ldw=516) == 3        # row stride not 16-byte aligned
 
@@ -98,6 +99,7 @@ def test_gemm_argument_errors(lib):
     assert call(r=128, X2=FAKE, W2=FAKE) == 2
     assert call(X=FAKE_ODD) == 3
     assert call(ldx=520) == 3
+    assert call(ldy=260) == 3        # output rows must stay 16-byte aligned
 
 
 def test_quantize_argument_errors(lib):

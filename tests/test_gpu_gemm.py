@@ -33,7 +33,15 @@ def _prep(ora, w: inputs.Workload):
     return xq, sx, values, meta, sw, x2, w2
 
 
+def _abi(ora, values, meta):
+    """Logical (values, meta) -> the tiled storage the library reads, as [N, K/2] / [N, K/8]."""
+    N = values.shape[0]
+    return (ora.tile_values(values).reshape(N, -1), ora.tile_meta(meta).reshape(N, -1))
+
+
 def _run_gpu(sp24, w, xq, sx, values, meta, sw, x2, w2):
+    import oracle as ora
+    values, meta = _abi(ora, values, meta)
     y = sp24.gemm(dev(xq), dev(sx), dev(values), dev(meta), dev(sw), w.gM, w.gN, w.gk,
                   None if x2 is None else dev(x2), None if w2 is None else dev(w2))
     torch.cuda.synchronize()
@@ -90,7 +98,8 @@ def test_identity_dequantize(ora, sp24):
     values, meta, sw = ora.compress(inputs.bf16_bits(W))
     xq = np.where(np.eye(K, dtype=bool), 0x38, 0).astype(np.uint8)
     sx = np.ones((1, K), np.float32)
-    y = sp24.gemm(dev(xq), dev(sx), dev(values), dev(meta), dev(sw))
+    tv, tm = _abi(ora, values, meta)
+    y = sp24.gemm(dev(xq), dev(sx), dev(tv), dev(tm), dev(sw))
     torch.cuda.synchronize()
     Wq = ora.e4m3_decode(ora.decompress(values, meta))
     ref = torch.from_numpy((Wq * sw[0][:, None]).astype(np.float32).T.copy()).to(torch.bfloat16)
@@ -101,8 +110,8 @@ def test_all_zero_weight(ora, sp24):
     M, N, K = 64, 128, 256
     X, _, _, _ = inputs.generate(inputs.Workload("z", M, N, K, seed=1))
     xq, sx = ora.quantize_act(X.numpy())
-    values, meta, sw = ora.compress(np.zeros((N, K), np.uint16))
-    y = sp24.gemm(dev(xq), dev(sx), dev(values), dev(meta), dev(sw))
+    values, meta, sw = ora.compress_abi(np.zeros((N, K), np.uint16))
+    y = sp24.gemm(dev(xq), dev(sx), dev(values.reshape(N, -1)), dev(meta.reshape(N, -1)), dev(sw))
     torch.cuda.synchronize()
     assert (y.float() == 0).all()
 
@@ -129,6 +138,7 @@ def test_one_hot_weight_patterns(ora, sp24):
 def test_repeat_is_deterministic(ora, sp24):
     w = inputs.Workload("det", 300, 384, 1024, gN=128, gK=128, seed=77)
     xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+    values, meta = _abi(ora, values, meta)
     a = [dev(t) for t in (xq, sx, values, meta, sw)]
     y1 = sp24.gemm(*a, w.gM, w.gN, w.gk)
     y2 = sp24.gemm(*a, w.gM, w.gN, w.gk)

@@ -361,3 +361,40 @@ def test_oracle_shares_nothing_with_cuda_path():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 txt = open(os.path.join(dirpath, f)).read()
                 assert not bad_in_pkg.search(txt), f
+
+
+# --------------------------------------------------------- storage layout
+def test_tiled_layout_is_a_permutation(ora):
+    N, K = 256, 512
+    rng = np.random.default_rng(0)
+    v = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    m = rng.integers(0, 256, (N, K // 8), dtype=np.uint8)
+    tv, tm = ora.tile_values(v), ora.tile_meta(m)
+    assert np.array_equal(ora.untile_values(tv, N, K), v)
+    assert np.array_equal(ora.untile_meta(tm, N, K), m)
+    # distinct positions: tile an index pattern and check every slot is hit once
+    idx = np.arange(N * K // 2, dtype=np.int64)
+    hit = np.zeros(N * K // 2, dtype=np.int64)
+    for shift in (0, 8, 16):
+        t = ora.tile_values(((idx >> shift) & 0xFF).astype(np.uint8).reshape(N, K // 2))
+        hit += t.astype(np.int64) << shift
+    assert np.array_equal(np.sort(hit), idx)
+
+
+def test_tiled_layout_known_positions(ora):
+    """Hand-computed positions: tile (n-band, k-block) order, row pitch 64 B,
+    16-byte chunks XOR-swizzled with (row/2) mod 4; metadata rows of 16 B."""
+    N, K = 256, 512
+    v = np.zeros((N, K // 2), np.uint8)
+    v[0, 0] = 1        # tile 0, row 0, chunk 0 -> offset 0
+    v[2, 0] = 2        # row 2: chunk 0 ^ 1 = 1 -> 2*64 + 16 = 144
+    v[7, 17] = 3       # row 7: (7//2)%4 = 3, chunk 1 ^ 3 = 2 -> 7*64 + 32 + 1 = 481
+    v[0, 64] = 4       # second K tile of band 0 -> 8192
+    v[130, 70] = 5     # band 1 (tiles 4..7), k tile 1 -> tile 5; row 2, b 6, chunk 0^1 -> 5*8192 + 128 + 16 + 6
+    t = ora.tile_values(v)
+    assert t[0] == 1 and t[144] == 2 and t[481] == 3 and t[8192] == 4 and t[5 * 8192 + 150] == 5
+    m = np.zeros((N, K // 8), np.uint8)
+    m[1, 3] = 7        # tile 0: 1*16 + 3
+    m[129, 20] = 9     # band 1, k tile 1 -> tile 5: 1*16 + 4
+    tm = ora.tile_meta(m)
+    assert tm[19] == 7 and tm[5 * 2048 + 20] == 9
