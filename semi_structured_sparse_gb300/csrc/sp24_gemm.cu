@@ -42,30 +42,40 @@ constexpr int META_STAGE = BM * BK / 8;  // metadata: one 2 KB storage tile
 constexpr int META_COL0 = 448;           // TMEM columns 448..511: metadata ring
 constexpr int META_SLOTS = 16;           // 4 columns each
 constexpr int MAX_STAGES = 16;
+constexpr int PRODUCERS = 2;             // load warps; warp p issues the stages p, p + 2, ...
+constexpr int MMA_WARP = PRODUCERS;
+constexpr int EPI_WARP0 = PRODUCERS + 1;
 constexpr int EPI_WARPS = 8;             // two per TMEM lane quadrant, each half of the columns
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
-constexpr int NUM_THREADS = 64 + EPI_THREADS;
+constexpr int NUM_THREADS = 32 * EPI_WARP0 + EPI_THREADS;
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr int BAR_BYTES = 1024;
 
-template <int BN, bool PROMOTE, bool SIDE>
+template <int BN, bool PROMOTE, bool SIDE, int CL>
 struct Cfg {
-  static constexpr int B_STAGE = BN * BK;  // e4m3 activations, 128 B per token row
-  static constexpr int STAGE = A_STAGE + META_STAGE + B_STAGE;
+  static constexpr int B_STAGE = BN * BK;            // e4m3 activations, 128 B per token row
+  static constexpr int SCL_STAGE = PROMOTE ? 1024 : 0;  // per-stage scales: sx[BN] then sw[128]
+  static constexpr int STAGE = A_STAGE + META_STAGE + B_STAGE + SCL_STAGE;
   static constexpr int SIDE_BYTES = SIDE ? (BM * 128 + BN * 128) : 0;
-  static constexpr int OUT_BYTES = BN * BM * 2;  // bf16 output tile staged for the TMA store
-  static constexpr int NACC = (PROMOTE && !SIDE && 3 * BN <= META_COL0) ? 3 : 2;
-  static constexpr int SCALE_BYTES = 4 * BN * (PROMOTE ? 2 : 1);
+  // bf16 output staged for the TMA store: the whole tile, or (BN = 256) half of it at a time
+  static constexpr int OUT_TOKENS = BN > 128 ? BN / 2 : BN;
+  static constexpr int OUT_BYTES = OUT_TOKENS * BM * 2;
+  static constexpr int NACC = BN > 128 ? 1 : ((PROMOTE && !SIDE && 3 * BN <= META_COL0) ? 3 : 2);
+  static constexpr int SCALE_BYTES = 4 * BN;
   static constexpr int FIXED = 1024 + SIDE_BYTES + OUT_BYTES + SCALE_BYTES + BAR_BYTES;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE;
   static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
   static constexpr int SMEM = FIXED + STAGES * STAGE;
-  static constexpr int COLS = BN / 2;  // accumulator columns (tokens) per epilogue warp
+  static constexpr int COLS = BN / 2;        // accumulator columns (tokens) per epilogue warp
+  static constexpr int SLICE = BN / CL;      // activation rows each CTA of a cluster loads and multicasts
   static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(STAGES >= 2, "need at least two stages");
   static_assert(NACC * BN + (SIDE ? BN : 0) <= META_COL0, "TMEM columns");
   static_assert(STAGES <= META_SLOTS, "metadata ring must cover the stage ring");
   static_assert(COLS % 8 == 0, "epilogue chunking");
+  static_assert(BN <= 128 || (!PROMOTE && !SIDE), "256-token tiles: plain per-tensor-K scaling only");
+  static_assert(!PROMOTE || BN <= 128, "per-stage scale slot holds BN + 128 floats");
+  static_assert(SLICE % 8 == 0, "multicast slices must keep the 1024-byte swizzle atom");
 };
 
 struct GemmArgs {
@@ -107,26 +117,36 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
   }
 }
 
-template <int BN, bool PROMOTE, bool SIDE>
+// Tile schedule: CL CTAs of a cluster take CL consecutive weight tiles of
+// the same token tile (and share its activation loads); clusters walk the
+// (token tile, weight-tile group) space round-robin.
+struct TileIter {
+  int group, ngroups, step, n_groups_per_m;
+  __device__ bool valid() const { return group < ngroups; }
+  __device__ void next() { group += step; }
+};
+
+template <int BN, bool PROMOTE, bool SIDE, int CL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sp24_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w2,
                      const __grid_constant__ CUtensorMap tm_x2, const __grid_constant__ CUtensorMap tm_y,
                      const GemmArgs p) {
-  using C = Cfg<BN, PROMOTE, SIDE>;
+  using C = Cfg<BN, PROMOTE, SIDE, CL>;
   constexpr int STAGES = C::STAGES;
   constexpr int NACC = C::NACC;
   constexpr int COLS = C::COLS;
   constexpr int CH = COLS >= 16 ? 16 : COLS;  // columns per TMEM load
+  constexpr uint16_t CL_MASK = static_cast<uint16_t>((1u << CL) - 1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = sm;
   uint8_t* side_w2 = sm + STAGES * C::STAGE;
   uint8_t* side_x2 = side_w2 + BM * 128;
-  uint8_t* out_tile = sm + STAGES * C::STAGE + C::SIDE_BYTES;      // [2 halves][BN tokens][64 channels] bf16
-  float* scl = reinterpret_cast<float*>(out_tile + C::OUT_BYTES);  // token scales, [1 or 2][BN]
+  uint8_t* out_tile = sm + STAGES * C::STAGE + C::SIDE_BYTES;      // [2 halves][tokens][64 channels] bf16
+  float* scl = reinterpret_cast<float*>(out_tile + C::OUT_BYTES);  // per-tile token scales [BN]
   uint64_t* bars = reinterpret_cast<uint64_t*>(out_tile + C::OUT_BYTES + C::SCALE_BYTES);
   uint64_t* full = bars;                   // [STAGES] loads -> MMA
-  uint64_t* empty = bars + MAX_STAGES;     // [STAGES] MMA -> loads
+  uint64_t* empty = bars + MAX_STAGES;     // [STAGES] MMA (and promotion epilogue) -> loads, cluster-wide
   uint64_t* accf = bars + 2 * MAX_STAGES;  // [NACC]  MMA -> epilogue
   uint64_t* acce = accf + 3;               // [NACC]  epilogue -> MMA
   uint64_t* sidef = acce + 3;              // side operands loaded
@@ -137,10 +157,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = CL > 1 ? cluster_rank() : 0u;
+  TileIter it0;
+  it0.n_groups_per_m = p.n_tiles / CL;
+  it0.ngroups = p.m_tiles * it0.n_groups_per_m;
+  it0.group = CL > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  it0.step = CL > 1 ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
+  auto tile_n = [&](const TileIter& t) { return (t.group % t.n_groups_per_m) * CL + static_cast<int>(crank); };
+  auto tile_m = [&](const TileIter& t) { return t.group / t.n_groups_per_m; };
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&full[i], 1 + (PROMOTE ? 32 : 0));
+      mbar_init(&empty[i], CL + (PROMOTE ? EPI_WARPS : 0));
     }
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&accf[i], 1);
@@ -153,7 +182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(drain, 1);
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == MMA_WARP + 1 && lane == 0) {
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_y);
     if (SIDE) {
@@ -161,62 +190,107 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&tm_x2);
     }
   }
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (CL > 1) cluster_sync();  // every CTA's barriers exist before anyone multicasts to them
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const int num_tiles = p.m_tiles * p.n_tiles;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, side_phase = 0;
-      int64_t issued = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int n_tile = tile % p.n_tiles;
-        const int m0 = (tile / p.n_tiles) * BN;
-        const uint8_t* vsrc = p.values + static_cast<int64_t>(n_tile) * p.k_tiles * A_STAGE;
-        const uint8_t* msrc = p.meta + static_cast<int64_t>(n_tile) * p.k_tiles * META_STAGE;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
-          uint8_t* sA = ring + stage * C::STAGE;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE);
+  if (warp < PRODUCERS) {
+    // ----------------------------------------------------------- producers
+    // Every mbarrier operation costs its thread a round trip, so stages are
+    // dealt out to PRODUCERS warps in turn (warp p takes flat stage indices
+    // p, p + PRODUCERS, ...).  Lane 0 issues the bulk/TMA copies; with
+    // promotion all 32 lanes also copy the stage's scale vectors (cp.async,
+    // zero-filled past M).
+    const int pw = warp;
+    int64_t flat = 0;  // stage index over this CTA's whole tile sequence
+    uint32_t side_phase = 0;
+    bool ok = true;
+    for (TileIter t = it0; t.valid() && ok; t.next()) {
+      const int n_tile = tile_n(t);
+      const int n0 = n_tile * BM;
+      const int m0 = tile_m(t) * BN;
+      const uint8_t* vsrc = p.values + static_cast<int64_t>(n_tile) * p.k_tiles * A_STAGE;
+      const uint8_t* msrc = p.meta + static_cast<int64_t>(n_tile) * p.k_tiles * META_STAGE;
+      for (int kt = 0; kt < p.k_tiles; ++kt, ++flat) {
+        if (flat % PRODUCERS != pw) continue;
+        const uint32_t stage = static_cast<uint32_t>(flat % STAGES);
+        const uint32_t phase = static_cast<uint32_t>((flat / STAGES) & 1);
+        const bool got = mbar_wait(&empty[stage], phase ^ 1);
+        if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
+        uint8_t* sA = ring + stage * C::STAGE;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], A_STAGE + META_STAGE + C::B_STAGE);
           bulk_load(sA, vsrc + static_cast<int64_t>(kt) * A_STAGE, A_STAGE, &full[stage]);
           bulk_load(sA + A_STAGE, msrc + static_cast<int64_t>(kt) * META_STAGE, META_STAGE, &full[stage]);
-          tma_load_2d(sA + A_STAGE + META_STAGE, &tm_x, &full[stage], kt * BK, m0);
-          ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          uint8_t* sB = sA + A_STAGE + META_STAGE;
+          if (CL == 1)
+            tma_load_2d(sB, &tm_x, &full[stage], kt * BK, m0);
+          else
+            tma_load_2d_multicast(sB + crank * (C::SLICE * 128), &tm_x, &full[stage], kt * BK,
+                                  m0 + static_cast<int>(crank) * C::SLICE, CL_MASK);
         }
-        if (SIDE && ok) {
-          if (!mbar_wait(sidee, side_phase ^ 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(sidef, BM * 128 + BN * 128);
-          tma_load_2d(side_w2, &tm_w2, sidef, 0, n_tile * BM);
-          tma_load_2d(side_x2, &tm_x2, sidef, 0, m0);
-          side_phase ^= 1;
+        if (PROMOTE) {
+          float* ssl = reinterpret_cast<float*>(sA + A_STAGE + META_STAGE + C::B_STAGE);
+          const float* sxk = p.sx + static_cast<int64_t>(kt) * p.ldsx;
+          for (int i = lane; i < BN; i += 32) {
+            const int m = m0 + i;
+            cp_async_4(&ssl[i], sxk + ((m < p.M ? m : p.M - 1) >> p.gM_shift), m < p.M ? 4u : 0u);
+          }
+          const float* swk = p.sw + static_cast<int64_t>(kt) * p.ldsw;
+          if (p.gN_shift == 0) {
+            for (int i = lane; i < BM; i += 32) cp_async_4(&ssl[BN + i], swk + n0 + i, 4u);
+          } else if (lane == 0) {
+            cp_async_4(&ssl[BN], swk + (n0 >> p.gN_shift), 4u);
+          }
+          cp_async_arrive(&full[stage]);
         }
       }
-      if (!ok) {
-        atomicOr(p.err, DEVERR_TIMEOUT_PRODUCER);
-        // let every load already issued land before the CTA's shared memory goes away
-        const int64_t first = issued > STAGES ? issued - STAGES : 0;
-        for (int64_t i = first; i < issued; ++i)
-          (void)mbar_wait(&full[i % STAGES], static_cast<uint32_t>((i / STAGES) & 1));
+      if (SIDE && ok && pw == 0) {
+        const bool got = mbar_wait(sidee, side_phase ^ 1);
+        if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(sidef, BM * 128 + BN * 128);
+          tma_load_2d(side_w2, &tm_w2, sidef, 0, n0);
+          tma_load_2d(side_x2, &tm_x2, sidef, 0, m0);
+        }
+        side_phase ^= 1;
       }
     }
-  } else if (warp == 1) {
+    if (lane == 0) {
+      if (!ok) atomicOr(p.err, DEVERR_TIMEOUT_PRODUCER);
+      // Before leaving: every stage this warp issued has landed (so nothing writes
+      // this CTA's shared memory later) and, with a cluster, every consumer of the
+      // last use of each of those slots -- in every CTA -- has arrived on this
+      // CTA's empty barrier.  Only the last use of a slot may be waited on (an
+      // older phase of the same parity would not be seen as complete).
+      const int64_t fmax = flat - 1;
+      for (int64_t f = fmax; f >= 0 && f > fmax - STAGES; --f) {
+        if (f % PRODUCERS != pw) continue;
+        (void)mbar_wait(&full[f % STAGES], static_cast<uint32_t>((f / STAGES) & 1));
+        (void)mbar_wait(&empty[f % STAGES], static_cast<uint32_t>((f / STAGES) & 1));
+      }
+    }
+  } else if (warp == MMA_WARP) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_sp = idesc_e4m3(BM, BN, true);
       constexpr uint32_t idesc_side = idesc_bf16(BM, BN);
+      constexpr uint64_t STAGE_DESC = C::STAGE >> 4;  // descriptor start-address units per stage
+      // stage-0 descriptors; a stage is a fixed offset in the start-address field
+      const uint32_t ring_u32 = smem_u32(ring);
+      const uint64_t a_desc0 = smem_desc(ring_u32, 16, 512, SWZ_64B);
+      const uint64_t m_desc0 = smem_desc(ring_u32 + A_STAGE, 128, 128, SWZ_NONE);
+      const uint64_t b_desc0 = smem_desc(ring_u32 + A_STAGE + META_STAGE, 16, 1024, SWZ_128B);
       uint32_t stage = 0, phase = 0, side_cnt = 0, meta_ctr = 0;
       uint32_t acc_cnt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (TileIter t = it0; t.valid() && ok; t.next()) {
         uint32_t d = 0;
         if (!PROMOTE) {
           const uint32_t b = acc_cnt % NACC;
@@ -233,21 +307,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             d = tbase + b * BN;
           }
           if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sA = smem_u32(ring + stage * C::STAGE);
-          const uint32_t sMeta = sA + A_STAGE;
-          const uint32_t sB = sMeta + META_STAGE;
-          const uint32_t mcol = tbase + META_COL0 + 4 * (meta_ctr % META_SLOTS);
+          const uint64_t off = stage * STAGE_DESC;
+          const uint32_t mcol = tbase + META_COL0 + 4 * (meta_ctr & (META_SLOTS - 1));
           ++meta_ctr;
-          tmem_cp_128x128b(mcol, smem_desc(sMeta, 128, 128, SWZ_NONE));
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint64_t da = smem_desc(sA + 32 * j, 16, 512, SWZ_64B);
-            const uint64_t db = smem_desc(sB + 64 * j, 16, 1024, SWZ_128B);
-            const uint32_t accumulate = PROMOTE ? (j > 0) : ((kt | j) != 0);
-            mma_sp_e4m3(d, da, db, mcol + 2 * j, idesc_sp, accumulate);
-          }
-          mma_commit(&empty[stage]);
+          tmem_cp_128x128b(mcol, m_desc0 + off);
+          const uint32_t acc0 = PROMOTE ? 0u : (kt != 0 ? 1u : 0u);
+          mma_sp_e4m3(d, a_desc0 + off, b_desc0 + off, mcol, idesc_sp, acc0);
+          mma_sp_e4m3(d, a_desc0 + off + 2, b_desc0 + off + 4, mcol + 2, idesc_sp, 1u);  // +32 B of A, +64 B of B
+          if (CL > 1) mma_commit_multicast(&empty[stage], CL_MASK);
+          else mma_commit(&empty[stage]);
           if (PROMOTE) {
             mma_commit(&accf[b]);
             ++acc_cnt;
@@ -274,28 +342,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++acc_cnt;
         }
       }
-      if (!ok) {
-        atomicOr(p.err, DEVERR_TIMEOUT_MMA);
-        mma_commit(drain);  // every MMA issued so far must finish before TMEM is freed
-        (void)mbar_wait(drain, 0);
-      }
+      if (!ok) atomicOr(p.err, DEVERR_TIMEOUT_MMA);
+      mma_commit(drain);  // every MMA issued so far must finish before TMEM is freed
+      (void)mbar_wait(drain, 0);
     }
   } else {
     // ------------------------------------------------------------- epilogue
-    const int ew = warp - 2;                  // 0..7
+    const int ew = warp - EPI_WARP0;          // 0..7
     const int q = warp & 3;                   // TMEM lane quadrant this warp may access
     const int half = ew >> 2;                 // which half of the tile's columns
     const int row = 32 * q + lane;            // weight row (channel) within the tile
-    const int et = threadIdx.x - 64;          // 0..EPI_THREADS-1
+    const int et = threadIdx.x - 32 * EPI_WARP0;  // 0..EPI_THREADS-1
     const int c0 = half * COLS;               // first accumulator column (token) of this warp
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(32 * q) << 16);
-    // staged output: channel half (row / 64) x BN tokens x 64 channels
-    uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (BN * 64) + (row & 63);
-    uint32_t acc_cnt = 0, side_cnt = 0;
+    // staged output: channel half (row / 64) x tokens x 64 channels
+    uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (C::OUT_TOKENS * 64) + (row & 63);
+    uint32_t acc_cnt = 0, side_cnt = 0, e_stage = 0, e_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const int n0 = (tile % p.n_tiles) * BM;
-      const int m0 = (tile / p.n_tiles) * BN;
+    for (TileIter t = it0; t.valid() && ok; t.next()) {
+      const int n0 = tile_n(t) * BM;
+      const int m0 = tile_m(t) * BN;
       const int n = n0 + row;
       if (et == 0) bulk_wait_read_all();  // the previous tile's store has read the staging buffer
       if (!PROMOTE) {
@@ -309,6 +375,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (epilogue_bar_any(!ok)) { ok = false; break; }
         tc_fence_after();
         const float swr = __ldg(&p.sw[n >> p.gN_shift]);
+        if constexpr (BN > 128) {
+          // one accumulator: copy this warp's 128 columns to registers and free
+          // TMEM at once, so the next tile's MMAs overlap the rest of the epilogue
+          uint32_t v[COLS];
+#pragma unroll
+          for (int c = 0; c < COLS; c += 16) tmem_ld16(lane_base + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&acce[b]);
+          ++acc_cnt;
+          // two passes through the half-size staging buffer: tokens [0,128), then [128,256)
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass) {
+            if (half == pass) {
+#pragma unroll
+              for (int j = 0; j < COLS; ++j) {
+                const float y = (scl[c0 + j] * swr) * __uint_as_float(v[j]);
+                out_row[j * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+              }
+            }
+            fence_proxy_async_smem();
+            epilogue_bar();
+            if (et == 0) {
+              tma_store_2d(&tm_y, out_tile, n0, m0 + pass * C::OUT_TOKENS);
+              tma_store_2d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0 + pass * C::OUT_TOKENS);
+              bulk_commit();
+              if (pass == 0) bulk_wait_read_all();
+            }
+            if (pass == 0) epilogue_bar();
+          }
+          continue;
+        }
 #pragma unroll
         for (int c = 0; c < COLS; c += CH) {
           uint32_t v[CH];
@@ -339,51 +437,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++side_cnt;
         }
       } else {
+        // promotion: each K block's partial arrives in its own accumulator buffer;
+        // its scales travel in the same pipeline stage (sx[BN], then sw)
         float acc[COLS];
 #pragma unroll
         for (int i = 0; i < COLS; ++i) acc[i] = 0.0f;
         const bool per_row_w = p.gN_shift == 0;  // gN = 1: weight scale varies by row
-        // column scale for K block kt: sx (x sw when the weight scale is uniform over the tile)
-        auto col_scale = [&](int kt) -> float {
-          const int m = m0 + et;
-          if (et >= BN || m >= p.M) return 0.0f;
-          float sc = __ldg(&p.sx[static_cast<int64_t>(kt) * p.ldsx + (m >> p.gM_shift)]);
-          if (!per_row_w) sc *= __ldg(&p.sw[static_cast<int64_t>(kt) * p.ldsw + (n0 >> p.gN_shift)]);
-          return sc;
-        };
-        float cs_next = col_scale(0);
-        float rowf_next = per_row_w ? __ldg(&p.sw[n]) : 1.0f;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          float* csb = scl + (kt & 1) * BN;
-          if (et < BN) csb[et] = cs_next;
-          const float rowf = rowf_next;
-          if (epilogue_bar_any(!ok)) { ok = false; break; }
-          if (kt + 1 < p.k_tiles) {
-            cs_next = col_scale(kt + 1);
-            if (per_row_w) rowf_next = __ldg(&p.sw[static_cast<int64_t>(kt + 1) * p.ldsw + n]);
-          }
           const uint32_t b = acc_cnt % NACC;
-          if (!mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) { ok = false; continue; }  // decided at the next barrier
-          tc_fence_after();
+          const float* ssl = reinterpret_cast<const float*>(ring + e_stage * C::STAGE + A_STAGE + META_STAGE +
+                                                            C::B_STAGE);
+          if (ok && !mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
+          if (ok && !mbar_wait(&full[e_stage], e_phase)) ok = false;  // scales visible (already complete)
+          if (ok) {
+            tc_fence_after();
+            const float rowf = per_row_w ? ssl[BN + row] : ssl[BN];
 #pragma unroll
-          for (int c = 0; c < COLS; c += CH) {
-            uint32_t v[CH];
-            tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
-            tmem_ld_wait();
+            for (int c = 0; c < COLS; c += CH) {
+              uint32_t v[CH];
+              tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
+              tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < CH; j += 4) {
-              const float4 s4 = *reinterpret_cast<const float4*>(csb + c0 + c + j);
-              float s0 = s4.x, s1 = s4.y, s2 = s4.z, s3 = s4.w;
-              if (per_row_w) {
-                s0 *= rowf; s1 *= rowf; s2 *= rowf; s3 *= rowf;
+              for (int j = 0; j < CH; j += 4) {
+                const float4 s4 = *reinterpret_cast<const float4*>(ssl + c0 + c + j);
+                float s0 = s4.x * rowf, s1 = s4.y * rowf, s2 = s4.z * rowf, s3 = s4.w * rowf;
+                ffma2(acc[c + j], acc[c + j + 1], __uint_as_float(v[j]), __uint_as_float(v[j + 1]), s0, s1);
+                ffma2(acc[c + j + 2], acc[c + j + 3], __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), s2,
+                      s3);
               }
-              ffma2(acc[c + j], acc[c + j + 1], __uint_as_float(v[j]), __uint_as_float(v[j + 1]), s0, s1);
-              ffma2(acc[c + j + 2], acc[c + j + 3], __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), s2, s3);
             }
+            tc_fence_before();
           }
-          tc_fence_before();
           mbar_arrive(&acce[b]);  // partial folded into registers: the MMA may overwrite it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[e_stage]);  // this warp is done with the stage's scales
           ++acc_cnt;
+          if (++e_stage == STAGES) { e_stage = 0; e_phase ^= 1; }
         }
         if (epilogue_bar_any(!ok)) { ok = false; break; }
         if (SIDE) {
@@ -410,7 +499,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       epilogue_bar();
       if (et == 0) {
         tma_store_2d(&tm_y, out_tile, n0, m0);
-        tma_store_2d(&tm_y, out_tile + BN * 128, n0 + 64, m0);
+        tma_store_2d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0);
         bulk_commit();
       }
     }
@@ -419,46 +508,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
+  if (CL > 1) cluster_sync();
+  else __syncthreads();
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
 }
 
-template <int BN, bool PROMOTE, bool SIDE>
+template <int BN, bool PROMOTE, bool SIDE, int CL>
 sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2, const CUtensorMap& x2,
                    const CUtensorMap& y, const GemmArgs& args, cudaStream_t stream) {
-  using C = Cfg<BN, PROMOTE, SIDE>;
-  auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE>;
-  static bool attr_done[64] = {};
-  if (!attr_done[dev->ordinal]) {
+  using C = Cfg<BN, PROMOTE, SIDE, CL>;
+  auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE, CL>;
+  static int max_clusters[64] = {};  // per device: co-resident clusters of this instance (0 = not yet known)
+  const int d = dev->ordinal;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters[d] == 0) {
     if (static_cast<size_t>(C::SMEM) > dev->smem_optin) return SP24_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return SP24_ERR_CUDA;
-    attr_done[dev->ordinal] = true;
+    int n = dev->sm_count / CL;
+    if (CL > 1) {
+      cfg.gridDim = dim3(CL * n, 1, 1);
+      int active = 0;
+      if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) return SP24_ERR_CUDA;
+      n = active;
+    }
+    max_clusters[d] = n;
   }
-  const int tiles = args.m_tiles * args.n_tiles;
-  const int grid = tiles < dev->sm_count ? tiles : dev->sm_count;
-  kern<<<grid, NUM_THREADS, C::SMEM, stream>>>(x, w2, x2, y, args);
+  const int groups = args.m_tiles * (args.n_tiles / CL);
+  const int clusters = groups < max_clusters[d] ? groups : max_clusters[d];
+  cfg.gridDim = dim3(CL * clusters, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, x, w2, x2, y, args) != cudaSuccess) return SP24_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }
 
+// Instances: token tiles of 16..64 run without clusters (the weight stream
+// dominates); 128 and 256 share each activation tile across a 4-CTA cluster
+// when the weight tiles divide evenly.
 template <bool PROMOTE, bool SIDE>
-sp24_status launch_bn(int bn, const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2,
+sp24_status launch_bn(int bn, int cl, const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2,
                       const CUtensorMap& x2, const CUtensorMap& y, const GemmArgs& args, cudaStream_t s) {
   switch (bn) {
-    case 16: return launch<16, PROMOTE, SIDE>(dev, x, w2, x2, y, args, s);
-    case 32: return launch<32, PROMOTE, SIDE>(dev, x, w2, x2, y, args, s);
-    case 64: return launch<64, PROMOTE, SIDE>(dev, x, w2, x2, y, args, s);
-    default: return launch<128, PROMOTE, SIDE>(dev, x, w2, x2, y, args, s);
+    case 16: return launch<16, PROMOTE, SIDE, 1>(dev, x, w2, x2, y, args, s);
+    case 32: return launch<32, PROMOTE, SIDE, 1>(dev, x, w2, x2, y, args, s);
+    case 64: return launch<64, PROMOTE, SIDE, 1>(dev, x, w2, x2, y, args, s);
+    case 256:
+      if constexpr (!PROMOTE && !SIDE) {
+        return cl == 4 ? launch<256, false, false, 4>(dev, x, w2, x2, y, args, s)
+                       : launch<256, false, false, 1>(dev, x, w2, x2, y, args, s);
+      }
+      return SP24_ERR_UNSUPPORTED;
+    default:
+      return cl == 4 ? launch<128, PROMOTE, SIDE, 4>(dev, x, w2, x2, y, args, s)
+                     : launch<128, PROMOTE, SIDE, 1>(dev, x, w2, x2, y, args, s);
   }
 }
 
-int pick_bn(int64_t M) {
+// Token tile: the smallest MMA N that covers M, up to 128; 256 for large M
+// when the plain epilogue applies (one accumulator of 256 columns).
+int pick_bn(int64_t M, bool plain) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
+  if (plain && M > 192) return 256;
   return 128;
 }
 
@@ -495,11 +619,14 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   sp24_status st = current_device(&dev);
   if (st != SP24_OK) return st;
 
-  const int bn = pick_bn(M);
+  const bool promote = (gK == 128 && K != 128);
+  const int bn = pick_bn(M, !promote && !side);
   CUtensorMap tm_x, tm_w2, tm_x2, tm_y;
-  st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  const int cl_x = (bn >= 128 && (N / BM) % 4 == 0) ? 4 : 1;  // activation rows per load: the cluster slice
+  st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn / cl_x, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == SP24_OK)
-    st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, bn, CU_TENSOR_MAP_SWIZZLE_NONE);
+    st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, bn > 128 ? bn / 2 : bn,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st == SP24_OK && side) {
     st = make_tmap_2d(&tm_w2, W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, N, r * 2, 64, BM,
                       CU_TENSOR_MAP_SWIZZLE_128B);
@@ -531,10 +658,10 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   a.err = dev->err_word;
   if (static_cast<int64_t>(a.m_tiles) * a.n_tiles > (1 << 30)) return SP24_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool promote = (gK == 128 && K != 128);
+  const int cl = (bn >= 128 && a.n_tiles % 4 == 0) ? 4 : 1;
   if (promote)
-    return side ? launch_bn<true, true>(bn, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
-                : launch_bn<true, false>(bn, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
-  return side ? launch_bn<false, true>(bn, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
-              : launch_bn<false, false>(bn, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
+    return side ? launch_bn<true, true>(bn, cl, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
+                : launch_bn<true, false>(bn, cl, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
+  return side ? launch_bn<false, true>(bn, cl, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
+              : launch_bn<false, false>(bn, cl, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
 }
