@@ -156,6 +156,8 @@ def run_ours(args):
         }
         sets.append(s)
     stream = torch.cuda.current_stream()
+    ws_bytes = sp24.workspace_size(w.M, w.N, w.K, w.r)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def step(s, ev=None):
         if ev is not None:
@@ -163,7 +165,8 @@ def run_ours(args):
         sp24.compress(s["W"], w.gN, gk, out=(s["v"], s["m"], s["sw"]))
         if ev is not None:
             ev[1].record(stream)
-        sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"])
+        sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"],
+                  workspace=ws)
         if ev is not None:
             ev[2].record(stream)
 

@@ -93,6 +93,11 @@ def _dev_tensor(t, dtype, name):
     return t
 
 
+def workspace_size(M: int, N: int, K: int, r: int = 0) -> int:
+    """Device scratch bytes gemm() wants for this shape (0 = none)."""
+    return int(load().sp24_fp8_gemm_workspace_size(M, N, K, r))
+
+
 def meta_bytes(N: int, K: int) -> int:
     return int(load().sp24_meta_bytes(N, K))
 

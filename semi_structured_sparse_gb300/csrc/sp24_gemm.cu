@@ -51,11 +51,20 @@ constexpr int NUM_THREADS = 32 * EPI_WARP0 + EPI_THREADS;
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr int BAR_BYTES = 1024;
 
-template <int BN, bool PROMOTE, bool SIDE, int CL>
+// A pipeline stage carries KS consecutive 128-K sub-tiles: the kept values
+// of all KS (one contiguous copy), their metadata (one copy), then KS
+// activation boxes.  Small token tiles use KS > 1 so that each barrier
+// round trip and metadata copy is amortised over more MMAs.
+template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS>
 struct Cfg {
-  static constexpr int B_STAGE = BN * BK;            // e4m3 activations, 128 B per token row
+  static constexpr int B_SUB = BN * BK;               // e4m3 activations of one sub-tile, 128 B per token row
+  static constexpr int A_OFF = 0;
+  static constexpr int META_OFF = KS * A_STAGE;
+  static constexpr int B_OFF = KS * (A_STAGE + META_STAGE);
+  static constexpr int SCL_OFF = B_OFF + KS * B_SUB;
   static constexpr int SCL_STAGE = PROMOTE ? 1024 : 0;  // per-stage scales: sx[BN] then sw[128]
-  static constexpr int STAGE = A_STAGE + META_STAGE + B_STAGE + SCL_STAGE;
+  static constexpr int STAGE = SCL_OFF + SCL_STAGE;
+  static constexpr int LOAD_BYTES = KS * (A_STAGE + META_STAGE + B_SUB);
   static constexpr int SIDE_BYTES = SIDE ? (BM * 128 + BN * 128) : 0;
   // bf16 output staged for the TMA store: the whole tile, or (BN = 256) half of it at a time
   static constexpr int OUT_TOKENS = BN > 128 ? BN / 2 : BN;
@@ -64,18 +73,17 @@ struct Cfg {
   static constexpr int SCALE_BYTES = 4 * BN;
   static constexpr int FIXED = 1024 + SIDE_BYTES + OUT_BYTES + SCALE_BYTES + BAR_BYTES;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE;
-  static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
+  static constexpr int STAGES_CAP = META_SLOTS / KS;  // metadata ring covers every sub-tile in flight
+  static constexpr int STAGES = STAGES_FIT < STAGES_CAP ? STAGES_FIT : STAGES_CAP;
   static constexpr int SMEM = FIXED + STAGES * STAGE;
-  static constexpr int COLS = BN / 2;        // accumulator columns (tokens) per epilogue warp
-  static constexpr int SLICE = BN / CL;      // activation rows each CTA of a cluster loads and multicasts
-  static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
+  static constexpr int COLS = BN / 2;  // accumulator columns (tokens) per epilogue warp
+  static_assert(STAGE % 1024 == 0 && B_OFF % 1024 == 0 && B_SUB % 1024 == 0, "1024-byte swizzle alignment");
   static_assert(STAGES >= 2, "need at least two stages");
   static_assert(NACC * BN + (SIDE ? BN : 0) <= META_COL0, "TMEM columns");
-  static_assert(STAGES <= META_SLOTS, "metadata ring must cover the stage ring");
   static_assert(COLS % 8 == 0, "epilogue chunking");
   static_assert(BN <= 128 || (!PROMOTE && !SIDE), "256-token tiles: plain per-tensor-K scaling only");
-  static_assert(!PROMOTE || BN <= 128, "per-stage scale slot holds BN + 128 floats");
-  static_assert(SLICE % 8 == 0, "multicast slices must keep the 1024-byte swizzle atom");
+  static_assert(!PROMOTE || (BN <= 128 && KS == 1), "per-stage scale slot holds one K block of BN + 128 floats");
+  static_assert(!SPLIT || (!PROMOTE && !SIDE && BN <= 128), "split-K: plain per-tensor-K scaling only");
 };
 
 struct GemmArgs {
@@ -88,6 +96,10 @@ struct GemmArgs {
   int gM_shift, gN_shift;  // log2 of the granularities (0 or 7)
   int m_tiles, n_tiles, k_tiles;
   int side_ksteps;  // r / 16
+  int splits;       // K splits per output tile (1 = none)
+  int kt_per_split; // 128-K sub-tiles per split (a multiple of the stage's KS)
+  float* ws;        // split-K partials [tile][split][BN][128] (fp32, unscaled)
+  unsigned int* counters;  // split-K arrival counters [tile], zero on entry
   unsigned int* err;
 };
 
@@ -117,26 +129,33 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
   }
 }
 
-// Tile schedule: CL CTAs of a cluster take CL consecutive weight tiles of
-// the same token tile (and share its activation loads); clusters walk the
-// (token tile, weight-tile group) space round-robin.
-struct TileIter {
-  int group, ngroups, step, n_groups_per_m;
-  __device__ bool valid() const { return group < ngroups; }
-  __device__ void next() { group += step; }
+// Work schedule: a unit is (token tile, weight tile, K split); units are
+// numbered weight tile fastest, then split, then token tile, and dealt to the
+// persistent CTAs round-robin.
+struct Unit {
+  int m_tile, n_tile, split, kt0, kt1;
 };
+__device__ __forceinline__ Unit unit_of(const GemmArgs& p, int u) {
+  Unit r;
+  r.n_tile = u % p.n_tiles;
+  const int rest = u / p.n_tiles;
+  r.split = rest % p.splits;
+  r.m_tile = rest / p.splits;
+  r.kt0 = r.split * p.kt_per_split;
+  r.kt1 = min(r.kt0 + p.kt_per_split, p.k_tiles);
+  return r;
+}
 
-template <int BN, bool PROMOTE, bool SIDE, int CL>
+template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sp24_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w2,
                      const __grid_constant__ CUtensorMap tm_x2, const __grid_constant__ CUtensorMap tm_y,
                      const GemmArgs p) {
-  using C = Cfg<BN, PROMOTE, SIDE, CL>;
+  using C = Cfg<BN, PROMOTE, SIDE, SPLIT, KS>;
   constexpr int STAGES = C::STAGES;
   constexpr int NACC = C::NACC;
   constexpr int COLS = C::COLS;
   constexpr int CH = COLS >= 16 ? 16 : COLS;  // columns per TMEM load
-  constexpr uint16_t CL_MASK = static_cast<uint16_t>((1u << CL) - 1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = sm;
@@ -155,21 +174,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* sacce = saccf + 1;             // side accumulator drained
   uint64_t* drain = sacce + 1;             // MMA drain on abort
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* last_flag = tslot + 1;  // split-K: this CTA completes the tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t crank = CL > 1 ? cluster_rank() : 0u;
-  TileIter it0;
-  it0.n_groups_per_m = p.n_tiles / CL;
-  it0.ngroups = p.m_tiles * it0.n_groups_per_m;
-  it0.group = CL > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-  it0.step = CL > 1 ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
-  auto tile_n = [&](const TileIter& t) { return (t.group % t.n_groups_per_m) * CL + static_cast<int>(crank); };
-  auto tile_m = [&](const TileIter& t) { return t.group / t.n_groups_per_m; };
-
+  const int num_units = p.m_tiles * p.n_tiles * p.splits;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1 + (PROMOTE ? 32 : 0));
-      mbar_init(&empty[i], CL + (PROMOTE ? EPI_WARPS : 0));
+      mbar_init(&empty[i], 1 + (PROMOTE ? EPI_WARPS : 0));
     }
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&accf[i], 1);
@@ -195,8 +207,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  if (CL > 1) cluster_sync();  // every CTA's barriers exist before anyone multicasts to them
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
@@ -211,13 +222,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int64_t flat = 0;  // stage index over this CTA's whole tile sequence
     uint32_t side_phase = 0;
     bool ok = true;
-    for (TileIter t = it0; t.valid() && ok; t.next()) {
-      const int n_tile = tile_n(t);
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const Unit t = unit_of(p, u);
+      const int n_tile = t.n_tile;
       const int n0 = n_tile * BM;
-      const int m0 = tile_m(t) * BN;
+      const int m0 = t.m_tile * BN;
       const uint8_t* vsrc = p.values + static_cast<int64_t>(n_tile) * p.k_tiles * A_STAGE;
       const uint8_t* msrc = p.meta + static_cast<int64_t>(n_tile) * p.k_tiles * META_STAGE;
-      for (int kt = 0; kt < p.k_tiles; ++kt, ++flat) {
+      for (int kt = t.kt0; kt < t.kt1; kt += KS, ++flat) {
         if (flat % PRODUCERS != pw) continue;
         const uint32_t stage = static_cast<uint32_t>(flat % STAGES);
         const uint32_t phase = static_cast<uint32_t>((flat / STAGES) & 1);
@@ -225,18 +237,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
         uint8_t* sA = ring + stage * C::STAGE;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], A_STAGE + META_STAGE + C::B_STAGE);
-          bulk_load(sA, vsrc + static_cast<int64_t>(kt) * A_STAGE, A_STAGE, &full[stage]);
-          bulk_load(sA + A_STAGE, msrc + static_cast<int64_t>(kt) * META_STAGE, META_STAGE, &full[stage]);
-          uint8_t* sB = sA + A_STAGE + META_STAGE;
-          if (CL == 1)
-            tma_load_2d(sB, &tm_x, &full[stage], kt * BK, m0);
-          else
-            tma_load_2d_multicast(sB + crank * (C::SLICE * 128), &tm_x, &full[stage], kt * BK,
-                                  m0 + static_cast<int>(crank) * C::SLICE, CL_MASK);
+          mbar_arrive_expect_tx(&full[stage], C::LOAD_BYTES);
+          bulk_load(sA + C::A_OFF, vsrc + static_cast<int64_t>(kt) * A_STAGE, KS * A_STAGE, &full[stage]);
+          bulk_load(sA + C::META_OFF, msrc + static_cast<int64_t>(kt) * META_STAGE, KS * META_STAGE, &full[stage]);
+#pragma unroll
+          for (int j = 0; j < KS; ++j)
+            tma_load_2d(sA + C::B_OFF + j * C::B_SUB, &tm_x, &full[stage], (kt + j) * BK, m0);
         }
         if (PROMOTE) {
-          float* ssl = reinterpret_cast<float*>(sA + A_STAGE + META_STAGE + C::B_STAGE);
+          float* ssl = reinterpret_cast<float*>(sA + C::SCL_OFF);
           const float* sxk = p.sx + static_cast<int64_t>(kt) * p.ldsx;
           for (int i = lane; i < BN; i += 32) {
             const int m = m0 + i;
@@ -265,10 +274,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       if (!ok) atomicOr(p.err, DEVERR_TIMEOUT_PRODUCER);
       // Before leaving: every stage this warp issued has landed (so nothing writes
-      // this CTA's shared memory later) and, with a cluster, every consumer of the
-      // last use of each of those slots -- in every CTA -- has arrived on this
-      // CTA's empty barrier.  Only the last use of a slot may be waited on (an
-      // older phase of the same parity would not be seen as complete).
+      // this CTA's shared memory later) and its consumers have released it.
+      // Only the last use of a slot may be waited on (an older phase of the same
+      // parity would not be seen as complete).
       const int64_t fmax = flat - 1;
       for (int64_t f = fmax; f >= 0 && f > fmax - STAGES; --f) {
         if (f % PRODUCERS != pw) continue;
@@ -284,13 +292,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint64_t STAGE_DESC = C::STAGE >> 4;  // descriptor start-address units per stage
       // stage-0 descriptors; a stage is a fixed offset in the start-address field
       const uint32_t ring_u32 = smem_u32(ring);
-      const uint64_t a_desc0 = smem_desc(ring_u32, 16, 512, SWZ_64B);
-      const uint64_t m_desc0 = smem_desc(ring_u32 + A_STAGE, 128, 128, SWZ_NONE);
-      const uint64_t b_desc0 = smem_desc(ring_u32 + A_STAGE + META_STAGE, 16, 1024, SWZ_128B);
+      const uint64_t a_desc0 = smem_desc(ring_u32 + C::A_OFF, 16, 512, SWZ_64B);
+      const uint64_t m_desc0 = smem_desc(ring_u32 + C::META_OFF, 128, 128, SWZ_NONE);
+      const uint64_t b_desc0 = smem_desc(ring_u32 + C::B_OFF, 16, 1024, SWZ_128B);
       uint32_t stage = 0, phase = 0, side_cnt = 0, meta_ctr = 0;
       uint32_t acc_cnt = 0;
       bool ok = true;
-      for (TileIter t = it0; t.valid() && ok; t.next()) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const Unit t = unit_of(p, u);
         uint32_t d = 0;
         if (!PROMOTE) {
           const uint32_t b = acc_cnt % NACC;
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           d = tbase + b * BN;
         }
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = t.kt0; kt < t.kt1; kt += KS) {
           uint32_t b = 0;
           if (PROMOTE) {
             b = acc_cnt % NACC;
@@ -308,14 +317,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
           const uint64_t off = stage * STAGE_DESC;
-          const uint32_t mcol = tbase + META_COL0 + 4 * (meta_ctr & (META_SLOTS - 1));
-          ++meta_ctr;
-          tmem_cp_128x128b(mcol, m_desc0 + off);
-          const uint32_t acc0 = PROMOTE ? 0u : (kt != 0 ? 1u : 0u);
-          mma_sp_e4m3(d, a_desc0 + off, b_desc0 + off, mcol, idesc_sp, acc0);
-          mma_sp_e4m3(d, a_desc0 + off + 2, b_desc0 + off + 4, mcol + 2, idesc_sp, 1u);  // +32 B of A, +64 B of B
-          if (CL > 1) mma_commit_multicast(&empty[stage], CL_MASK);
-          else mma_commit(&empty[stage]);
+#pragma unroll
+          for (int j = 0; j < KS; ++j) {
+            const uint32_t mcol = tbase + META_COL0 + 4 * (meta_ctr & (META_SLOTS - 1));
+            ++meta_ctr;
+            tmem_cp_128x128b(mcol, m_desc0 + off + j * (META_STAGE >> 4));
+            const uint32_t acc0 = PROMOTE ? 0u : ((kt != t.kt0 || j != 0) ? 1u : 0u);
+            const uint64_t aj = a_desc0 + off + j * (A_STAGE >> 4);
+            const uint64_t bj = b_desc0 + off + j * (C::B_SUB >> 4);
+            mma_sp_e4m3(d, aj, bj, mcol, idesc_sp, acc0);
+            mma_sp_e4m3(d, aj + 2, bj + 4, mcol + 2, idesc_sp, 1u);  // +32 B of A, +64 B of B
+          }
+          mma_commit(&empty[stage]);
           if (PROMOTE) {
             mma_commit(&accf[b]);
             ++acc_cnt;
@@ -359,9 +372,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (C::OUT_TOKENS * 64) + (row & 63);
     uint32_t acc_cnt = 0, side_cnt = 0, e_stage = 0, e_phase = 0;
     bool ok = true;
-    for (TileIter t = it0; t.valid() && ok; t.next()) {
-      const int n0 = tile_n(t) * BM;
-      const int m0 = tile_m(t) * BN;
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const Unit t = unit_of(p, u);
+      const int n0 = t.n_tile * BM;
+      const int m0 = t.m_tile * BN;
       const int n = n0 + row;
       if (et == 0) bulk_wait_read_all();  // the previous tile's store has read the staging buffer
       if (!PROMOTE) {
@@ -407,6 +421,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           continue;
         }
+        if constexpr (SPLIT) {
+          if (p.splits > 1) {
+            // unscaled fp32 partial of this K split -> workspace [tile][split][col][row]
+            const int tile_id = t.m_tile * p.n_tiles + t.n_tile;
+            float* wpart = p.ws + (static_cast<int64_t>(tile_id) * p.splits + t.split) * (BN * BM);
+#pragma unroll
+            for (int c = 0; c < COLS; c += CH) {
+              uint32_t v[CH];
+              tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < CH; ++j) __stcg(wpart + (c0 + c + j) * BM + row, __uint_as_float(v[j]));
+            }
+            tc_fence_before();
+            mbar_arrive(&acce[b]);
+            ++acc_cnt;
+            __threadfence();
+            epilogue_bar();
+            if (et == 0) *last_flag = atomicAdd(&p.counters[tile_id], 1u) == static_cast<unsigned>(p.splits - 1);
+            epilogue_bar();
+            if (!*last_flag) continue;
+            // the last split to arrive sums all partials in split order (deterministic)
+            __threadfence();
+            const float* wtile = p.ws + static_cast<int64_t>(tile_id) * p.splits * (BN * BM);
+            float acc[COLS];
+#pragma unroll
+            for (int c = 0; c < COLS; ++c) acc[c] = 0.0f;
+            for (int sp = 0; sp < p.splits; ++sp) {  // all columns of one split per round: COLS loads in flight
+              const float* wsp = wtile + sp * (BN * BM) + c0 * BM + row;
+#pragma unroll
+              for (int c = 0; c < COLS; ++c) acc[c] += __ldcg(wsp + c * BM);
+            }
+#pragma unroll
+            for (int c = 0; c < COLS; ++c) {
+              const float y = (scl[c0 + c] * swr) * acc[c];
+              out_row[(c0 + c) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            }
+            if (et == 0) p.counters[tile_id] = 0u;  // ready for the next call
+            fence_proxy_async_smem();
+            epilogue_bar();
+            if (et == 0) {
+              tma_store_2d(&tm_y, out_tile, n0, m0);
+              tma_store_2d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0);
+              bulk_commit();
+            }
+            continue;
+          }
+        }
 #pragma unroll
         for (int c = 0; c < COLS; c += CH) {
           uint32_t v[CH];
@@ -443,10 +505,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < COLS; ++i) acc[i] = 0.0f;
         const bool per_row_w = p.gN_shift == 0;  // gN = 1: weight scale varies by row
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = t.kt0; kt < t.kt1; ++kt) {
           const uint32_t b = acc_cnt % NACC;
-          const float* ssl = reinterpret_cast<const float*>(ring + e_stage * C::STAGE + A_STAGE + META_STAGE +
-                                                            C::B_STAGE);
+          const float* ssl = reinterpret_cast<const float*>(ring + e_stage * C::STAGE + C::SCL_OFF);
           if (ok && !mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
           if (ok && !mbar_wait(&full[e_stage], e_phase)) ok = false;  // scales visible (already complete)
           if (ok) {
@@ -508,71 +569,69 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   tc_fence_before();
-  if (CL > 1) cluster_sync();
-  else __syncthreads();
+  __syncthreads();
   if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
 }
 
-template <int BN, bool PROMOTE, bool SIDE, int CL>
+template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS>
 sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2, const CUtensorMap& x2,
                    const CUtensorMap& y, const GemmArgs& args, cudaStream_t stream) {
-  using C = Cfg<BN, PROMOTE, SIDE, CL>;
-  auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE, CL>;
-  static int max_clusters[64] = {};  // per device: co-resident clusters of this instance (0 = not yet known)
-  const int d = dev->ordinal;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (max_clusters[d] == 0) {
+  using C = Cfg<BN, PROMOTE, SIDE, SPLIT, KS>;
+  auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE, SPLIT, KS>;
+  static bool attr_done[64] = {};
+  if (!attr_done[dev->ordinal]) {
     if (static_cast<size_t>(C::SMEM) > dev->smem_optin) return SP24_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return SP24_ERR_CUDA;
-    int n = dev->sm_count / CL;
-    if (CL > 1) {
-      cfg.gridDim = dim3(CL * n, 1, 1);
-      int active = 0;
-      if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) return SP24_ERR_CUDA;
-      n = active;
-    }
-    max_clusters[d] = n;
+    attr_done[dev->ordinal] = true;
   }
-  const int groups = args.m_tiles * (args.n_tiles / CL);
-  const int clusters = groups < max_clusters[d] ? groups : max_clusters[d];
-  cfg.gridDim = dim3(CL * clusters, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, x, w2, x2, y, args) != cudaSuccess) return SP24_ERR_CUDA;
+  const int units = args.m_tiles * args.n_tiles * args.splits;
+  const int grid = units < dev->sm_count ? units : dev->sm_count;
+  kern<<<grid, NUM_THREADS, C::SMEM, stream>>>(x, w2, x2, y, args);
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }
 
-// Instances: token tiles of 16..64 run without clusters (the weight stream
-// dominates); 128 and 256 share each activation tile across a 4-CTA cluster
-// when the weight tiles divide evenly.
+// Sub-tiles per stage for a token tile: small tiles batch more K per stage.
+constexpr int ks_for(int bn, bool promote) { return promote ? 1 : (bn <= 32 ? 4 : (bn == 64 ? 2 : 1)); }
+
 template <bool PROMOTE, bool SIDE>
-sp24_status launch_bn(int bn, int cl, const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2,
+sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2,
                       const CUtensorMap& x2, const CUtensorMap& y, const GemmArgs& args, cudaStream_t s) {
+  const bool split = args.splits > 1;
+  constexpr bool PLAIN = !PROMOTE && !SIDE;
   switch (bn) {
-    case 16: return launch<16, PROMOTE, SIDE, 1>(dev, x, w2, x2, y, args, s);
-    case 32: return launch<32, PROMOTE, SIDE, 1>(dev, x, w2, x2, y, args, s);
-    case 64: return launch<64, PROMOTE, SIDE, 1>(dev, x, w2, x2, y, args, s);
-    case 256:
-      if constexpr (!PROMOTE && !SIDE) {
-        return cl == 4 ? launch<256, false, false, 4>(dev, x, w2, x2, y, args, s)
-                       : launch<256, false, false, 1>(dev, x, w2, x2, y, args, s);
+    case 16:
+      if constexpr (!PROMOTE) {
+        if (ks == 4) {
+          if constexpr (PLAIN) if (split) return launch<16, false, false, true, 4>(dev, x, w2, x2, y, args, s);
+          return launch<16, false, SIDE, false, 4>(dev, x, w2, x2, y, args, s);
+        }
       }
+      return launch<16, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
+    case 32:
+      if constexpr (!PROMOTE) {
+        if (ks == 4) {
+          if constexpr (PLAIN) if (split) return launch<32, false, false, true, 4>(dev, x, w2, x2, y, args, s);
+          return launch<32, false, SIDE, false, 4>(dev, x, w2, x2, y, args, s);
+        }
+      }
+      return launch<32, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
+    case 64:
+      if constexpr (!PROMOTE) {
+        if (ks == 2) {
+          if constexpr (PLAIN) if (split) return launch<64, false, false, true, 2>(dev, x, w2, x2, y, args, s);
+          return launch<64, false, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
+        }
+      }
+      return launch<64, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
+    case 256:
+      if constexpr (PLAIN) return launch<256, false, false, false, 1>(dev, x, w2, x2, y, args, s);
       return SP24_ERR_UNSUPPORTED;
     default:
-      return cl == 4 ? launch<128, PROMOTE, SIDE, 4>(dev, x, w2, x2, y, args, s)
-                     : launch<128, PROMOTE, SIDE, 1>(dev, x, w2, x2, y, args, s);
+      return launch<128, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
   }
 }
 
@@ -586,12 +645,65 @@ int pick_bn(int64_t M, bool plain) {
   return 128;
 }
 
+// K splits for small-token shapes whose weight tiles alone leave SMs idle:
+// the smallest split count (up to 8, at least 4 K steps each) whose units
+// fill the SMs at least 5 % better than no split.
+int pick_splits(int tiles, int k_stages, int sm_count, bool splittable) {
+  if (!splittable || 2 * tiles >= sm_count) return 1;  // at least half the SMs busy without splitting
+  auto fill = [&](int s) {
+    const int units = tiles * s;
+    const int rounds = (units + sm_count - 1) / sm_count;
+    return static_cast<double>(units) / (static_cast<double>(rounds) * sm_count);
+  };
+  int best = 1;
+  double best_fill = fill(1);
+  for (int s = 2; s <= 8 && k_stages / s >= 4; ++s) {
+    if (fill(s) > best_fill + 0.05) {
+      best = s;
+      best_fill = fill(s);
+    }
+  }
+  return best;
+}
+
+struct Plan {
+  int bn, ks, m_tiles, n_tiles, k_tiles, splits;
+  size_t ws_partials, ws_bytes;  // partials bytes; total with counters (0 when not splitting)
+};
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, bool promote, bool side, int sm_count) {
+  Plan pl;
+  pl.bn = pick_bn(M, !promote && !side);
+  pl.m_tiles = static_cast<int>((M + pl.bn - 1) / pl.bn);
+  pl.n_tiles = static_cast<int>(N / BM);
+  pl.k_tiles = static_cast<int>(K / BK);
+  pl.ks = ks_for(pl.bn, promote);
+  while (pl.ks > 1 && pl.k_tiles % pl.ks != 0) pl.ks /= 2;  // stages hold whole sub-tile groups
+  pl.splits = pick_splits(pl.m_tiles * pl.n_tiles, pl.k_tiles / pl.ks, sm_count, !promote && !side && pl.bn <= 64);
+  const size_t tiles = static_cast<size_t>(pl.m_tiles) * pl.n_tiles;
+  pl.ws_partials = pl.splits > 1 ? tiles * pl.splits * pl.bn * BM * sizeof(float) : 0;
+  pl.ws_bytes = pl.splits > 1 ? pl.ws_partials + tiles * sizeof(unsigned int) : 0;
+  return pl;
+}
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
 }  // namespace
 }  // namespace sp24
 
 extern "C" size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r) {
-  (void)M; (void)N; (void)K; (void)r;
-  return 0;
+  using namespace sp24;
+  if (M < 1 || N < BM || N % BM != 0 || K < BK || K % BK != 0 || r < 0) return 0;
+  const int sms = current_sm_count();
+  if (sms <= 0) return 0;
+  // the workspace depends on the scale granularity only through promotion; size it for the
+  // per-tensor-K case, which is the one that splits
+  return make_plan(M, N, K, false, r > 0, sms).ws_bytes;
 }
 
 extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
@@ -599,7 +711,6 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
                                      int gK, const void* X2, const void* W2, int64_t r, void* Y, int64_t ldy,
                                      void* workspace, size_t workspace_bytes, void* stream) {
   using namespace sp24;
-  (void)workspace; (void)workspace_bytes;
   if (!Xq || !sx || !values || !meta || !sw || !Y) return SP24_ERR_INVALID_ARG;
   if (M < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0) return SP24_ERR_INVALID_ARG;
   if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
@@ -620,10 +731,13 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   if (st != SP24_OK) return st;
 
   const bool promote = (gK == 128 && K != 128);
-  const int bn = pick_bn(M, !promote && !side);
+  Plan pl = make_plan(M, N, K, promote, side, dev->sm_count);
+  if (pl.splits > 1 && (workspace == nullptr || workspace_bytes < pl.ws_bytes || !aligned16(workspace))) {
+    pl.splits = 1;  // no (or too small a) workspace: run unsplit
+  }
+  const int bn = pl.bn;
   CUtensorMap tm_x, tm_w2, tm_x2, tm_y;
-  const int cl_x = (bn >= 128 && (N / BM) % 4 == 0) ? 4 : 1;  // activation rows per load: the cluster slice
-  st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn / cl_x, CU_TENSOR_MAP_SWIZZLE_128B);
+  st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == SP24_OK)
     st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, bn > 128 ? bn / 2 : bn,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -651,17 +765,26 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   a.ldsw = static_cast<int>((N + gN - 1) / gN);
   a.gM_shift = gM == 128 ? 7 : 0;
   a.gN_shift = gN == 128 ? 7 : 0;
-  a.m_tiles = static_cast<int>((M + bn - 1) / bn);
-  a.n_tiles = static_cast<int>(N / BM);
-  a.k_tiles = static_cast<int>(K / BK);
+  a.m_tiles = pl.m_tiles;
+  a.n_tiles = pl.n_tiles;
+  a.k_tiles = pl.k_tiles;
   a.side_ksteps = static_cast<int>(r / 16);
+  a.splits = pl.splits;
+  a.kt_per_split = ((pl.k_tiles / pl.ks + pl.splits - 1) / pl.splits) * pl.ks;
+  a.ws = nullptr;
+  a.counters = nullptr;
   a.err = dev->err_word;
-  if (static_cast<int64_t>(a.m_tiles) * a.n_tiles > (1 << 30)) return SP24_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(a.m_tiles) * a.n_tiles * a.splits > (1 << 30)) return SP24_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int cl = (bn >= 128 && a.n_tiles % 4 == 0) ? 4 : 1;
+  if (pl.splits > 1) {
+    a.ws = static_cast<float*>(workspace);
+    a.counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + pl.ws_partials);
+    const size_t counter_bytes = static_cast<size_t>(a.m_tiles) * a.n_tiles * sizeof(unsigned int);
+    if (cudaMemsetAsync(a.counters, 0, counter_bytes, s) != cudaSuccess) return SP24_ERR_CUDA;
+  }
   if (promote)
-    return side ? launch_bn<true, true>(bn, cl, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
-                : launch_bn<true, false>(bn, cl, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
-  return side ? launch_bn<false, true>(bn, cl, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
-              : launch_bn<false, false>(bn, cl, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
+    return side ? launch_bn<true, true>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
+                : launch_bn<true, false>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
+  return side ? launch_bn<false, true>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
+              : launch_bn<false, false>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
 }

@@ -189,3 +189,30 @@ def test_compress_then_gemm_on_device(ora, sp24):
     xq, sx = ora.quantize_act(X.numpy())
     values, meta, sw = ora.compress(inputs.bf16_bits(W))
     assert_close(y, ora.gemm(xq, sx, values, meta, sw), "device path")
+
+
+# ------------------------------------------------------------------ split-K
+@pytest.mark.parametrize("M,N,K", [(16, 5120, 4096), (1, 5120, 4096), (64, 4096, 4096), (33, 6144, 2048)])
+def test_split_k(ora, sp24, M, N, K):
+    """Few token tiles and few weight tiles: K is split across CTAs and the
+    last one to finish a tile sums the partials in a fixed order."""
+    w = inputs.Workload("sk", M, N, K, seed=M + N)
+    assert sp24.workspace_size(M, N, K) > 0, "this shape is expected to split K"
+    y, ref = _check_full(ora, sp24, w, "split-K M=%d N=%d K=%d" % (M, N, K))
+    # deterministic: same bits on a second run
+    xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+    y2 = _run_gpu(sp24, w, xq, sx, values, meta, sw, None, None)
+    assert np.array_equal(y, y2)
+
+
+def test_split_k_without_workspace_runs_unsplit(ora, sp24):
+    """A too-small workspace is not an error: the call runs without splitting."""
+    M, N, K = 16, 5120, 4096
+    w = inputs.Workload("sk0", M, N, K, seed=9)
+    xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+    tv, tm = _abi(ora, values, meta)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    y = sp24.gemm(dev(xq), dev(sx), dev(tv), dev(tm), dev(sw), workspace=small)
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    assert_close(bf16_to_f64(y), ora.gemm(xq, sx, values, meta, sw), "unsplit fallback")
