@@ -155,6 +155,34 @@ SP24_API sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, i
                           const void* X2, const void* W2, int64_t r, void* Y, int64_t ldy, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/*
+ * sp24_fp8_gemm_fixed_scratch -- sp24_fp8_gemm for callers that may not
+ * allocate.  The pages have no counterpart to this entry point.
+ *
+ * Some callers own their device memory outright and must not allocate while
+ * they run (serving loops that plan every buffer at start-up, code hosted in
+ * a framework whose allocator this library cannot reach).  This call takes
+ * the same arguments as sp24_fp8_gemm minus the workspace and computes the
+ * same result; the split-K scratch comes from a fixed 4 MiB array inside the
+ * library's device image instead.  It calls no allocating routine.
+ *   - Every GPU that loads the library holds that array until the process
+ *     exits, and all calls on a device share it: calls that overlap on the
+ *     GPU (other streams, other host threads) race on it and corrupt each
+ *     other's results.  Serialise them.
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time set-up with that device current); make that first call before
+ *     any stream capture.
+ *   - A shape whose scratch need (sp24_fp8_gemm_workspace_size) exceeds
+ *     4 MiB is refused with SP24_ERR_WORKSPACE; shapes that need no scratch
+ *     always run.
+ * The tile counters in the scratch are cleared on the stream before each
+ * use; everything else it holds from the previous call is overwritten.
+ */
+SP24_API sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
+                                                 int gM, const void* values, const void* meta, const float* sw,
+                                                 int64_t N, int gN, int gK, const void* X2, const void* W2, int64_t r,
+                                                 void* Y, int64_t ldy, void* stream);
+
 /* Device scratch bytes sp24_fp8_gemm needs for this problem (0 = none). */
 SP24_API size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r);
 

@@ -34,6 +34,8 @@ SIGNATURES = {
     "sp24_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _I64,
                        _P, _SZ, _P], _I),
     "sp24_fp8_gemm_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
+    "sp24_fp8_gemm_fixed_scratch": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _I64,
+                                     _P], _I),
     "sp24_last_device_error": ([_P], _I),
 }
 

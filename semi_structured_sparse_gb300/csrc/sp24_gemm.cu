@@ -29,6 +29,7 @@
 // the sparse K loop the MMA thread issues bf16 tcgen05.mma over r <= 64 into
 // a second accumulator that the epilogue adds after scaling.
 #include <cuda_bf16.h>
+#include <mutex>
 #include "sp24_internal.cuh"
 #include "sp24_ptx.cuh"
 
@@ -787,4 +788,60 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
                 : launch_bn<true, false>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
   return side ? launch_bn<false, true>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
               : launch_bn<false, false>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free GEMM entry point.
+//
+// Some callers own their device-memory budget outright and must not allocate
+// once they are running: serving loops that plan every buffer at start-up,
+// or code hosted inside a framework whose allocator this library cannot
+// reach.  For them the split-K scratch of sp24_fp8_gemm comes from the fixed
+// array below instead of a caller-provided workspace.  The array lives in
+// this library's device image, so every GPU that loads the library holds it
+// (kFixedScratchBytes) until the process exits, and all calls on a device
+// share it.
+namespace sp24 {
+namespace {
+
+constexpr size_t kFixedScratchBytes = size_t(4) << 20;  // 4 MiB per device
+static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+
+std::mutex g_fixed_scratch_mutex;
+void* g_fixed_scratch_addr[64] = {};  // device address of g_fixed_scratch, per device ordinal
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side handle; the real device address is looked up
+// once per device (with that device current) and cached.
+sp24_status fixed_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SP24_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_fixed_scratch_mutex);
+  if (g_fixed_scratch_addr[dev] == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_fixed_scratch) != cudaSuccess || addr == nullptr) return SP24_ERR_CUDA;
+    g_fixed_scratch_addr[dev] = addr;
+  }
+  *out = g_fixed_scratch_addr[dev];
+  return SP24_OK;
+}
+
+}  // namespace
+}  // namespace sp24
+
+extern "C" sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
+                                                   int gM, const void* values, const void* meta, const float* sw,
+                                                   int64_t N, int gN, int gK, const void* X2, const void* W2,
+                                                   int64_t r, void* Y, int64_t ldy, void* stream) {
+  using namespace sp24;
+  // scratch this shape needs (split-K partials and tile counters); more than the
+  // fixed array holds is refused rather than silently run another way
+  if (sp24_fp8_gemm_workspace_size(M, N, K, r) > kFixedScratchBytes) return SP24_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const sp24_status st = fixed_scratch_address(&scratch);
+  if (st != SP24_OK) return st;
+  // sp24_fp8_gemm clears the tile counters in the scratch (stream-ordered) before
+  // the kernel runs; the partial sums need no clearing.
+  return sp24_fp8_gemm(Xq, sx, M, K, ldx, gM, values, meta, sw, N, gN, gK, X2, W2, r, Y, ldy, scratch,
+                       kFixedScratchBytes, stream);
 }
