@@ -42,37 +42,44 @@ __device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi) {
   return r;
 }
 
-// Select, quantize and pack one group of four bf16 values (bit patterns
-// e0..e3).  Each element gets the key  |w| bits << 3 | (3 - i) << 1 | sign:
-// a larger key is a larger magnitude, and among equal magnitudes the lower
-// index (the sign bit never decides because indices differ), so the two
-// largest keys are exactly the two kept elements.  Found with a 4-input
-// max/min network.  Returns the two e4m3 codes in ascending position in bits
-// [15:0] and the metadata nibble i0 | i1 << 2 in bits [19:16].
-__device__ __forceinline__ uint32_t group_key(uint32_t e, uint32_t i) {
-  return ((e & 0x7FFFu) << 3) | ((3u - i) << 1) | (e >> 15);
+// Select, quantize and pack one group of four bf16 values held as two
+// packed words: lo = (w1 << 16) | w0 and hi = (w3 << 16) | w2.
+// Each element gets the key  |w| << 2 | (3 - i):  a larger key is a larger
+// magnitude, and among equal magnitudes the lower index.  The two largest
+// keys (a 4-input max/min network) are the two kept elements.  Their bf16
+// bits are then pulled out of the 8 input bytes with one byte permute.
+// Returns the two e4m3 codes in ascending position in bits [15:0] and the
+// metadata nibble i0 | i1 << 2 in bits [19:16].
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
 }
-__device__ __forceinline__ uint32_t pack_group(uint32_t e0, uint32_t e1, uint32_t e2, uint32_t e3, float s) {
-  const uint32_t k0 = group_key(e0, 0), k1 = group_key(e1, 1), k2 = group_key(e2, 2), k3 = group_key(e3, 3);
+__device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s) {
+  const uint32_t ml = lo & 0x7FFF7FFFu, mh = hi & 0x7FFF7FFFu;
+  const uint32_t k0 = ((ml << 2) & 0x1FFFCu) | 3u;  // element 0
+  const uint32_t k1 = ((ml >> 14) & 0x1FFFCu) | 2u;  // element 1
+  const uint32_t k2 = ((mh << 2) & 0x1FFFCu) | 1u;  // element 2
+  const uint32_t k3 = (mh >> 14) & 0x1FFFCu;         // element 3
   const uint32_t hi01 = max(k0, k1), lo01 = min(k0, k1);
   const uint32_t hi23 = max(k2, k3), lo23 = min(k2, k3);
   const uint32_t first = max(hi01, hi23);
   const uint32_t second = max(min(hi01, hi23), max(lo01, lo23));
-  const uint32_t ia = 3u - ((first >> 1) & 3u), ib = 3u - ((second >> 1) & 3u);
-  // bf16 bits back from a key: sign in bit 0, magnitude in bits [17:3]
-  const uint32_t va = ((first & 1u) << 15) | (first >> 3), vb = ((second & 1u) << 15) | (second >> 3);
-  const bool a_first = ia < ib;
-  const uint32_t i0 = a_first ? ia : ib, i1 = a_first ? ib : ia;
-  const uint32_t v0 = a_first ? va : vb, v1 = a_first ? vb : va;
-  const uint32_t q = to_e4m3x2(__fdiv_rn(bf16_bits_to_float(v0), s), __fdiv_rn(bf16_bits_to_float(v1), s));
-  return q | ((i0 | (i1 << 2)) << 16);
+  const uint32_t ia = (first & 3u) ^ 3u, ib = (second & 3u) ^ 3u;
+  const uint32_t i0 = min(ia, ib), i1 = max(ia, ib);
+  // byte selector: element i is bytes 2i, 2i+1 of {hi:lo}; kept pair -> {v_i1 : v_i0}
+  const uint32_t sel = i0 * 0x22u + i1 * 0x2200u + 0x1010u;
+  const uint32_t pair = prmt(lo, hi, sel);
+  const float x0 = __uint_as_float(pair << 16), x1 = __uint_as_float(pair & 0xFFFF0000u);
+  const uint32_t q = to_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  return q | ((i0 + 4u * i1) << 16);
 }
 
 // Two groups (8 bf16 in a 16-byte chunk) -> 4 value bytes and 1 meta byte.
 __device__ __forceinline__ void pack_chunk(const uint4& v, float s, uint32_t& vals, uint32_t& metab) {
-  const uint32_t g0 = pack_group(v.x & 0xFFFFu, v.x >> 16, v.y & 0xFFFFu, v.y >> 16, s);
-  const uint32_t g1 = pack_group(v.z & 0xFFFFu, v.z >> 16, v.w & 0xFFFFu, v.w >> 16, s);
-  vals = (g0 & 0xFFFFu) | ((g1 & 0xFFFFu) << 16);
+  const uint32_t g0 = pack_group(v.x, v.y, s);
+  const uint32_t g1 = pack_group(v.z, v.w, s);
+  vals = (g0 & 0xFFFFu) | (g1 << 16);
   metab = (g0 >> 16) | ((g1 >> 16) << 4);
 }
 
@@ -89,6 +96,21 @@ __device__ __forceinline__ int64_t meta_offset(int n, int jb, int K) {
   const int64_t t = static_cast<int64_t>(n >> 7) * (K >> 7) + (jb >> 4);
   return t * 2048 + (n & 127) * 16 + (jb & 15);
 }
+
+// Per-lane parts of those offsets for the row kernels, where lane l of a warp
+// packs the 8 weights at k = 256 c + 8 l: its 4 value bytes land in tile
+// 2c + l/16 and its meta byte in the same tile; chunk c adds 2 tiles.
+struct RowStore {
+  int64_t v, m;  // offsets for chunk 0
+  __device__ RowStore(int n, int K, int lane) {
+    const int r = n & 127;
+    const int64_t band = static_cast<int64_t>(n >> 7) * (K >> 7);
+    v = band * 8192 + (lane >> 4) * 8192 + r * 64 + ((((lane & 15) >> 2) ^ ((r >> 1) & 3)) << 4) + (lane & 3) * 4;
+    m = band * 2048 + (lane >> 4) * 2048 + r * 16 + (lane & 15);
+  }
+  __device__ int64_t values_at(int c) const { return v + static_cast<int64_t>(c) * 16384; }
+  __device__ int64_t meta_at(int c) const { return m + static_cast<int64_t>(c) * 4096; }
+};
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
@@ -140,14 +162,15 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
     amax = max(pair_amax[warp & ~1], pair_amax[warp | 1]);
     const float s = weight_scale(amax);
     if (lane == 0 && h == 0) scales[n] = s;
+    const RowStore st(n, K, lane);
 #pragma unroll
     for (int i = 0; i < kHeldChunks; ++i) {
       const int c = 2 * i + h, k = c * 256 + lane * 8;
       if (c < nchunks && k < K) {
         uint32_t vals, mb;
         pack_chunk(held[i], s, vals, mb);
-        *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
-        meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
+        *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
+        meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
       }
     }
     for (int c = 2 * kHeldChunks + h; c < nchunks; c += 2) {
@@ -155,8 +178,8 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
       if (k < K) {
         uint32_t vals, mb;
         pack_chunk(*reinterpret_cast<const uint4*>(row + k), s, vals, mb);
-        *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
-        meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
+        *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
+        meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
       }
     }
   } else {
@@ -164,6 +187,7 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
     const int n = blockIdx.x * kRowsPerCta + warp;
     if (n >= N) return;
     const uint16_t* row = W + static_cast<int64_t>(n) * ldw;
+    const RowStore st(n, K, lane);
     for (int c = 0; c < nchunks; ++c) {
       const int k = c * 256 + lane * 8;
       const bool active = k < K;
@@ -177,8 +201,8 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
         if ((lane & 15) == 0) scales[static_cast<int64_t>(k / 128) * N + n] = s;
         uint32_t vals, mb;
         pack_chunk(v, s, vals, mb);
-        *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
-        meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
+        *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
+        meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
       }
     }
   }

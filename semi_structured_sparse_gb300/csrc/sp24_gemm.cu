@@ -596,7 +596,9 @@ sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMa
 }
 
 // Sub-tiles per stage for a token tile: small tiles batch more K per stage.
-constexpr int ks_for(int bn, bool promote) { return promote ? 1 : (bn <= 32 ? 4 : (bn == 64 ? 2 : 1)); }
+constexpr int ks_for(int bn, bool promote) {
+  return promote ? 1 : (bn <= 32 ? 4 : (bn <= 128 ? 2 : 1));
+}
 
 template <bool PROMOTE, bool SIDE>
 sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2,
@@ -632,6 +634,9 @@ sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& 
       if constexpr (PLAIN) return launch<256, false, false, false, 1>(dev, x, w2, x2, y, args, s);
       return SP24_ERR_UNSUPPORTED;
     default:
+      if constexpr (!PROMOTE) {
+        if (ks == 2) return launch<128, false, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
+      }
       return launch<128, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
   }
 }

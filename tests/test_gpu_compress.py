@@ -110,3 +110,36 @@ def test_e4m3_rounding_boundaries_on_gpu(ora, sp24):
     torch.cuda.synchronize()
     assert (osx == 1.0).all()
     assert np.array_equal(host_bits(gq), oq)
+
+
+def test_quotients_near_e4m3_midpoints(ora, sp24):
+    """Random per-row scales with values placed so that x / s lands on, and a
+    few fp32 ulps around, every e4m3 rounding midpoint: the device's division
+    (reciprocal with a correction step, exact division near midpoints) must
+    give the oracle's correctly rounded codes everywhere."""
+    rng = np.random.default_rng(17)
+    q = np.arange(0x7F, dtype=np.uint8)
+    v = ora.e4m3_decode(q)
+    mids = (v[:-1] + v[1:]) / 2                       # includes the subnormal range
+    K = 512
+    rows = []
+    for _ in range(64):
+        amax = np.float32(rng.uniform(0.25, 16.0))
+        s = np.float32(amax / np.float32(448.0))
+        t = rng.choice(mids, size=K - 1) * (1.0 + rng.integers(-4, 5, size=K - 1) * 2.0 ** -23)
+        x = (t * np.float64(s)).astype(np.float32) * rng.choice([-1.0, 1.0], size=K - 1).astype(np.float32)
+        x = np.clip(x, -amax, amax)
+        rows.append(np.concatenate([[amax], x]).astype(np.float32))
+    X = np.stack(rows)
+    oq, osx = ora.quantize_act(X)
+    gq, gsx = sp24.quantize_act(dev(X))
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(gsx).view(np.uint32), osx.view(np.uint32))
+    assert np.array_equal(host_bits(gq), oq)
+    # the same through weight compression (bf16 rows, kept elements divided by the row scale)
+    Wt = torch.from_numpy(X[:, :K].copy()).to(torch.bfloat16)
+    Wt = torch.cat([Wt, Wt.flip(0)], 0)               # 128 rows
+    ov, om, os_ = ora.compress_abi(inputs.bf16_bits(Wt))
+    gv, gm, gs = sp24.compress(dev(inputs.bf16_bits(Wt)))
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(gv).ravel(), ov) and np.array_equal(host_bits(gm).ravel(), om)
