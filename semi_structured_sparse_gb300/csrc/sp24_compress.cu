@@ -12,6 +12,7 @@
 // Activation path: same PR #3258, the activation is divided by its scale and
 // cast to e4m3.
 #include "sp24_internal.cuh"
+#include "sp24_ptx.cuh"
 
 namespace sp24 {
 namespace {
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
                                                             float* __restrict__ scales) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = (K + 255) / 256;  // 256 elements per warp step, 8 per lane
+  pdl_wait();
 
   if (!GK128) {
     __shared__ uint32_t pair_amax[8];
@@ -206,6 +208,7 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
       }
     }
   }
+  pdl_trigger();
 }
 
 // gN = gK = 128: one CTA of 256 threads per 128 x 128 block.  Thread t owns
@@ -218,6 +221,7 @@ __global__ void __launch_bounds__(256) compress_blocks_kernel(const uint16_t* __
   const int kb = blockIdx.x, nb = blockIdx.y;
   const int t = threadIdx.x, cseg = t & 15, r0 = t >> 4;
   const int k = kb * 128 + cseg * 8;
+  pdl_wait();
   uint4 v[8];
   uint32_t amax = 0;
 #pragma unroll
@@ -242,6 +246,7 @@ __global__ void __launch_bounds__(256) compress_blocks_kernel(const uint16_t* __
     *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
     meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
   }
+  pdl_trigger();
 }
 
 // Activation quantization: one warp per token row; 128 elements per warp
@@ -251,6 +256,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
                                                            uint8_t* __restrict__ xq, float* __restrict__ sx) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * 8 + warp;
+  pdl_wait();
   if (m >= M) return;
   const float* row = X + static_cast<int64_t>(m) * ldx;
   uint8_t* qrow = xq + static_cast<int64_t>(m) * K;
@@ -281,6 +287,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
       *reinterpret_cast<uint32_t*>(qrow + c * 128 + lane * 4) = quant4(f, s);
     }
   }
+  pdl_trigger();
 }
 
 }  // namespace
@@ -308,14 +315,20 @@ extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, in
   if (block128) {
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
     if (grid.y > 65535u) return SP24_ERR_UNSUPPORTED;
-    compress_blocks_kernel<<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
+    if (launch_pdl(compress_blocks_kernel, grid, dim3(256), 0, s, w, (int)N, (int)K, ldw, v, m, scales) !=
+        cudaSuccess)
+      return SP24_ERR_CUDA;
   } else {
     if (per_channel) {
       const unsigned grid = static_cast<unsigned>((N + kPairRowsPerCta - 1) / kPairRowsPerCta);
-      compress_rows_kernel<false><<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
+      if (launch_pdl(compress_rows_kernel<false>, dim3(grid), dim3(256), 0, s, w, (int)N, (int)K, ldw, v, m,
+                     scales) != cudaSuccess)
+        return SP24_ERR_CUDA;
     } else {
       const unsigned grid = static_cast<unsigned>((N + kRowsPerCta - 1) / kRowsPerCta);
-      compress_rows_kernel<true><<<grid, 256, 0, s>>>(w, (int)N, (int)K, ldw, v, m, scales);
+      if (launch_pdl(compress_rows_kernel<true>, dim3(grid), dim3(256), 0, s, w, (int)N, (int)K, ldw, v, m,
+                     scales) != cudaSuccess)
+        return SP24_ERR_CUDA;
     }
   }
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
@@ -335,8 +348,11 @@ extern "C" sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>((M + 7) / 8);
   if (gK == 128)
-    quantize_act_kernel<true><<<grid, 256, 0, s>>>(X, (int)M, (int)K, ldx, static_cast<uint8_t*>(xq), sx);
+    st = launch_pdl(quantize_act_kernel<true>, dim3(grid), dim3(256), 0, s, X, (int)M, (int)K, ldx,
+                    static_cast<uint8_t*>(xq), sx) == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
   else
-    quantize_act_kernel<false><<<grid, 256, 0, s>>>(X, (int)M, (int)K, ldx, static_cast<uint8_t*>(xq), sx);
+    st = launch_pdl(quantize_act_kernel<false>, dim3(grid), dim3(256), 0, s, X, (int)M, (int)K, ldx,
+                    static_cast<uint8_t*>(xq), sx) == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+  if (st != SP24_OK) return st;
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }

@@ -30,27 +30,12 @@
 // a second accumulator that the epilogue adds after scaling.
 #include <cuda_bf16.h>
 #include <mutex>
+#include "sp24_gemm_common.cuh"
 #include "sp24_internal.cuh"
 #include "sp24_ptx.cuh"
 
 namespace sp24 {
 namespace {
-
-constexpr int BM = 128;                  // weight rows per tile (MMA M)
-constexpr int BK = 128;                  // logical K per stage (two sparse MMAs of K = 64)
-constexpr int A_STAGE = BM * BK / 2;     // kept values: one 8 KB storage tile
-constexpr int META_STAGE = BM * BK / 8;  // metadata: one 2 KB storage tile
-constexpr int META_COL0 = 448;           // TMEM columns 448..511: metadata ring
-constexpr int META_SLOTS = 16;           // 4 columns each
-constexpr int MAX_STAGES = 16;
-constexpr int PRODUCERS = 2;             // load warps; warp p issues the stages p, p + 2, ...
-constexpr int MMA_WARP = PRODUCERS;
-constexpr int EPI_WARP0 = PRODUCERS + 1;
-constexpr int EPI_WARPS = 8;             // two per TMEM lane quadrant, each half of the columns
-constexpr int EPI_THREADS = 32 * EPI_WARPS;
-constexpr int NUM_THREADS = 32 * EPI_WARP0 + EPI_THREADS;
-constexpr int SMEM_LIMIT = 227 * 1024;
-constexpr int BAR_BYTES = 1024;
 
 // A pipeline stage carries KS consecutive 128-K sub-tiles: the kept values
 // of all KS (one contiguous copy), their metadata (one copy), then KS
@@ -86,49 +71,6 @@ struct Cfg {
   static_assert(!PROMOTE || (BN <= 128 && KS == 1), "per-stage scale slot holds one K block of BN + 128 floats");
   static_assert(!SPLIT || (!PROMOTE && !SIDE && BN <= 128), "split-K: plain per-tensor-K scaling only");
 };
-
-struct GemmArgs {
-  const uint8_t* values;  // tiled kept values
-  const uint8_t* meta;    // tiled metadata
-  const float* sx;
-  const float* sw;
-  int M, N, K;
-  int ldsx, ldsw;          // row strides (floats) of the scale tensors
-  int gM_shift, gN_shift;  // log2 of the granularities (0 or 7)
-  int m_tiles, n_tiles, k_tiles;
-  int side_ksteps;  // r / 16
-  int splits;       // K splits per output tile (1 = none)
-  int kt_per_split; // 128-K sub-tiles per split (a multiple of the stage's KS)
-  float* ws;        // split-K partials [tile][split][BN][128] (fp32, unscaled)
-  unsigned int* counters;  // split-K arrival counters [tile], zero on entry
-  unsigned int* err;
-};
-
-// Barrier over the epilogue threads (named barrier 1) that also ORs a
-// predicate across them, so that a give-up decision is taken by all or none.
-__device__ __forceinline__ bool epilogue_bar_any(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(pred ? 1u : 0u), "n"(EPI_THREADS)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
-
-// Loads `N8 * 8` consecutive accumulator columns of this warp's lanes.
-template <int N8>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
-  if constexpr (N8 % 2 == 0) {
-#pragma unroll
-    for (int i = 0; i < N8 / 2; ++i) tmem_ld16(taddr + 16 * i, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * i));
-  } else {
-#pragma unroll
-    for (int i = 0; i < N8; ++i) tmem_ld8(taddr + 8 * i, r + 8 * i);
-  }
-}
 
 // Work schedule: a unit is (token tile, weight tile, K split); units are
 // numbered weight tile fastest, then split, then token tile, and dealt to the
@@ -211,6 +153,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < PRODUCERS) {
     // ----------------------------------------------------------- producers
@@ -569,6 +512,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (!ok) atomicOr(p.err, DEVERR_TIMEOUT_EPILOGUE);
   }
 
+  pdl_trigger();  // only teardown is left: the next kernel may begin launching
   tc_fence_before();
   __syncthreads();
   if (warp == MMA_WARP) {
@@ -591,7 +535,8 @@ sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMa
   }
   const int units = args.m_tiles * args.n_tiles * args.splits;
   const int grid = units < dev->sm_count ? units : dev->sm_count;
-  kern<<<grid, NUM_THREADS, C::SMEM, stream>>>(x, w2, x2, y, args);
+  if (launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), C::SMEM, stream, x, w2, x2, y, args) != cudaSuccess)
+    return SP24_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }
 
@@ -741,24 +686,6 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   if (pl.splits > 1 && (workspace == nullptr || workspace_bytes < pl.ws_bytes || !aligned16(workspace))) {
     pl.splits = 1;  // no (or too small a) workspace: run unsplit
   }
-  const int bn = pl.bn;
-  CUtensorMap tm_x, tm_w2, tm_x2, tm_y;
-  st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st == SP24_OK)
-    st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, bn > 128 ? bn / 2 : bn,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st == SP24_OK && side) {
-    st = make_tmap_2d(&tm_w2, W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, N, r * 2, 64, BM,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st == SP24_OK)
-      st = make_tmap_2d(&tm_x2, X2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, M, r * 2, 64, bn,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
-  } else {
-    tm_w2 = tm_x;
-    tm_x2 = tm_x;
-  }
-  if (st != SP24_OK) return st;
-
   GemmArgs a;
   a.values = static_cast<const uint8_t*>(values);
   a.meta = static_cast<const uint8_t*>(meta);
@@ -782,6 +709,27 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   a.err = dev->err_word;
   if (static_cast<int64_t>(a.m_tiles) * a.n_tiles * a.splits > (1 << 30)) return SP24_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // large token counts with plain scaling: 256 x 256 tiles on SM pairs
+  if (pair_gemm_applies(M, N, K, !promote && !side)) return launch_pair_gemm(dev, Xq, ldx, Y, ldy, a, s);
+
+  const int bn = pl.bn;
+  CUtensorMap tm_x, tm_w2, tm_x2, tm_y;
+  st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == SP24_OK)
+    st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, bn > 128 ? bn / 2 : bn,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st == SP24_OK && side) {
+    st = make_tmap_2d(&tm_w2, W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, N, r * 2, 64, BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == SP24_OK)
+      st = make_tmap_2d(&tm_x2, X2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, M, r * 2, 64, bn,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    tm_w2 = tm_x;
+    tm_x2 = tm_x;
+  }
+  if (st != SP24_OK) return st;
+
   if (pl.splits > 1) {
     a.ws = static_cast<float*>(workspace);
     a.counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + pl.ws_partials);

@@ -1,0 +1,85 @@
+// sp24_gemm_common.cuh -- definitions shared by the GEMM translation units
+// (the one-CTA kernel in sp24_gemm.cu, the SM-pair kernel in
+// sp24_gemm_pair.cu): tile constants, the kernel argument block, the epilogue
+// barriers and TMEM column loads, and the pair kernel's host entry.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include "sp24_internal.cuh"
+#include "sp24_ptx.cuh"
+
+namespace sp24 {
+
+struct GemmArgs {
+  const uint8_t* values;  // tiled kept values
+  const uint8_t* meta;    // tiled metadata
+  const float* sx;
+  const float* sw;
+  int M, N, K;
+  int ldsx, ldsw;          // row strides (floats) of the scale tensors
+  int gM_shift, gN_shift;  // log2 of the granularities (0 or 7)
+  int m_tiles, n_tiles, k_tiles;
+  int side_ksteps;  // r / 16
+  int splits;       // K splits per output tile (1 = none)
+  int kt_per_split; // 128-K sub-tiles per split (a multiple of the stage's KS)
+  float* ws;        // split-K partials [tile][split][BN][128] (fp32, unscaled)
+  unsigned int* counters;  // split-K arrival counters [tile], zero on entry
+  unsigned int* err;
+};
+
+namespace {
+
+constexpr int BM = 128;                  // weight rows per tile (MMA M)
+constexpr int BK = 128;                  // logical K per stage (two sparse MMAs of K = 64)
+constexpr int A_STAGE = BM * BK / 2;     // kept values: one 8 KB storage tile
+constexpr int META_STAGE = BM * BK / 8;  // metadata: one 2 KB storage tile
+constexpr int META_COL0 = 448;           // TMEM columns 448..511: metadata ring
+constexpr int META_SLOTS = 16;           // 4 columns each
+constexpr int MAX_STAGES = 16;
+constexpr int PRODUCERS = 2;             // load warps; warp p issues the stages p, p + 2, ...
+constexpr int MMA_WARP = PRODUCERS;
+constexpr int EPI_WARP0 = PRODUCERS + 1;
+constexpr int EPI_WARPS = 8;             // two per TMEM lane quadrant, each half of the columns
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int NUM_THREADS = 32 * EPI_WARP0 + EPI_THREADS;
+constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr int BAR_BYTES = 1024;
+
+// Barrier over the epilogue threads (named barrier 1) that also ORs a
+// predicate across them, so that a give-up decision is taken by all or none.
+__device__ __forceinline__ bool epilogue_bar_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "n"(EPI_THREADS)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
+
+// Loads `N8 * 8` consecutive accumulator columns of this warp's lanes.
+template <int N8>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
+  if constexpr (N8 % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < N8 / 2; ++i) tmem_ld16(taddr + 16 * i, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * i));
+  } else {
+#pragma unroll
+    for (int i = 0; i < N8; ++i) tmem_ld8(taddr + 8 * i, r + 8 * i);
+  }
+}
+
+}  // namespace
+
+// SM-pair kernel (sp24_gemm_pair.cu): plain per-token x per-channel scaling,
+// 256 weight rows x 256 tokens per pair tile.  pair_gemm_applies says whether
+// a call takes it; launch_pair_gemm builds its tensor maps and launches it
+// (args: operands, scales, sizes and the error word; tile counts are its own).
+bool pair_gemm_applies(int64_t M, int64_t N, int64_t K, bool plain);
+sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
+                             const GemmArgs& args, cudaStream_t stream);
+
+}  // namespace sp24

@@ -37,6 +37,25 @@ sp24_status make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
                          uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
                          CUtensorMapSwizzle swizzle);
 
+// Launches `kern` with programmatic stream serialisation: it may begin while
+// the previous kernel in the stream finishes, and must call pdl_wait() (see
+// sp24_ptx.cuh) before its first global-memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace sp24

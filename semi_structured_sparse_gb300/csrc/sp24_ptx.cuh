@@ -275,6 +275,78 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream is still
+// running; it must call pdl_wait() before touching global memory that the
+// previous kernel may read or write.  pdl_trigger() lets the next kernel's
+// launch begin (it still waits in its own pdl_wait for this grid to finish).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ------------------------------------------------------ SM pairs (cta_group::2)
+// A pair is the two CTAs of a 2-CTA cluster.  One thread of the even CTA
+// issues the MMA for both; A (weight rows) is split by CTA, B (tokens) along
+// N: CTA c holds rows [c N/2, (c+1) N/2) of B at the same shared-memory
+// offset, and each CTA's tensor memory receives its 128 rows x N columns of D.
+// Every tcgen05 instruction of a pair kernel carries cta_group::2.
+
+// shared::cluster address of the object at `p`'s offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// TMA 2D load into this CTA's shared memory, with its transaction bytes
+// signalled on the mbarrier at `bar_cluster`, which may be in the pair peer.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+// Tensor-memory allocation for a pair: one warp of EACH CTA issues it, both
+// with the same column count; both receive the same address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Sparse e4m3 MMA over the pair (M = 256: 128 weight rows per CTA); each
+// CTA's metadata for its own rows sits at meta_tmem in its own TMEM.
+__device__ __forceinline__ void mma_sp_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t meta_tmem, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.sp.cta_group::2.kind::f8f6f4 [%0], %1, %2, [%3], %4, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Each CTA's shared memory at the descriptor's offset -> its own TMEM (128 lanes x 128 bits).
+__device__ __forceinline__ void tmem_cp_128x128b_pair(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+// Arrive once on `bar`'s offset in every CTA of `cta_mask` when the pair
+// operations this thread issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // Packed fp32 pair FMA (one instruction for two lanes of work):
 // (a0, a1) = (x0 * s0 + a0, x1 * s1 + a1), each rounded to nearest.
 __device__ __forceinline__ void ffma2(float& a0, float& a1, float x0, float x1, float s0, float s1) {

@@ -191,6 +191,36 @@ def test_compress_then_gemm_on_device(ora, sp24):
     assert_close(y, ora.gemm(xq, sx, values, meta, sw), "device path")
 
 
+# ---------------------------------------------------------------- SM pairs
+@pytest.mark.parametrize("M,N,K", [(193, 256, 256), (256, 512, 128), (300, 768, 512), (511, 256, 1024),
+                                   (2048, 2560, 256)])
+def test_pair_tiles(ora, sp24, M, N, K):
+    """More than 192 tokens with N a multiple of 256 run on SM pairs: one
+    M = 256 sparse MMA across two SMs per 128-wide K half-step, 256 x 256
+    output tiles.  Ragged token tails (the second SM's activation rows past
+    M), a single K block, and more tiles than pairs (each pair loops)."""
+    w = inputs.Workload("pair", M, N, K, seed=M + N + K)
+    _check_full(ora, sp24, w, "pair M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("gM,gN", [(128, 128), (1, 128), (128, 1)])
+def test_pair_tiles_coarse_scales(ora, sp24, gM, gN):
+    w = inputs.Workload("pairg", 400, 512, 384, gM=gM, gN=gN, seed=gM + 3 * gN)
+    _check_full(ora, sp24, w, "pair gM=%d gN=%d" % (gM, gN))
+
+
+def test_pair_tiles_deterministic(ora, sp24):
+    w = inputs.Workload("pdet", 700, 1024, 512, seed=5)
+    xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+    values, meta = _abi(ora, values, meta)
+    a = [dev(t) for t in (xq, sx, values, meta, sw)]
+    y1 = sp24.gemm(*a)
+    y2 = sp24.gemm(*a)
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    assert torch.equal(y1, y2)
+
+
 # ------------------------------------------------------------------ split-K
 @pytest.mark.parametrize("M,N,K", [(16, 5120, 4096), (1, 5120, 4096), (64, 4096, 4096), (33, 6144, 2048)])
 def test_split_k(ora, sp24, M, N, K):
