@@ -285,7 +285,8 @@ def run_ours(args):
                         pk["source"], FP8_OVER_BF16, pk["source"]),
                     "achieved_counts": "algorithmic 2*M*N*K/2 flops (kept weights only) per launch"}
     else:
-        roofline = {"kernel": "compress_rows_kernel", "bound": "hbm", "achieved": round(comp_gbs, 1),
+        comp_kernel = "compress_blocks_kernel" if w.gN == 128 else "compress_rows_kernel"
+        roofline = {"kernel": comp_kernel, "bound": "hbm", "achieved": round(comp_gbs, 1),
                     "peak": round(pk["hbm_gbs"], 1), "unit": "GB/s", "frac": round(comp_gbs / pk["hbm_gbs"], 4),
                     "traffic": captured_traffic(args.workload, w.M, "compress"),
                     "peak_source": "%s copy bandwidth, of %s" % (pk["source"], pk["source"]),

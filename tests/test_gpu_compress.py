@@ -40,6 +40,28 @@ def test_compress_ragged_shapes(ora, sp24, N, K, gN, gK):
     assert np.array_equal(gv, ov)
 
 
+@pytest.mark.parametrize("N,K", [(256, 2048), (128, 2176), (384, 3072), (128, 5120), (256, 8192), (128, 12288),
+                                 (128, 16384), (128, 16512), (128, 20480)])
+def test_compress_row_lengths(ora, sp24, N, K):
+    """Per-channel compression across row lengths: rows held in registers
+    whole (K <= 4096), rows whose amax pass streams past the held chunks,
+    and ragged final chunks (K % 256 == 128)."""
+    _, W, _, _ = inputs.generate(inputs.Workload("rl", 1, N, K, seed=N ^ K))
+    (ov, om, os_), (gv, gm, gs) = _compress_both(ora, sp24, W, 1, K)
+    assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(gm, om)
+    assert np.array_equal(gv, ov)
+
+
+def test_compress_many_rows_per_cta(ora, sp24):
+    """Many short rows: thousands of CTAs, most rows' chunks partly idle."""
+    _, W, _, _ = inputs.generate(inputs.Workload("mr", 1, 16384, 256, seed=3))
+    (ov, om, os_), (gv, gm, gs) = _compress_both(ora, sp24, W, 1, 256)
+    assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(gm, om)
+    assert np.array_equal(gv, ov)
+
+
 def test_compress_edge_values(ora, sp24):
     """Ties, signed zeros, an all-zero row, subnormal bf16 and huge values."""
     N, K = 128, 256
