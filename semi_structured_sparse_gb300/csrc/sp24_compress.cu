@@ -35,6 +35,25 @@ __device__ __forceinline__ uint32_t chunk_amax_bits(const uint4& v) {
   return max(m2 & 0xFFFFu, m2 >> 16);
 }
 
+// x / s, correctly rounded, given r = RN(1/s): Markstein's correction step
+// (P. W. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x r) is
+// within an ulp of the quotient, the residual x - s q0 is exact in one FMA,
+// and RN(q0 + residual r) is the correctly rounded x / s.  One reciprocal
+// per row replaces a full division per element.  Conditions: every quotient
+// here is at most 448 in magnitude (|x| <= amax = 448 s), so nothing
+// overflows; the scale must be at least kMinFastScale, so that r is finite
+// and, for any quotient that can round to a nonzero e4m3 code (>= 2^-10), the
+// residual stays in the fp32 normal range (rows below it divide exactly).
+// The sign is copied from x: for x = -0 the residual sum gives +0.
+constexpr float kMinFastScale = 8.0779356e-28f;  // 2^-90
+__device__ __forceinline__ float div_scale(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float rem = __fmaf_rn(-q0, s, x);
+  const float q = __fmaf_rn(rem, r, q0);
+  return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
 // Two fp32 -> e4m3 conversions in one instruction (round to nearest even,
 // saturate to +-448); `lo` lands in bits [7:0], `hi` in bits [15:8].
 __device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi) {
@@ -56,7 +75,8 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
-__device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s) {
+template <bool FAST>
+__device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s, float r) {
   const uint32_t ml = lo & 0x7FFF7FFFu, mh = hi & 0x7FFF7FFFu;
   const uint32_t k0 = ((ml << 2) & 0x1FFFCu) | 3u;  // element 0
   const uint32_t k1 = ((ml >> 14) & 0x1FFFCu) | 2u;  // element 1
@@ -72,14 +92,16 @@ __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s
   const uint32_t sel = i0 * 0x22u + i1 * 0x2200u + 0x1010u;
   const uint32_t pair = prmt(lo, hi, sel);
   const float x0 = __uint_as_float(pair << 16), x1 = __uint_as_float(pair & 0xFFFF0000u);
-  const uint32_t q = to_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  const uint32_t q = FAST ? to_e4m3x2(div_scale(x0, s, r), div_scale(x1, s, r))
+                          : to_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
   return q | ((i0 + 4u * i1) << 16);
 }
 
 // Two groups (8 bf16 in a 16-byte chunk) -> 4 value bytes and 1 meta byte.
-__device__ __forceinline__ void pack_chunk(const uint4& v, float s, uint32_t& vals, uint32_t& metab) {
-  const uint32_t g0 = pack_group(v.x, v.y, s);
-  const uint32_t g1 = pack_group(v.z, v.w, s);
+template <bool FAST>
+__device__ __forceinline__ void pack_chunk(const uint4& v, float s, float r, uint32_t& vals, uint32_t& metab) {
+  const uint32_t g0 = pack_group<FAST>(v.x, v.y, s, r);
+  const uint32_t g1 = pack_group<FAST>(v.z, v.w, s, r);
   vals = (g0 & 0xFFFFu) | (g1 << 16);
   metab = (g0 >> 16) | ((g1 >> 16) << 4);
 }
@@ -121,6 +143,33 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
+// Packs and stores the chunks c = h, h + 2, ... of row n (two warps per row):
+// the first kHeldChunks from registers, any further ones re-read from global.
+template <bool FAST>
+__device__ __forceinline__ void emit_row(const uint4 (&held)[8], const uint16_t* row, int n, int K, int nchunks, int h,
+                                         int lane, float s, float r, uint8_t* values, uint8_t* meta) {
+  const RowStore st(n, K, lane);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int c = 2 * i + h, k = c * 256 + lane * 8;
+    if (c < nchunks && k < K) {
+      uint32_t vals, mb;
+      pack_chunk<FAST>(held[i], s, r, vals, mb);
+      *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
+      meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
+    }
+  }
+  for (int c = 16 + h; c < nchunks; c += 2) {
+    const int k = c * 256 + lane * 8;
+    if (k < K) {
+      uint32_t vals, mb;
+      pack_chunk<FAST>(*reinterpret_cast<const uint4*>(row + k), s, r, vals, mb);
+      *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
+      meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
+    }
+  }
+}
+
 constexpr int kRowsPerCta = 8;   // gK = 128: one warp per weight row
 constexpr int kPairRowsPerCta = 4;  // gK = K: two warps per weight row
 constexpr int kHeldChunks = 8;   // per warp: 8 x 16 bytes per lane stay in registers
@@ -130,7 +179,7 @@ constexpr int kHeldChunks = 8;   // per warp: 8 x 16 bytes per lane stay in regi
 // row's amax is combined through shared memory.  GK128 = true: one scale per
 // row and 128-wide K block; one warp per row, each half-warp owns a block.
 template <bool GK128>
-__global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __restrict__ W, int N, int K, int64_t ldw,
+__global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* __restrict__ W, int N, int K, int64_t ldw,
                                                             uint8_t* __restrict__ values, uint8_t* __restrict__ meta,
                                                             float* __restrict__ scales) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,28 +211,12 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
     __syncthreads();
     if (!valid) return;
     amax = max(pair_amax[warp & ~1], pair_amax[warp | 1]);
-    const float s = weight_scale(amax);
+    const float s = weight_scale(amax), r = __frcp_rn(s);
     if (lane == 0 && h == 0) scales[n] = s;
-    const RowStore st(n, K, lane);
-#pragma unroll
-    for (int i = 0; i < kHeldChunks; ++i) {
-      const int c = 2 * i + h, k = c * 256 + lane * 8;
-      if (c < nchunks && k < K) {
-        uint32_t vals, mb;
-        pack_chunk(held[i], s, vals, mb);
-        *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
-        meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
-      }
-    }
-    for (int c = 2 * kHeldChunks + h; c < nchunks; c += 2) {
-      const int k = c * 256 + lane * 8;
-      if (k < K) {
-        uint32_t vals, mb;
-        pack_chunk(*reinterpret_cast<const uint4*>(row + k), s, vals, mb);
-        *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
-        meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
-      }
-    }
+    if (s >= kMinFastScale)  // the same for the whole row: warp-uniform
+      emit_row<true>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+    else
+      emit_row<false>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
   } else {
     // lanes 0-15 cover K block 2c, lanes 16-31 block 2c+1 (when it exists)
     const int n = blockIdx.x * kRowsPerCta + warp;
@@ -198,11 +231,14 @@ __global__ void __launch_bounds__(256) compress_rows_kernel(const uint16_t* __re
       uint32_t amax = active ? chunk_amax_bits(v) : 0u;
 #pragma unroll
       for (int off = 8; off >= 1; off >>= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-      const float s = weight_scale(amax);
+      const float s = weight_scale(amax), r = __frcp_rn(s);
       if (active) {
         if ((lane & 15) == 0) scales[static_cast<int64_t>(k / 128) * N + n] = s;
         uint32_t vals, mb;
-        pack_chunk(v, s, vals, mb);
+        if (s >= kMinFastScale)
+          pack_chunk<true>(v, s, r, vals, mb);
+        else
+          pack_chunk<false>(v, s, r, vals, mb);
         *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
         meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
       }
@@ -236,13 +272,16 @@ __global__ void __launch_bounds__(256) compress_blocks_kernel(const uint16_t* __
   amax = warp_max[0];
 #pragma unroll
   for (int w = 1; w < 8; ++w) amax = max(amax, warp_max[w]);
-  const float s = weight_scale(amax);
+  const float s = weight_scale(amax), r = __frcp_rn(s);
   if (t == 0) scales[static_cast<int64_t>(kb) * (N / 128) + nb] = s;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int n = nb * 128 + r0 + 16 * i;
     uint32_t vals, mb;
-    pack_chunk(v[i], s, vals, mb);
+    if (s >= kMinFastScale)  // the same for the whole block: CTA-uniform
+      pack_chunk<true>(v[i], s, r, vals, mb);
+    else
+      pack_chunk<false>(v[i], s, r, vals, mb);
     *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
     meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
   }

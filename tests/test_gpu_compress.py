@@ -165,3 +165,45 @@ def test_quotients_near_e4m3_midpoints(ora, sp24):
     gv, gm, gs = sp24.compress(dev(inputs.bf16_bits(Wt)))
     torch.cuda.synchronize()
     assert np.array_equal(host_bits(gv).ravel(), ov) and np.array_equal(host_bits(gm).ravel(), om)
+
+
+def test_every_bf16_magnitude_against_many_scales(ora, sp24):
+    """Every finite positive bf16 magnitude up to the row's amax is divided by
+    that row's scale and rounded to e4m3, for 48 amax values (random, powers of
+    two, all-ones mantissas, bf16 subnormal and near the bf16 maximum): the
+    device's division must give the oracle's correctly rounded fp32 quotient
+    wherever that decides the e4m3 code.  Each group of four is [x, x', 0, 0],
+    so both nonzero elements are kept; random signs."""
+    rng = np.random.default_rng(23)
+    amaxes = [0x3F80, 0x4000, 0x43E0, 0x3FFF, 0x407F, 0x0005, 0x0080, 0x7F7F, 0x7F00, 0x2000, 0x5F7F, 0x3C01]
+    amaxes += [int(b) for b in rng.integers(0x0100, 0x7F00, size=36)]
+    K = 4096
+    rows = []
+    for a in amaxes:
+        mags = np.arange(1, a + 1, dtype=np.uint32)
+        mags = mags[(mags & 0x7F80) != 0x7F80]            # finite only
+        per_row = K // 2 - 2                                # group 0 holds [amax, x, 0, 0]
+        for start in range(0, len(mags), per_row):
+            chunk = mags[start:start + per_row]
+            row = np.zeros(K, np.uint16)
+            row[0] = a
+            xs = np.concatenate([chunk, np.zeros(per_row + 1 - len(chunk), np.uint32)])
+            row[1] = xs[0]
+            g = xs[1:].reshape(-1, 2)
+            body = row[4:].reshape(-1, 4)
+            body[:len(g), 0] = g[:, 0]
+            body[:len(g), 1] = g[:, 1]
+            signs = rng.integers(0, 2, size=K).astype(np.uint16) << 15
+            rows.append((row | signs) * (row != 0))
+    while len(rows) % 128:
+        rows.append(rows[-1])
+    Wb = np.stack(rows).astype(np.uint16)
+    ov, om, os_ = ora.compress_abi(Wb)
+    gv, gm, gs = sp24.compress(dev(Wb))
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    assert np.array_equal(host_bits(gs).view(np.uint32), os_.view(np.uint32)), "scales"
+    assert np.array_equal(host_bits(gm).ravel(), om), "metadata"
+    gvb = host_bits(gv).ravel()
+    bad = np.flatnonzero(gvb != ov)
+    assert bad.size == 0, "%d value bytes differ, first at %s" % (bad.size, bad[:8])
