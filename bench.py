@@ -47,7 +47,10 @@ DESCR = {
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture of the current kernel build (summaries and commands under profiles/).
 # An entry is removed when its kernel changes; absent entries report null.
-CAPTURED_TRAFFIC = {}
+CAPTURED_TRAFFIC = {
+    # sp24_gemm_pair_kernel on the Llama-style linear (M 2048, N 4096, K 4096)
+    ("llama", 2048, "gemm"): 18952448 + 256,
+}
 
 
 def captured_traffic(workload, M, kernel):
