@@ -100,7 +100,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int COLS = C::COLS;
   constexpr int CH = COLS >= 16 ? 16 : COLS;  // columns per TMEM load
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base by pointer arithmetic on the shared array, so that
+  // accesses through it compile to shared-memory instructions
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = sm;
   uint8_t* side_w2 = sm + STAGES * C::STAGE;
   uint8_t* side_x2 = side_w2 + BM * 128;
@@ -348,10 +350,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int pass = 0; pass < 2; ++pass) {
             if (half == pass) {
 #pragma unroll
-              for (int j = 0; j < COLS; ++j) {
-                const float y = (scl[c0 + j] * swr) * __uint_as_float(v[j]);
-                out_row[j * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-              }
+              for (int j = 0; j < COLS; j += 4)
+                scale4_store<false>(scl + c0 + j, swr, v + j, nullptr, out_row + j * 64, 64);
             }
             fence_proxy_async_smem();
             epilogue_bar();
@@ -398,9 +398,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int c = 0; c < COLS; ++c) acc[c] += __ldcg(wsp + c * BM);
             }
 #pragma unroll
-            for (int c = 0; c < COLS; ++c) {
-              const float y = (scl[c0 + c] * swr) * acc[c];
-              out_row[(c0 + c) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            for (int c = 0; c < COLS; c += 4) {
+              const uint32_t a4[4] = {__float_as_uint(acc[c]), __float_as_uint(acc[c + 1]), __float_as_uint(acc[c + 2]),
+                                      __float_as_uint(acc[c + 3])};
+              scale4_store<false>(scl + c0 + c, swr, a4, nullptr, out_row + (c0 + c) * 64, 64);
             }
             if (et == 0) p.counters[tile_id] = 0u;  // ready for the next call
             fence_proxy_async_smem();
@@ -422,17 +423,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_load_cols<CH / 8>(lane_base + NACC * BN + c0 + c, s2);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < CH; ++j) {
-              const float y = fmaf(scl[c0 + c + j] * swr, __uint_as_float(v[j]), __uint_as_float(s2[j]));
-              out_row[(c0 + c + j) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-            }
+            for (int j = 0; j < CH; j += 4)
+              scale4_store<true>(scl + c0 + c + j, swr, v + j, s2 + j, out_row + (c0 + c + j) * 64, 64);
           } else {
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < CH; ++j) {
-              const float y = (scl[c0 + c + j] * swr) * __uint_as_float(v[j]);
-              out_row[(c0 + c + j) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-            }
+            for (int j = 0; j < CH; j += 4)
+              scale4_store<false>(scl + c0 + c + j, swr, v + j, nullptr, out_row + (c0 + c + j) * 64, 64);
           }
         }
         tc_fence_before();
@@ -497,7 +494,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++side_cnt;
         }
 #pragma unroll
-        for (int j = 0; j < COLS; ++j) out_row[(c0 + j) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+        for (int j = 0; j < COLS; j += 4)
+          st_bf16x4(out_row + (c0 + j) * 64, 64, bf16x2_rn(acc[j], acc[j + 1]), bf16x2_rn(acc[j + 2], acc[j + 3]));
       }
       // hand the staged tile to the TMA engine: rows past M are clipped by it
       fence_proxy_async_smem();

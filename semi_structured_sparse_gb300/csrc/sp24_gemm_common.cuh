@@ -60,6 +60,38 @@ __device__ __forceinline__ bool epilogue_bar_any(bool pred) {
 }
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
 
+// Packed round-to-nearest-even of two fp32 values to bf16 (lo in the low
+// half): one conversion instruction for two outputs, which matters because
+// the scalar conversion runs at a fraction of the FP32 rate.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Writes the four bf16 in (lo, hi) to dst[0], dst[stride], dst[2 stride], dst[3 stride].
+__device__ __forceinline__ void st_bf16x4(uint16_t* dst, int stride, uint32_t lo, uint32_t hi) {
+  dst[0] = static_cast<uint16_t>(lo & 0xFFFFu);
+  dst[stride] = static_cast<uint16_t>(lo >> 16);
+  dst[2 * stride] = static_cast<uint16_t>(hi & 0xFFFFu);
+  dst[3 * stride] = static_cast<uint16_t>(hi >> 16);
+}
+// bf16((s_t sw) acc_t + add_t) for 4 consecutive tokens t; s points at their
+// 4 scales (16-byte aligned shared memory, the same address in every lane).
+template <bool ADD>
+__device__ __forceinline__ void scale4_store(const float* s, float sw, const uint32_t* acc, const uint32_t* add,
+                                             uint16_t* dst, int stride) {
+  const float4 s4 = *reinterpret_cast<const float4*>(s);
+  float y[4] = {(s4.x * sw) * __uint_as_float(acc[0]), (s4.y * sw) * __uint_as_float(acc[1]),
+                (s4.z * sw) * __uint_as_float(acc[2]), (s4.w * sw) * __uint_as_float(acc[3])};
+  if constexpr (ADD) {
+    y[0] = fmaf(s4.x * sw, __uint_as_float(acc[0]), __uint_as_float(add[0]));
+    y[1] = fmaf(s4.y * sw, __uint_as_float(acc[1]), __uint_as_float(add[1]));
+    y[2] = fmaf(s4.z * sw, __uint_as_float(acc[2]), __uint_as_float(add[2]));
+    y[3] = fmaf(s4.w * sw, __uint_as_float(acc[3]), __uint_as_float(add[3]));
+  }
+  st_bf16x4(dst, stride, bf16x2_rn(y[0], y[1]), bf16x2_rn(y[2], y[3]));
+}
+
 // Loads `N8 * 8` consecutive accumulator columns of this warp's lanes.
 template <int N8>
 __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {

@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                           const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_y,
                           const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base by pointer arithmetic on the shared array, so that
+  // accesses through it compile to shared-memory instructions
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = sm;
   uint8_t* out_tile = sm + P_STAGES * P_STAGE;                     // [2 channel halves][64 tokens][64] bf16
   float* scl = reinterpret_cast<float*>(out_tile + P_OUT_BYTES);  // token scales of the tile [PN]
@@ -250,10 +252,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < P_COLS / CHUNK; ++i) {
           const int t0 = CHUNK * (half + 2 * i);
 #pragma unroll
-          for (int j = 0; j < CHUNK; ++j) {
-            const float y = (scl[t0 + j] * swr) * __uint_as_float(v[CHUNK * i + j]);
-            ring_row[(t0 + j) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-          }
+          for (int j = 0; j < CHUNK; j += 4)
+            scale4_store<false>(scl + t0 + j, swr, v + CHUNK * i + j, nullptr, ring_row + (t0 + j) * 64, 64);
         }
         fence_proxy_async_smem();
         epilogue_bar();
@@ -273,10 +273,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < NPASS; ++s) {
           const int t0 = P_OUT_TOKENS * s + CHUNK * half;
 #pragma unroll
-          for (int j = 0; j < CHUNK; ++j) {
-            const float y = (scl[t0 + j] * swr) * __uint_as_float(v[CHUNK * s + j]);
-            out_row[(CHUNK * half + j) * 64] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-          }
+          for (int j = 0; j < CHUNK; j += 4)
+            scale4_store<false>(scl + t0 + j, swr, v + CHUNK * s + j, nullptr, out_row + (CHUNK * half + j) * 64, 64);
           fence_proxy_async_smem();
           epilogue_bar();
           if (et == 0) {

@@ -192,14 +192,25 @@ def test_compress_then_gemm_on_device(ora, sp24):
 
 
 # ---------------------------------------------------------------- SM pairs
-@pytest.mark.parametrize("M,N,K", [(193, 256, 256), (256, 512, 128), (300, 768, 512), (511, 256, 1024),
-                                   (2048, 2560, 256)])
+@pytest.mark.parametrize("M,N,K", [(193, 256, 256), (256, 768, 128), (300, 768, 512), (511, 256, 1024),
+                                   (2048, 2816, 256)])
 def test_pair_tiles(ora, sp24, M, N, K):
-    """More than 192 tokens with N a multiple of 256 run on SM pairs: one
-    M = 256 sparse MMA across two SMs per 128-wide K half-step, 256 x 256
+    """More than 192 tokens with N an odd multiple of 256 run on SM pairs:
+    one M = 256 sparse MMA across two SMs per 128-wide K half-step, 256 x 256
     output tiles.  Ragged token tails (the second SM's activation rows past
     M), a single K block, and more tiles than pairs (each pair loops)."""
     w = inputs.Workload("pair", M, N, K, seed=M + N + K)
+    _check_full(ora, sp24, w, "pair M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("M,N,K", [(240, 512, 128), (241, 1024, 640), (481, 512, 1024), (1000, 1536, 2048),
+                                   (2048, 5120, 256)])
+def test_pair_tiles_more_shapes(ora, sp24, M, N, K):
+    """More pair-tile shapes: token tails inside the first and second SM's
+    halves of a 256-token tile, a single K block, K block counts that are not
+    a multiple of the stage depth, and more tiles than pairs (2048 x 5120:
+    160 tiles, so pairs store one tile while the next one runs)."""
+    w = inputs.Workload("pair2", M, N, K, seed=M + N + K + 1)
     _check_full(ora, sp24, w, "pair M=%d N=%d K=%d" % (M, N, K))
 
 
