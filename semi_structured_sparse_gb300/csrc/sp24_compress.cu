@@ -47,11 +47,15 @@ __device__ __forceinline__ uint32_t chunk_amax_bits(const uint4& v) {
 // residual stays in the fp32 normal range (rows below it divide exactly).
 // The sign is copied from x: for x = -0 the residual sum gives +0.
 constexpr float kMinFastScale = 8.0779356e-28f;  // 2^-90
+// The residual is formed as q0 s - x (the negated residual, equally exact)
+// and the correction as q0 - that * r: for x = -0 this keeps q = -0 (with the
+// residual taken as x - q0 s the sum +0 + -0 would give +0), so no separate
+// sign fix is needed; for every other x the two forms compute the same
+// correctly rounded quotient.
 __device__ __forceinline__ float div_scale(float x, float s, float r) {
   const float q0 = __fmul_rn(x, r);
-  const float rem = __fmaf_rn(-q0, s, x);
-  const float q = __fmaf_rn(rem, r, q0);
-  return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+  const float nrem = __fmaf_rn(q0, s, -x);
+  return __fmaf_rn(-nrem, r, q0);
 }
 
 // Two fp32 -> e4m3 conversions in one instruction (round to nearest even,
@@ -77,11 +81,15 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 template <bool FAST>
 __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s, float r) {
-  const uint32_t ml = lo & 0x7FFF7FFFu, mh = hi & 0x7FFF7FFFu;
-  const uint32_t k0 = ((ml << 2) & 0x1FFFCu) | 3u;  // element 0
-  const uint32_t k1 = ((ml >> 14) & 0x1FFFCu) | 2u;  // element 1
-  const uint32_t k2 = ((mh << 2) & 0x1FFFCu) | 1u;  // element 2
-  const uint32_t k3 = (mh >> 14) & 0x1FFFCu;         // element 3
+  // Keys from the raw words: the shifts move each 15-bit magnitude to bits
+  // [16:2] and the mask drops the sign bit and the neighbouring element, so
+  // no separate |w| step is needed.  Left shifts are written as multiplies
+  // and right shifts as high multiplies, which run on the FMA pipe beside the
+  // integer min/max work.
+  const uint32_t k0 = ((lo * 4u) & 0x1FFFCu) | 3u;               // element 0
+  const uint32_t k1 = (__umulhi(lo, 1u << 18) & 0x1FFFCu) | 2u;  // element 1: lo >> 14
+  const uint32_t k2 = ((hi * 4u) & 0x1FFFCu) | 1u;               // element 2
+  const uint32_t k3 = __umulhi(hi, 1u << 18) & 0x1FFFCu;         // element 3
   const uint32_t hi01 = max(k0, k1), lo01 = min(k0, k1);
   const uint32_t hi23 = max(k2, k3), lo23 = min(k2, k3);
   const uint32_t first = max(hi01, hi23);
@@ -91,10 +99,10 @@ __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s
   // byte selector: element i is bytes 2i, 2i+1 of {hi:lo}; kept pair -> {v_i1 : v_i0}
   const uint32_t sel = i0 * 0x22u + i1 * 0x2200u + 0x1010u;
   const uint32_t pair = prmt(lo, hi, sel);
-  const float x0 = __uint_as_float(pair << 16), x1 = __uint_as_float(pair & 0xFFFF0000u);
+  const float x0 = __uint_as_float(pair * 65536u), x1 = __uint_as_float(pair & 0xFFFF0000u);
   const uint32_t q = FAST ? to_e4m3x2(div_scale(x0, s, r), div_scale(x1, s, r))
                           : to_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-  return q | ((i0 + 4u * i1) << 16);
+  return q + i0 * 0x10000u + i1 * 0x40000u;  // q < 2^16: the nibble i0 | i1 << 2 in bits [19:16]
 }
 
 // Two groups (8 bf16 in a 16-byte chunk) -> 4 value bytes and 1 meta byte.
