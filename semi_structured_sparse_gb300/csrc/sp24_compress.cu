@@ -11,6 +11,7 @@
 // Groupwise scaling along M for FP8 gemm", ScaleGranularity description).
 // Activation path: same PR #3258, the activation is divided by its scale and
 // cast to e4m3.
+#include <cuda_bf16.h>
 #include "sp24_internal.cuh"
 #include "sp24_ptx.cuh"
 
@@ -26,6 +27,21 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_
 __device__ __forceinline__ float weight_scale(uint32_t amax_bits) {
   return amax_bits == 0 ? 1.0f : __fdiv_rn(bf16_bits_to_float(amax_bits), kE4M3Max);
 }
+
+// Running max of |w| over 16-byte chunks, kept as a packed bf16 pair: for
+// finite bf16 the order of |w| is the order of the magnitude bits, so the
+// packed bf16 max (on the half-precision pipe, beside the integer work of the
+// packing) gives the same result as an integer max of the magnitude bits.
+__device__ __forceinline__ uint32_t amax2_acc(uint32_t acc, const uint4& v) {
+  const __nv_bfloat162 a = __hmax2(__habs2(*reinterpret_cast<const __nv_bfloat162*>(&v.x)),
+                                   __habs2(*reinterpret_cast<const __nv_bfloat162*>(&v.y)));
+  const __nv_bfloat162 b = __hmax2(__habs2(*reinterpret_cast<const __nv_bfloat162*>(&v.z)),
+                                   __habs2(*reinterpret_cast<const __nv_bfloat162*>(&v.w)));
+  const __nv_bfloat162 m = __hmax2(__hmax2(a, b), *reinterpret_cast<const __nv_bfloat162*>(&acc));
+  return *reinterpret_cast<const uint32_t*>(&m);
+}
+// Magnitude bits of the larger half of a packed pair from amax2_acc.
+__device__ __forceinline__ uint32_t amax2_bits(uint32_t acc) { return max(acc & 0x7FFFu, (acc >> 16) & 0x7FFFu); }
 
 // Largest bf16 magnitude (sign cleared) among the 8 values of a 16-byte
 // chunk, with packed 16-bit unsigned max.
@@ -79,7 +95,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
-template <bool FAST>
+template <bool FAST, int NIB_SHIFT = 16>
 __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s, float r) {
   // Keys from the raw words: the shifts move each 15-bit magnitude to bits
   // [16:2] and the mask drops the sign bit and the neighbouring element, so
@@ -102,16 +118,17 @@ __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s
   const float x0 = __uint_as_float(pair * 65536u), x1 = __uint_as_float(pair & 0xFFFF0000u);
   const uint32_t q = FAST ? to_e4m3x2(div_scale(x0, s, r), div_scale(x1, s, r))
                           : to_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-  return q + i0 * 0x10000u + i1 * 0x40000u;  // q < 2^16: the nibble i0 | i1 << 2 in bits [19:16]
+  // q < 2^16: the nibble i0 | i1 << 2 goes to bits [NIB_SHIFT + 3 : NIB_SHIFT]
+  return q + i0 * (1u << NIB_SHIFT) + i1 * (4u << NIB_SHIFT);
 }
 
 // Two groups (8 bf16 in a 16-byte chunk) -> 4 value bytes and 1 meta byte.
 template <bool FAST>
 __device__ __forceinline__ void pack_chunk(const uint4& v, float s, float r, uint32_t& vals, uint32_t& metab) {
-  const uint32_t g0 = pack_group<FAST>(v.x, v.y, s, r);
-  const uint32_t g1 = pack_group<FAST>(v.z, v.w, s, r);
-  vals = (g0 & 0xFFFFu) | (g1 << 16);
-  metab = (g0 >> 16) | ((g1 >> 16) << 4);
+  const uint32_t g0 = pack_group<FAST, 16>(v.x, v.y, s, r);  // nibble in bits [19:16]
+  const uint32_t g1 = pack_group<FAST, 20>(v.z, v.w, s, r);  // nibble in bits [23:20]
+  vals = prmt(g0, g1, 0x5410u);           // codes of group 0 in bytes 0-1, group 1 in bytes 2-3
+  metab = prmt(g0 | g1, 0u, 0x4442u);     // byte 2 of (g0 | g1): the two nibbles
 }
 
 // Storage the GEMM reads (see sp24.h): 128-row x 128-K tiles, tile-contiguous,
@@ -201,20 +218,20 @@ __global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* _
     const bool valid = n < N;
     const uint16_t* row = W + static_cast<int64_t>(valid ? n : 0) * ldw;
     uint4 held[kHeldChunks];
-    uint32_t amax = 0;
+    uint32_t amax2 = 0;
 #pragma unroll
     for (int i = 0; i < kHeldChunks; ++i) {
       const int c = 2 * i + h, k = c * 256 + lane * 8;
       if (valid && c < nchunks && k < K) {
         held[i] = ldg_stream(row + k);
-        amax = max(amax, chunk_amax_bits(held[i]));
+        amax2 = amax2_acc(amax2, held[i]);
       }
     }
     for (int c = 2 * kHeldChunks + h; valid && c < nchunks; c += 2) {  // rows longer than 4096: stream for amax
       const int k = c * 256 + lane * 8;
-      if (k < K) amax = max(amax, chunk_amax_bits(ldg_stream(row + k)));
+      if (k < K) amax2 = amax2_acc(amax2, ldg_stream(row + k));
     }
-    amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+    uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, amax2_bits(amax2));
     if (lane == 0) pair_amax[warp] = amax;
     __syncthreads();
     if (!valid) return;
