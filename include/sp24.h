@@ -144,7 +144,11 @@ SP24_API sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K,
  *           16-byte aligned.
  *   workspace, workspace_bytes: device scratch of at least
  *           sp24_fp8_gemm_workspace_size(M, N, K, r) bytes (may be NULL when
- *           that size is 0).
+ *           that size is 0).  It holds the fp32 partial sums of tiles whose K
+ *           range is split across CTAs (when the tiles alone would leave SMs
+ *           idle in the last wave) and one flag per split; it needs no
+ *           clearing, but calls that overlap on the GPU must not share it.
+ *           With less than the queried size the call runs unsplit.
  * Preconditions: M >= 1; N a positive multiple of 128; K a positive multiple
  * of 128; all scales finite and > 0; device pointers 16-byte aligned.
  * Errors: SP24_ERR_* as above; device-side wait timeouts are reported by
@@ -175,8 +179,8 @@ SP24_API sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, i
  *   - A shape whose scratch need (sp24_fp8_gemm_workspace_size) exceeds
  *     4 MiB is refused with SP24_ERR_WORKSPACE; shapes that need no scratch
  *     always run.
- * The tile counters in the scratch are cleared on the stream before each
- * use; everything else it holds from the previous call is overwritten.
+ * Nothing in the scratch needs clearing between calls: the split flags carry
+ * a per-launch epoch, and the partial sums are overwritten.
  */
 SP24_API sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
                                                  int gM, const void* values, const void* meta, const float* sw,

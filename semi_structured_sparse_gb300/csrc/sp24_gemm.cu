@@ -29,6 +29,8 @@
 // the sparse K loop the MMA thread issues bf16 tcgen05.mma over r <= 64 into
 // a second accumulator that the epilogue adds after scaling.
 #include <cuda_bf16.h>
+#include <atomic>
+#include <chrono>
 #include <mutex>
 #include "sp24_gemm_common.cuh"
 #include "sp24_internal.cuh"
@@ -119,7 +121,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* sacce = saccf + 1;             // side accumulator drained
   uint64_t* drain = sacce + 1;             // MMA drain on abort
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile uint32_t* last_flag = tslot + 1;  // split-K: this CTA completes the tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_units = p.m_tiles * p.n_tiles * p.splits;
@@ -367,43 +368,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if constexpr (SPLIT) {
           if (p.splits > 1) {
-            // unscaled fp32 partial of this K split -> workspace [tile][split][col][row]
+            // unscaled fp32 partials of the K splits of a tile, [tile][split][col][row]
             const int tile_id = t.m_tile * p.n_tiles + t.n_tile;
-            float* wpart = p.ws + (static_cast<int64_t>(tile_id) * p.splits + t.split) * (BN * BM);
+            unsigned long long* tflags = p.flags + static_cast<int64_t>(tile_id) * p.splits;
+            if (t.split < p.splits - 1) {
+              // an earlier split: publish the partial for the tile's last split
+              float* wpart = p.ws + (static_cast<int64_t>(tile_id) * p.splits + t.split) * (BN * BM);
+#pragma unroll
+              for (int c = 0; c < COLS; c += CH) {
+                uint32_t v[CH];
+                tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < CH; ++j) __stcg(wpart + (c0 + c + j) * BM + row, __uint_as_float(v[j]));
+              }
+              tc_fence_before();
+              mbar_arrive(&acce[b]);
+              ++acc_cnt;
+              __threadfence();
+              epilogue_bar();
+              if (et == 0) st_release_u64(&tflags[t.split], p.epoch);
+              continue;
+            }
+            // The tile's last split completes it: its own accumulator, then the
+            // earlier splits' partials in split order (a fixed summation order,
+            // whatever the arrival order).  Units are ordered split-major within
+            // a token tile, so every earlier split was handed to a CTA no later
+            // than this one and all CTAs are resident: the waits end.
+            float acc[COLS];
 #pragma unroll
             for (int c = 0; c < COLS; c += CH) {
               uint32_t v[CH];
               tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
               tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < CH; ++j) __stcg(wpart + (c0 + c + j) * BM + row, __uint_as_float(v[j]));
+              for (int j = 0; j < CH; ++j) acc[c + j] = __uint_as_float(v[j]);
             }
             tc_fence_before();
             mbar_arrive(&acce[b]);
             ++acc_cnt;
-            __threadfence();
-            epilogue_bar();
-            if (et == 0) *last_flag = atomicAdd(&p.counters[tile_id], 1u) == static_cast<unsigned>(p.splits - 1);
-            epilogue_bar();
-            if (!*last_flag) continue;
-            // the last split to arrive sums all partials in split order (deterministic)
-            __threadfence();
             const float* wtile = p.ws + static_cast<int64_t>(tile_id) * p.splits * (BN * BM);
-            float acc[COLS];
-#pragma unroll
-            for (int c = 0; c < COLS; ++c) acc[c] = 0.0f;
-            for (int sp = 0; sp < p.splits; ++sp) {  // all columns of one split per round: COLS loads in flight
-              const float* wsp = wtile + sp * (BN * BM) + c0 * BM + row;
+            for (int sp = 0; sp < p.splits - 1; ++sp) {
+              bool got = true;
+              if (et == 0) {
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_acquire_u64(&tflags[sp]) != p.epoch) {
+                  if (globaltimer_ns() - t0 > SP24_WAIT_TIMEOUT_NS) { got = false; break; }
+                }
+              }
+              if (epilogue_bar_any(!got)) { ok = false; break; }
+              const float* wsp = wtile + sp * (BN * BM) + c0 * BM + row;  // all columns of one split: COLS loads in flight
 #pragma unroll
               for (int c = 0; c < COLS; ++c) acc[c] += __ldcg(wsp + c * BM);
             }
+            if (!ok) break;
 #pragma unroll
             for (int c = 0; c < COLS; c += 4) {
               const uint32_t a4[4] = {__float_as_uint(acc[c]), __float_as_uint(acc[c + 1]), __float_as_uint(acc[c + 2]),
                                       __float_as_uint(acc[c + 3])};
               scale4_store<false>(scl + c0 + c, swr, a4, nullptr, out_row + (c0 + c) * 64, 64);
             }
-            if (et == 0) p.counters[tile_id] = 0u;  // ready for the next call
             fence_proxy_async_smem();
             epilogue_bar();
             if (et == 0) {
@@ -596,7 +620,9 @@ int pick_bn(int64_t M, bool plain) {
 
 // K splits for small-token shapes whose weight tiles alone leave SMs idle:
 // the smallest split count (up to 8, at least 4 K steps each) whose units
-// fill the SMs at least 5 % better than no split.
+// fill the SMs at least 5 % better than no split.  (When the tiles already
+// occupy half the SMs or more, splitting only to even out the last wave does
+// not pay: fewer SMs still pull the weights at full HBM rate.)
 int pick_splits(int tiles, int k_stages, int sm_count, bool splittable) {
   if (!splittable || 2 * tiles >= sm_count) return 1;  // at least half the SMs busy without splitting
   auto fill = [&](int s) {
@@ -615,9 +641,24 @@ int pick_splits(int tiles, int k_stages, int sm_count, bool splittable) {
   return best;
 }
 
+std::atomic<unsigned long long> g_epoch{0};
+
+// A fresh 64-bit epoch per split launch: larger than the value of any flag an
+// earlier launch in this process published, and, from a clock-derived base,
+// not a plausible leftover of another process.
+unsigned long long next_epoch() {
+  unsigned long long e = g_epoch.load();
+  if (e == 0) {
+    const unsigned long long base =
+        (static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) << 8) | 1ull;
+    g_epoch.compare_exchange_strong(e, base);
+  }
+  return ++g_epoch;
+}
+
 struct Plan {
   int bn, ks, m_tiles, n_tiles, k_tiles, splits;
-  size_t ws_partials, ws_bytes;  // partials bytes; total with counters (0 when not splitting)
+  size_t ws_partials, ws_bytes;  // partials bytes; total with the split flags (0 when not splitting)
 };
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, bool promote, bool side, int sm_count) {
@@ -631,7 +672,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bool promote, bool side, int sm_
   pl.splits = pick_splits(pl.m_tiles * pl.n_tiles, pl.k_tiles / pl.ks, sm_count, !promote && !side && pl.bn <= 64);
   const size_t tiles = static_cast<size_t>(pl.m_tiles) * pl.n_tiles;
   pl.ws_partials = pl.splits > 1 ? tiles * pl.splits * pl.bn * BM * sizeof(float) : 0;
-  pl.ws_bytes = pl.splits > 1 ? pl.ws_partials + tiles * sizeof(unsigned int) : 0;
+  pl.ws_bytes = pl.splits > 1 ? pl.ws_partials + tiles * pl.splits * sizeof(unsigned long long) : 0;
   return pl;
 }
 
@@ -703,7 +744,8 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   a.splits = pl.splits;
   a.kt_per_split = ((pl.k_tiles / pl.ks + pl.splits - 1) / pl.splits) * pl.ks;
   a.ws = nullptr;
-  a.counters = nullptr;
+  a.flags = nullptr;
+  a.epoch = 0;
   a.err = dev->err_word;
   if (static_cast<int64_t>(a.m_tiles) * a.n_tiles * a.splits > (1 << 30)) return SP24_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -729,10 +771,12 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   if (st != SP24_OK) return st;
 
   if (pl.splits > 1) {
+    // the partials, then one 8-byte flag per (tile, split); a fresh epoch per
+    // launch makes every flag left by an earlier launch read as unpublished,
+    // so the workspace needs no clearing
     a.ws = static_cast<float*>(workspace);
-    a.counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + pl.ws_partials);
-    const size_t counter_bytes = static_cast<size_t>(a.m_tiles) * a.n_tiles * sizeof(unsigned int);
-    if (cudaMemsetAsync(a.counters, 0, counter_bytes, s) != cudaSuccess) return SP24_ERR_CUDA;
+    a.flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + pl.ws_partials);
+    a.epoch = next_epoch();
   }
   if (promote)
     return side ? launch_bn<true, true>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
@@ -785,14 +829,13 @@ extern "C" sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* 
                                                    int64_t N, int gN, int gK, const void* X2, const void* W2,
                                                    int64_t r, void* Y, int64_t ldy, void* stream) {
   using namespace sp24;
-  // scratch this shape needs (split-K partials and tile counters); more than the
+  // scratch this shape needs (split-K partials and their flags); more than the
   // fixed array holds is refused rather than silently run another way
   if (sp24_fp8_gemm_workspace_size(M, N, K, r) > kFixedScratchBytes) return SP24_ERR_WORKSPACE;
   void* scratch = nullptr;
   const sp24_status st = fixed_scratch_address(&scratch);
   if (st != SP24_OK) return st;
-  // sp24_fp8_gemm clears the tile counters in the scratch (stream-ordered) before
-  // the kernel runs; the partial sums need no clearing.
+  // Nothing in the scratch needs clearing: split flags carry a per-launch epoch.
   return sp24_fp8_gemm(Xq, sx, M, K, ldx, gM, values, meta, sw, N, gN, gK, X2, W2, r, Y, ldy, scratch,
                        kFixedScratchBytes, stream);
 }

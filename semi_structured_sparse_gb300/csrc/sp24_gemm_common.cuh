@@ -24,7 +24,8 @@ struct GemmArgs {
   int splits;       // K splits per output tile (1 = none)
   int kt_per_split; // 128-K sub-tiles per split (a multiple of the stage's KS)
   float* ws;        // split-K partials [tile][split][BN][128] (fp32, unscaled)
-  unsigned int* counters;  // split-K arrival counters [tile], zero on entry
+  unsigned long long* flags;  // split-K: [tile][split], the epoch at which that partial was published
+  unsigned long long epoch;   // this launch's epoch (split-K), larger than any earlier launch's
   unsigned int* err;
 };
 
@@ -105,6 +106,16 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
 }
 
 }  // namespace
+
+// Global-memory publish/observe of a 64-bit flag (release/acquire at GPU scope).
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // SM-pair kernel (sp24_gemm_pair.cu): plain per-token x per-channel scaling,
 // 256 weight rows x 256 tokens per pair tile.  pair_gemm_applies says whether
