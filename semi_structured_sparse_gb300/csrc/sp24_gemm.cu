@@ -750,7 +750,8 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   if (static_cast<int64_t>(a.m_tiles) * a.n_tiles * a.splits > (1 << 30)) return SP24_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // large token counts with plain scaling: 256 x 256 tiles on SM pairs
-  if (pair_gemm_applies(M, N, K, !promote && !side)) return launch_pair_gemm(dev, Xq, ldx, Y, ldy, a, s);
+  if (pair_gemm_applies(M, N, K, !promote, r))
+    return launch_pair_gemm(dev, Xq, ldx, Y, ldy, X2, W2, r, a, s);
 
   const int bn = pl.bn;
   CUtensorMap tm_x, tm_w2, tm_x2, tm_y;

@@ -117,12 +117,13 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   return v;
 }
 
-// SM-pair kernel (sp24_gemm_pair.cu): plain per-token x per-channel scaling,
-// 256 weight rows x 256 tokens per pair tile.  pair_gemm_applies says whether
-// a call takes it; launch_pair_gemm builds its tensor maps and launches it
-// (args: operands, scales, sizes and the error word; tile counts are its own).
-bool pair_gemm_applies(int64_t M, int64_t N, int64_t K, bool plain);
+// SM-pair kernel (sp24_gemm_pair.cu): per-token x per-channel scaling (gK =
+// K), 256 weight rows x 256 tokens per pair tile, or x 240 tokens with the
+// fused side GEMM (r <= 64).  pair_gemm_applies says whether a call takes it;
+// launch_pair_gemm builds its tensor maps and launches it (args: operands,
+// scales, sizes and the error word; tile counts are its own).
+bool pair_gemm_applies(int64_t M, int64_t N, int64_t K, bool plain, int64_t r);
 sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
-                             const GemmArgs& args, cudaStream_t stream);
+                             const void* X2, const void* W2, int64_t r, const GemmArgs& args, cudaStream_t stream);
 
 }  // namespace sp24

@@ -35,6 +35,15 @@
 //              passes; for the CTA's last tile the idle stage ring holds the
 //              whole tile and the stores go out at once.
 //
+// Fused side GEMM (SIDE, CUTLASS issue #2058: Y = X1 W1^T + X2 W2^T in one
+// kernel).  Token tiles are then 240 wide, so that TMEM holds the main
+// accumulator (columns 0-239), the side accumulator (240-479) and an 8-slot
+// metadata ring (480-511, one slot per K block in flight).  Each tile starts
+// with one extra pipeline stage that carries the W2 tile of the CTA's 128
+// channels and the X2 rows of its 120 tokens (bf16, 128-byte swizzle); the
+// MMA thread turns it into r / 16 bf16 M = 256 MMAs into the side
+// accumulator.  The epilogue forms bf16((sx sw) acc + side).
+//
 // The kernel is launched with programmatic stream serialisation: its
 // prologue (barriers, TMEM, descriptor prefetch) overlaps the previous
 // kernel's tail, and pdl_wait() precedes every global-memory access.
@@ -44,46 +53,89 @@
 namespace sp24 {
 namespace {
 
-constexpr int PN = 256;                        // tokens per pair tile (MMA N)
-constexpr int HALF_N = PN / 2;                 // activation rows each CTA loads
 constexpr int KS = 2;                          // K blocks per stage
-constexpr int P_B = HALF_N * BK;               // 16 KB of activations per CTA per K block
-constexpr int P_A_OFF = 0;                     // KS values tiles (contiguous in the tiled storage)
-constexpr int P_META_OFF = KS * A_STAGE;       // KS metadata tiles
-constexpr int P_B_OFF = KS * (A_STAGE + META_STAGE);
-constexpr int P_STAGE = P_B_OFF + KS * P_B;    // bytes each CTA receives per stage
-constexpr int P_OUT_TOKENS = 64;               // tokens per staged store pass
-constexpr int P_OUT_BYTES = P_OUT_TOKENS * BM * 2;
-constexpr int P_SCALE_BYTES = 4 * PN;
-constexpr int P_FIXED = 1024 + P_OUT_BYTES + P_SCALE_BYTES + BAR_BYTES;
-constexpr int P_STAGES_FIT = (SMEM_LIMIT - P_FIXED) / P_STAGE;
-constexpr int P_STAGES = P_STAGES_FIT < META_SLOTS / KS ? P_STAGES_FIT : META_SLOTS / KS;
-constexpr int P_SMEM = P_FIXED + P_STAGES * P_STAGE;
-constexpr int P_COLS = PN / 2;                 // accumulator columns per epilogue warp
-constexpr int CHUNK = 32;                      // token chunk: warp half h holds chunks h, h + 2, ...
-constexpr int NPASS = PN / P_OUT_TOKENS;
 constexpr int VROWS = A_STAGE / 128;           // a values tile is 64 rows of 128 B
 constexpr int MROWS = META_STAGE / 128;        // a metadata tile is 16 rows of 128 B
-static_assert(P_B_OFF % 1024 == 0 && P_STAGE % 1024 == 0, "1024-byte swizzle alignment");
-static_assert(P_STAGES >= 3 && P_STAGES <= MAX_STAGES, "pipeline depth");
-static_assert(PN <= META_COL0, "TMEM columns");
-static_assert(P_OUT_TOKENS == 2 * CHUNK, "each pass takes one chunk from each warp half");
-static_assert(P_STAGES * P_STAGE >= PN * BM * 2, "the ring holds a whole output tile");
+constexpr int SIDE_COL = 240;                  // first TMEM column of the side accumulator
+constexpr int SIDE_W2_BYTES = BM * 128;        // side stage: W2 tile (128 channels x 64 bf16)
 
+template <int PN_, bool SIDE_>
+struct PairCfg {
+  static constexpr int PN = PN_;                    // tokens per pair tile (MMA N)
+  static constexpr bool SIDE = SIDE_;
+  static constexpr int HALF_N = PN / 2;             // activation rows each CTA loads
+  static constexpr int P_B = HALF_N * BK;           // activations per CTA per K block
+  static constexpr int A_OFF = 0;                   // KS values tiles (contiguous in the tiled storage)
+  static constexpr int META_OFF = KS * A_STAGE;     // KS metadata tiles
+  static constexpr int B_OFF = KS * (A_STAGE + META_STAGE);
+  static constexpr int STAGE = B_OFF + KS * P_B;    // bytes each CTA receives per stage
+  static constexpr int CHUNK = SIDE ? 24 : 32;      // token chunk: warp half h holds chunks h, h + 2, ...
+  static constexpr int OUT_TOKENS = 2 * CHUNK;      // tokens per staged store pass
+  static constexpr int OUT_BYTES = OUT_TOKENS * BM * 2;
+  static constexpr int SCALE_BYTES = 4 * 256;
+  static constexpr int FIXED = 1024 + OUT_BYTES + SCALE_BYTES + BAR_BYTES;
+  static constexpr int META_RING = SIDE ? 8 : META_SLOTS;  // metadata slots (4 TMEM columns each)
+  static constexpr int META_BASE = SIDE ? 480 : META_COL0;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE;
+  static constexpr int STAGES = STAGES_FIT < META_RING / KS ? STAGES_FIT : META_RING / KS;
+  static constexpr int SMEM = FIXED + STAGES * STAGE;
+  static constexpr int COLS = PN / 2;               // accumulator columns per epilogue warp
+  static constexpr int NCHUNK = COLS / CHUNK;       // chunks per epilogue warp
+  static constexpr int NPASS = PN / OUT_TOKENS;
+  static constexpr int SIDE_X2_BYTES = HALF_N * 128;  // side stage: this CTA's X2 rows
+  static_assert(B_OFF % 1024 == 0 && STAGE % 1024 == 0 && P_B % 1024 == 0, "1024-byte swizzle alignment");
+  static_assert(STAGES >= 3 && STAGES <= MAX_STAGES, "pipeline depth");
+  static_assert(SIDE ? (PN <= SIDE_COL && SIDE_COL + PN <= META_BASE) : PN <= META_COL0, "TMEM columns");
+  static_assert(NCHUNK * CHUNK == COLS && CHUNK % 8 == 0 && OUT_TOKENS * NPASS == PN, "epilogue chunks");
+  static_assert(STAGES * STAGE >= PN * BM * 2, "the ring holds a whole output tile");
+  static_assert(!SIDE || SIDE_W2_BYTES + SIDE_X2_BYTES <= STAGE, "the side operands fit one stage");
+};
+
+// bf16((s_t sw) acc_t [+ add_t]) of 4 consecutive tokens, as two packed words.
+template <bool ADD>
+__device__ __forceinline__ uint2 scale4_pack(const float* s, float sw, const uint32_t* acc, const uint32_t* add) {
+  const float4 s4 = *reinterpret_cast<const float4*>(s);
+  float y0, y1, y2, y3;
+  if constexpr (ADD) {
+    y0 = fmaf(s4.x * sw, __uint_as_float(acc[0]), __uint_as_float(add[0]));
+    y1 = fmaf(s4.y * sw, __uint_as_float(acc[1]), __uint_as_float(add[1]));
+    y2 = fmaf(s4.z * sw, __uint_as_float(acc[2]), __uint_as_float(add[2]));
+    y3 = fmaf(s4.w * sw, __uint_as_float(acc[3]), __uint_as_float(add[3]));
+  } else {
+    y0 = (s4.x * sw) * __uint_as_float(acc[0]);
+    y1 = (s4.y * sw) * __uint_as_float(acc[1]);
+    y2 = (s4.z * sw) * __uint_as_float(acc[2]);
+    y3 = (s4.w * sw) * __uint_as_float(acc[3]);
+  }
+  return make_uint2(bf16x2_rn(y0, y1), bf16x2_rn(y2, y3));
+}
+
+// Loads N consecutive accumulator columns (N a multiple of 8) of this warp's lanes.
+template <int N>
+__device__ __forceinline__ void tmem_load_n(uint32_t taddr, uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i + 16 <= N; i += 16) tmem_ld16(taddr + i, *reinterpret_cast<uint32_t(*)[16]>(r + i));
+  if constexpr (N % 16 != 0) tmem_ld8(taddr + (N / 16) * 16, r + (N / 16) * 16);
+}
+
+template <int PN, bool SIDE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sp24_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_y,
+                          const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x2,
                           const GemmArgs p) {
+  using C = PairCfg<PN, SIDE>;
+  constexpr int HALF_N = C::HALF_N, CHUNK = C::CHUNK;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base by pointer arithmetic on the shared array, so that
   // accesses through it compile to shared-memory instructions
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = sm;
-  uint8_t* out_tile = sm + P_STAGES * P_STAGE;                     // [2 channel halves][64 tokens][64] bf16
-  float* scl = reinterpret_cast<float*>(out_tile + P_OUT_BYTES);  // token scales of the tile [PN]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(out_tile + P_OUT_BYTES + P_SCALE_BYTES);
-  uint64_t* full = bars;                  // [P_STAGES] leader: both CTAs' loads -> MMA
-  uint64_t* empty = bars + MAX_STAGES;    // [P_STAGES] each CTA: MMA done with the stage -> its loads
+  uint8_t* out_tile = sm + C::STAGES * C::STAGE;                   // [2 channel halves][OUT_TOKENS][64] bf16
+  float* scl = reinterpret_cast<float*>(out_tile + C::OUT_BYTES);  // token scales of the tile [PN]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_tile + C::OUT_BYTES + C::SCALE_BYTES);
+  uint64_t* full = bars;                  // [STAGES] leader: both CTAs' loads -> MMA
+  uint64_t* empty = bars + MAX_STAGES;    // [STAGES] each CTA: MMA done with the stage -> its loads
   uint64_t* accf = bars + 2 * MAX_STAGES; // each CTA: accumulator complete -> its epilogue
   uint64_t* acce = accf + 1;              // leader: both epilogues drained the accumulator -> MMA
   uint64_t* drain = acce + 1;             // leader: every MMA finished (before TMEM is freed)
@@ -97,7 +149,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int num_units = p.m_tiles * p.n_tiles;
   const int k_stages = (p.k_tiles + KS - 1) / KS;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < P_STAGES; ++i) {
+    for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
@@ -111,6 +163,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_m);
     tma_prefetch_desc(&tm_y);
+    if (SIDE) {
+      tma_prefetch_desc(&tm_w2);
+      tma_prefetch_desc(&tm_x2);
+    }
   }
   if (warp == MMA_WARP) {
     tmem_alloc_pair(tslot, 512);
@@ -132,24 +188,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int m0 = (u / p.n_tiles) * PN + static_cast<int>(rank) * HALF_N;  // this CTA's token rows
       const int vrow = n_tile * p.k_tiles * VROWS;
       const int mrow = n_tile * p.k_tiles * MROWS;
-      for (int ks = 0; ks < k_stages; ++ks, ++flat) {
+      // with SIDE, stage -1 of the tile carries the side operands
+      for (int ks = SIDE ? -1 : 0; ks < k_stages; ++ks, ++flat) {
         if (flat % PRODUCERS != warp) continue;
-        const uint32_t stage = static_cast<uint32_t>(flat % P_STAGES);
-        const uint32_t phase = static_cast<uint32_t>((flat / P_STAGES) & 1);
+        const uint32_t stage = static_cast<uint32_t>(flat % C::STAGES);
+        const uint32_t phase = static_cast<uint32_t>((flat / C::STAGES) & 1);
         const bool got = mbar_wait(&empty[stage], phase ^ 1);
         if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
         if (lane == 0) {
-          // Always KS blocks: with an odd block count the last stage's second
-          // block reads the next weight tile's rows (or zero fill past the end)
-          // and K coordinates past K (zero fill); the MMA skips it.
-          const int kt = ks * KS;
           const uint32_t fb = full0 + 8u * stage;
-          uint8_t* st = ring + stage * P_STAGE;
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE);  // both CTAs' bytes
-          tma_load_2d_pair(st + P_A_OFF, &tm_v, fb, 0, vrow + kt * VROWS);
-          tma_load_2d_pair(st + P_META_OFF, &tm_m, fb, 0, mrow + kt * MROWS);
+          uint8_t* st = ring + stage * C::STAGE;
+          if (SIDE && ks < 0) {
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (SIDE_W2_BYTES + C::SIDE_X2_BYTES));
+            tma_load_2d_pair(st, &tm_w2, fb, 0, n_tile * BM);
+            tma_load_2d_pair(st + SIDE_W2_BYTES, &tm_x2, fb, 0, m0);
+          } else {
+            // Always KS blocks: with an odd block count the last stage's second
+            // block reads the next weight tile's rows (or zero fill past the end)
+            // and K coordinates past K (zero fill); the MMA skips it.
+            const int kt = ks * KS;
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE);  // both CTAs' bytes
+            tma_load_2d_pair(st + C::A_OFF, &tm_v, fb, 0, vrow + kt * VROWS);
+            tma_load_2d_pair(st + C::META_OFF, &tm_m, fb, 0, mrow + kt * MROWS);
 #pragma unroll
-          for (int j = 0; j < KS; ++j) tma_load_2d_pair(st + P_B_OFF + j * P_B, &tm_x, fb, (kt + j) * BK, m0);
+            for (int j = 0; j < KS; ++j) tma_load_2d_pair(st + C::B_OFF + j * C::P_B, &tm_x, fb, (kt + j) * BK, m0);
+          }
         }
       }
     }
@@ -159,44 +222,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // copies have landed and nothing writes this CTA's shared memory later).
       // Only the last use of a slot may be waited on.
       const int64_t fmax = flat - 1;
-      for (int64_t f = fmax; f >= 0 && f > fmax - P_STAGES; --f) {
+      for (int64_t f = fmax; f >= 0 && f > fmax - C::STAGES; --f) {
         if (f % PRODUCERS != warp) continue;
-        (void)mbar_wait(&empty[f % P_STAGES], static_cast<uint32_t>((f / P_STAGES) & 1));
+        (void)mbar_wait(&empty[f % C::STAGES], static_cast<uint32_t>((f / C::STAGES) & 1));
       }
     }
   } else if (warp == MMA_WARP) {
     // ----------------------------------------------------------- MMA issuer
     if (leader && lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3(2 * BM, PN, true);
-      constexpr uint64_t STAGE_DESC = P_STAGE >> 4;
+      constexpr uint32_t idesc_side = idesc_bf16(2 * BM, PN);
+      constexpr uint64_t STAGE_DESC = C::STAGE >> 4;
       const uint32_t ring_u32 = smem_u32(ring);
-      const uint64_t a_desc0 = smem_desc(ring_u32 + P_A_OFF, 16, 512, SWZ_64B);
-      const uint64_t m_desc0 = smem_desc(ring_u32 + P_META_OFF, 128, 128, SWZ_NONE);
-      const uint64_t b_desc0 = smem_desc(ring_u32 + P_B_OFF, 16, 1024, SWZ_128B);
+      const uint64_t a_desc0 = smem_desc(ring_u32 + C::A_OFF, 16, 512, SWZ_64B);
+      const uint64_t m_desc0 = smem_desc(ring_u32 + C::META_OFF, 128, 128, SWZ_NONE);
+      const uint64_t b_desc0 = smem_desc(ring_u32 + C::B_OFF, 16, 1024, SWZ_128B);
+      const uint64_t w2_desc0 = smem_desc(ring_u32, 16, 1024, SWZ_128B);
+      const uint64_t x2_desc0 = smem_desc(ring_u32 + SIDE_W2_BYTES, 16, 1024, SWZ_128B);
       uint32_t stage = 0, phase = 0, meta_ctr = 0, acc_cnt = 0;
       bool ok = true;
       for (int u = pair; u < num_units && ok; u += npairs) {
         if (!mbar_wait(acce, (acc_cnt & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
-        for (int ks = 0; ks < k_stages; ++ks) {
+        for (int ks = SIDE ? -1 : 0; ks < k_stages; ++ks) {
           if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
           const uint64_t off = stage * STAGE_DESC;
-          const int nsub = min(KS, p.k_tiles - ks * KS);
+          if (SIDE && ks < 0) {
+            // X2 W2^T into the side accumulator: r / 16 bf16 MMAs, +32 B per 16 of K
+            for (int j = 0; j < p.side_ksteps; ++j)
+              mma_bf16_pair(tbase + SIDE_COL, w2_desc0 + off + 2 * j, x2_desc0 + off + 2 * j, idesc_side,
+                            j > 0 ? 1u : 0u);
+          } else {
+            const int nsub = min(KS, p.k_tiles - ks * KS);
 #pragma unroll
-          for (int j = 0; j < KS; ++j) {
-            if (j < nsub) {
-              const uint32_t mcol = tbase + META_COL0 + 4 * (meta_ctr & (META_SLOTS - 1));
-              ++meta_ctr;
-              tmem_cp_128x128b_pair(mcol, m_desc0 + off + j * (META_STAGE >> 4));
-              const uint64_t aj = a_desc0 + off + j * (A_STAGE >> 4);
-              const uint64_t bj = b_desc0 + off + j * (P_B >> 4);
-              mma_sp_e4m3_pair(tbase, aj, bj, mcol, idesc, (ks != 0 || j != 0) ? 1u : 0u);
-              mma_sp_e4m3_pair(tbase, aj + 2, bj + 4, mcol + 2, idesc, 1u);  // +32 B of A, +64 B of B
+            for (int j = 0; j < KS; ++j) {
+              if (j < nsub) {
+                const uint32_t mcol = tbase + C::META_BASE + 4 * (meta_ctr & (C::META_RING - 1));
+                ++meta_ctr;
+                tmem_cp_128x128b_pair(mcol, m_desc0 + off + j * (META_STAGE >> 4));
+                const uint64_t aj = a_desc0 + off + j * (A_STAGE >> 4);
+                const uint64_t bj = b_desc0 + off + j * (C::P_B >> 4);
+                mma_sp_e4m3_pair(tbase, aj, bj, mcol, idesc, (ks != 0 || j != 0) ? 1u : 0u);
+                mma_sp_e4m3_pair(tbase, aj + 2, bj + 4, mcol + 2, idesc, 1u);  // +32 B of A, +64 B of B
+              }
             }
           }
           mma_commit_pair(&empty[stage], 3);
-          if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
         mma_commit_pair(accf, 3);
@@ -210,7 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------- epilogue
     const int ew = warp - EPI_WARP0;              // 0..7
     const int q = warp & 3;                       // TMEM lane quadrant this warp may access
-    const int half = ew >> 2;                     // token chunks half, half + 2, half + 4, half + 6
+    const int half = ew >> 2;                     // token chunks half, half + 2, half + 4, ...
     const int row = 32 * q + lane;                // weight row within this CTA's 128
     const int et = threadIdx.x - 32 * EPI_WARP0;  // 0..EPI_THREADS-1
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(32 * q) << 16);
@@ -223,7 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int m0 = (u / p.n_tiles) * PN;                                  // the tile's tokens
       const int n = n0 + row;
       if (et == 0) bulk_wait_read_all();  // the previous tile's stores have read the staging buffer
-      {
+      if (et < PN) {
         const int m = m0 + et;
         scl[et] = m < p.M ? __ldg(&p.sx[m >> p.gM_shift]) : 0.0f;
       }
@@ -233,9 +306,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(accf, acc_cnt & 1)) ok = false;
       if (epilogue_bar_any(!ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t v[P_COLS];  // chunk i of this warp: tokens CHUNK * (half + 2 i) + [0, CHUNK)
+      if constexpr (SIDE) {
+      // bf16 results of this thread's row, two tokens per word: chunk i covers
+      // tokens CHUNK * (half + 2 i) + [0, CHUNK)
+      uint32_t pk[C::COLS / 2];
 #pragma unroll
-      for (int i = 0; i < P_COLS / CHUNK; ++i) {
+      for (int i = 0; i < C::NCHUNK; ++i) {
+        const uint32_t col = lane_base + CHUNK * (half + 2 * i);
+        uint32_t v[CHUNK], s2[CHUNK];
+        tmem_load_n<CHUNK>(col, v);
+        tmem_load_n<CHUNK>(col + SIDE_COL, s2);
+        tmem_ld_wait();
+        const float* sc = scl + CHUNK * (half + 2 * i);
+#pragma unroll
+        for (int j = 0; j < CHUNK; j += 4) {
+          const uint2 w = scale4_pack<true>(sc + j, swr, v + j, s2 + j);
+          pk[(CHUNK * i + j) / 2] = w.x;
+          pk[(CHUNK * i + j) / 2 + 1] = w.y;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce_leader);  // the next tile's MMAs may overwrite TMEM
+      ++acc_cnt;
+      if (last) {
+        // whole tile through the idle ring: [channel half][PN tokens][64 channels] bf16
+        uint16_t* ring_row = reinterpret_cast<uint16_t*>(ring) + (row >> 6) * (PN * 64) + (row & 63);
+#pragma unroll
+        for (int i = 0; i < C::NCHUNK; ++i)
+#pragma unroll
+          for (int j = 0; j < CHUNK; j += 4)
+            st_bf16x4(ring_row + (CHUNK * (half + 2 * i) + j) * 64, 64, pk[(CHUNK * i + j) / 2],
+                      pk[(CHUNK * i + j) / 2 + 1]);
+        fence_proxy_async_smem();
+        epilogue_bar();
+        if (et == 0) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int t = 0; t < PN; t += C::OUT_TOKENS)
+              tma_store_2d(&tm_y, ring + c * (PN * 128) + t * 128, n0 + 64 * c, m0 + t);
+          bulk_commit();
+        }
+      } else {
+        // passes of OUT_TOKENS tokens through the staging buffer; in pass s
+        // every warp stores its chunk s (tokens OUT_TOKENS s + CHUNK half + [0, CHUNK))
+        uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (C::OUT_TOKENS * 64) + (row & 63);
+#pragma unroll
+        for (int s = 0; s < C::NPASS; ++s) {
+#pragma unroll
+          for (int j = 0; j < CHUNK; j += 4)
+            st_bf16x4(out_row + (CHUNK * half + j) * 64, 64, pk[(CHUNK * s + j) / 2], pk[(CHUNK * s + j) / 2 + 1]);
+          fence_proxy_async_smem();
+          epilogue_bar();
+          if (et == 0) {
+            tma_store_2d(&tm_y, out_tile, n0, m0 + C::OUT_TOKENS * s);
+            tma_store_2d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0 + C::OUT_TOKENS * s);
+            bulk_commit();
+            if (s < C::NPASS - 1) bulk_wait_read_all();
+          }
+          if (s < C::NPASS - 1) epilogue_bar();
+        }
+      }
+      } else {
+      uint32_t v[C::COLS];  // chunk i of this warp: tokens CHUNK * (half + 2 i) + [0, CHUNK)
+#pragma unroll
+      for (int i = 0; i < C::COLS / CHUNK; ++i) {
         const uint32_t col = lane_base + CHUNK * (half + 2 * i);
         tmem_ld16(col, *reinterpret_cast<uint32_t(*)[16]>(v + CHUNK * i));
         tmem_ld16(col + 16, *reinterpret_cast<uint32_t(*)[16]>(v + CHUNK * i + 16));
@@ -249,7 +385,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // whole tile through the idle ring: [channel half][256 tokens][64 channels] bf16
         uint16_t* ring_row = reinterpret_cast<uint16_t*>(ring) + (row >> 6) * (PN * 64) + (row & 63);
 #pragma unroll
-        for (int i = 0; i < P_COLS / CHUNK; ++i) {
+        for (int i = 0; i < C::COLS / CHUNK; ++i) {
           const int t0 = CHUNK * (half + 2 * i);
 #pragma unroll
           for (int j = 0; j < CHUNK; j += 4)
@@ -261,30 +397,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int t = 0; t < PN; t += P_OUT_TOKENS)
+            for (int t = 0; t < PN; t += C::OUT_TOKENS)
               tma_store_2d(&tm_y, ring + c * (PN * 128) + t * 128, n0 + 64 * c, m0 + t);
           bulk_commit();
         }
       } else {
         // four passes of 64 tokens through the staging buffer; in pass s every
         // warp converts its chunk s (tokens 64 s + 32 half + [0, 32))
-        uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (P_OUT_TOKENS * 64) + (row & 63);
+        uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (C::OUT_TOKENS * 64) + (row & 63);
 #pragma unroll
-        for (int s = 0; s < NPASS; ++s) {
-          const int t0 = P_OUT_TOKENS * s + CHUNK * half;
+        for (int s = 0; s < C::NPASS; ++s) {
+          const int t0 = C::OUT_TOKENS * s + CHUNK * half;
 #pragma unroll
           for (int j = 0; j < CHUNK; j += 4)
             scale4_store<false>(scl + t0 + j, swr, v + CHUNK * s + j, nullptr, out_row + (CHUNK * half + j) * 64, 64);
           fence_proxy_async_smem();
           epilogue_bar();
           if (et == 0) {
-            tma_store_2d(&tm_y, out_tile, n0, m0 + P_OUT_TOKENS * s);
-            tma_store_2d(&tm_y, out_tile + P_OUT_TOKENS * 128, n0 + 64, m0 + P_OUT_TOKENS * s);
+            tma_store_2d(&tm_y, out_tile, n0, m0 + C::OUT_TOKENS * s);
+            tma_store_2d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0 + C::OUT_TOKENS * s);
             bulk_commit();
-            if (s < NPASS - 1) bulk_wait_read_all();
+            if (s < C::NPASS - 1) bulk_wait_read_all();
           }
-          if (s < NPASS - 1) epilogue_bar();
+          if (s < C::NPASS - 1) epilogue_bar();
         }
+      }
       }
     }
     if (et == 0) bulk_wait_all();
@@ -302,14 +439,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
-bool pair_gemm_applies(int64_t M, int64_t N, int64_t K, bool plain) {
-  // 256-token tiles pay off from a little under one full tile; TMA row
-  // coordinates of the tiled weight views must fit in int32
-  return plain && M > 192 && N % (2 * BM) == 0 && (N / 256) * (K + BK) < (int64_t(1) << 31);
+bool pair_gemm_applies(int64_t M, int64_t N, int64_t K, bool plain, int64_t r) {
+  // 256-token tiles (240 with the side GEMM) pay off from a little under one
+  // full tile; TMA row coordinates of the tiled weight views must fit in int32
+  return plain && r <= 64 && M > 192 && N % (2 * BM) == 0 && (N / 256) * (K + BK) < (int64_t(1) << 31);
 }
 
-sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
-                             const GemmArgs& args_in, cudaStream_t stream) {
+namespace {
+
+template <int PN, bool SIDE>
+sp24_status launch_pair(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
+                        const void* X2, const void* W2, int64_t r, const GemmArgs& args_in, cudaStream_t stream) {
+  using C = PairCfg<PN, SIDE>;
   GemmArgs a = args_in;
   const int64_t M = a.M, N = a.N, K = a.K;
   a.m_tiles = static_cast<int>((M + PN - 1) / PN);
@@ -317,8 +458,9 @@ sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx,
   a.k_tiles = static_cast<int>(K / BK);
   a.splits = 1;
   a.kt_per_split = a.k_tiles;
-  CUtensorMap tm_x, tm_v, tm_m, tm_y;
-  sp24_status st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, HALF_N,
+  a.side_ksteps = SIDE ? static_cast<int>(r / 16) : 0;
+  CUtensorMap tm_x, tm_v, tm_m, tm_y, tm_w2, tm_x2;
+  sp24_status st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, C::HALF_N,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
   // tiled weight storage as 128-byte rows: a values tile is 64 rows, a metadata tile 16
   if (st == SP24_OK)
@@ -328,11 +470,22 @@ sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx,
     st = make_tmap_2d(&tm_m, a.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 128, N * K / 1024, 128, 128, KS * MROWS,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st == SP24_OK)
-    st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, P_OUT_TOKENS,
+    st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, C::OUT_TOKENS,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (SIDE) {
+    // [rows][r] bf16, boxes of 64 columns (zero fill past r), 128-byte swizzle
+    if (st == SP24_OK)
+      st = make_tmap_2d(&tm_w2, W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, N, r * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == SP24_OK)
+      st = make_tmap_2d(&tm_x2, X2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, M, r * 2, 64, C::HALF_N,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    tm_w2 = tm_x;
+    tm_x2 = tm_x;
+  }
   if (st != SP24_OK) return st;
 
-  auto kern = sp24_gemm_pair_kernel;
+  auto kern = sp24_gemm_pair_kernel<PN, SIDE>;
   static int max_pairs[64] = {};  // per device: co-resident pairs (0 = not yet known)
   const int d = dev->ordinal;
   cudaLaunchConfig_t cfg = {};
@@ -344,13 +497,13 @@ sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx,
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = P_SMEM;
+  cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (max_pairs[d] == 0) {
-    if (static_cast<size_t>(P_SMEM) > dev->smem_optin) return SP24_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM) != cudaSuccess)
+    if (static_cast<size_t>(C::SMEM) > dev->smem_optin) return SP24_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return SP24_ERR_CUDA;
     cfg.gridDim = dim3(2 * (dev->sm_count / 2), 1, 1);
     int active = 0;
@@ -361,8 +514,16 @@ sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx,
   const int pairs = units < max_pairs[d] ? units : max_pairs[d];
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, kern, tm_x, tm_v, tm_m, tm_y, a) != cudaSuccess) return SP24_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, tm_x, tm_v, tm_m, tm_y, tm_w2, tm_x2, a) != cudaSuccess) return SP24_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+}
+
+}  // namespace
+
+sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
+                             const void* X2, const void* W2, int64_t r, const GemmArgs& args, cudaStream_t stream) {
+  if (r > 0) return launch_pair<240, true>(dev, Xq, ldx, Y, ldy, X2, W2, r, args, stream);
+  return launch_pair<256, false>(dev, Xq, ldx, Y, ldy, X2, W2, 0, args, stream);
 }
 
 }  // namespace sp24

@@ -333,6 +333,16 @@ __device__ __forceinline__ void mma_sp_e4m3_pair(uint32_t d_tmem, uint64_t a_des
       "l"(a_desc), "l"(b_desc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// bf16 x bf16 -> fp32 MMA over the pair (M = 256), both operands K-major in
+// each CTA's shared memory at the descriptors' offsets.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Each CTA's shared memory at the descriptor's offset -> its own TMEM (128 lanes x 128 bits).
 __device__ __forceinline__ void tmem_cp_128x128b_pair(uint32_t taddr, uint64_t src_desc) {
   asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");

@@ -214,6 +214,18 @@ def test_pair_tiles_more_shapes(ora, sp24, M, N, K):
     _check_full(ora, sp24, w, "pair M=%d N=%d K=%d" % (M, N, K))
 
 
+@pytest.mark.parametrize("M,N,K,r", [(193, 256, 256, 64), (240, 512, 128, 16), (241, 512, 384, 32),
+                                     (481, 768, 1024, 48), (2048, 2816, 256, 64)])
+def test_pair_tiles_side_gemm(ora, sp24, M, N, K, r):
+    """The fused side GEMM on SM pairs: 240-token tiles with the main and the
+    side accumulator side by side in tensor memory, the side operands loaded
+    as the first stage of each tile.  Tails in both halves of a tile, a single
+    K block, r not a power of two, and more tiles than pairs (99 tiles:
+    pairs store one tile while the next one runs)."""
+    w = inputs.Workload("pside", M, N, K, r=r, seed=M + N + K + r)
+    _check_full(ora, sp24, w, "pair side M=%d N=%d K=%d r=%d" % (M, N, K, r))
+
+
 @pytest.mark.parametrize("gM,gN", [(128, 128), (1, 128), (128, 1)])
 def test_pair_tiles_coarse_scales(ora, sp24, gM, gN):
     w = inputs.Workload("pairg", 400, 512, 384, gM=gM, gN=gN, seed=gM + 3 * gN)
