@@ -50,7 +50,7 @@ struct Cfg {
   static constexpr int META_OFF = KS * A_STAGE;
   static constexpr int B_OFF = KS * (A_STAGE + META_STAGE);
   static constexpr int SCL_OFF = B_OFF + KS * B_SUB;
-  static constexpr int SCL_STAGE = PROMOTE ? 1024 : 0;  // per-stage scales: sx[BN] then sw[128]
+  static constexpr int SCL_STAGE = PROMOTE ? KS * 1024 : 0;  // per K block of the stage: sx[BN] then sw[128]
   static constexpr int STAGE = SCL_OFF + SCL_STAGE;
   static constexpr int LOAD_BYTES = KS * (A_STAGE + META_STAGE + B_SUB);
   static constexpr int SIDE_BYTES = SIDE ? (BM * 128 + BN * 128) : 0;
@@ -70,7 +70,7 @@ struct Cfg {
   static_assert(NACC * BN + (SIDE ? BN : 0) <= META_COL0, "TMEM columns");
   static_assert(COLS % 8 == 0, "epilogue chunking");
   static_assert(BN <= 128 || (!PROMOTE && !SIDE), "256-token tiles: plain per-tensor-K scaling only");
-  static_assert(!PROMOTE || (BN <= 128 && KS == 1), "per-stage scale slot holds one K block of BN + 128 floats");
+  static_assert(!PROMOTE || (BN <= 128 && KS <= 2), "a scale slot holds BN + 128 floats per K block");
   static_assert(!SPLIT || (!PROMOTE && !SIDE && BN <= 128), "split-K: plain per-tensor-K scaling only");
 };
 
@@ -131,12 +131,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], EPI_THREADS);
+      mbar_init(&acce[i], EPI_WARPS);  // one arrival per epilogue warp
     }
     mbar_init(sidef, 1);
     mbar_init(sidee, 1);
     mbar_init(saccf, 1);
-    mbar_init(sacce, EPI_THREADS);
+    mbar_init(sacce, EPI_WARPS);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -192,17 +192,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_2d(sA + C::B_OFF + j * C::B_SUB, &tm_x, &full[stage], (kt + j) * BK, m0);
         }
         if (PROMOTE) {
-          float* ssl = reinterpret_cast<float*>(sA + C::SCL_OFF);
-          const float* sxk = p.sx + static_cast<int64_t>(kt) * p.ldsx;
-          for (int i = lane; i < BN; i += 32) {
-            const int m = m0 + i;
-            cp_async_4(&ssl[i], sxk + ((m < p.M ? m : p.M - 1) >> p.gM_shift), m < p.M ? 4u : 0u);
-          }
-          const float* swk = p.sw + static_cast<int64_t>(kt) * p.ldsw;
-          if (p.gN_shift == 0) {
-            for (int i = lane; i < BM; i += 32) cp_async_4(&ssl[BN + i], swk + n0 + i, 4u);
-          } else if (lane == 0) {
-            cp_async_4(&ssl[BN], swk + (n0 >> p.gN_shift), 4u);
+#pragma unroll
+          for (int j = 0; j < KS; ++j) {  // the scales of each K block of the stage, in its own slot
+            float* ssl = reinterpret_cast<float*>(sA + C::SCL_OFF + j * 1024);
+            const float* sxk = p.sx + static_cast<int64_t>(kt + j) * p.ldsx;
+            for (int i = lane; i < BN; i += 32) {
+              const int m = m0 + i;
+              cp_async_4(&ssl[i], sxk + ((m < p.M ? m : p.M - 1) >> p.gM_shift), m < p.M ? 4u : 0u);
+            }
+            const float* swk = p.sw + static_cast<int64_t>(kt + j) * p.ldsw;
+            if (p.gN_shift == 0) {
+              for (int i = lane; i < BM; i += 32) cp_async_4(&ssl[BN + i], swk + n0 + i, 4u);
+            } else if (lane == 0) {
+              cp_async_4(&ssl[BN], swk + (n0 >> p.gN_shift), 4u);
+            }
           }
           cp_async_arrive(&full[stage]);
         }
@@ -254,18 +257,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           d = tbase + b * BN;
         }
-        for (int kt = t.kt0; kt < t.kt1; kt += KS) {
-          uint32_t b = 0;
-          if (PROMOTE) {
-            b = acc_cnt % NACC;
-            if (!mbar_wait(&acce[b], ((acc_cnt / NACC) & 1) ^ 1)) { ok = false; break; }
-            tc_fence_after();
-            d = tbase + b * BN;
-          }
+        for (int kt = t.kt0; kt < t.kt1 && ok; kt += KS) {
           if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
           const uint64_t off = stage * STAGE_DESC;
 #pragma unroll
           for (int j = 0; j < KS; ++j) {
+            uint32_t b = 0;
+            if (PROMOTE) {  // each K block's partial goes to its own accumulator buffer
+              b = acc_cnt % NACC;
+              if (!mbar_wait(&acce[b], ((acc_cnt / NACC) & 1) ^ 1)) { ok = false; break; }
+              tc_fence_after();
+              d = tbase + b * BN;
+            }
             const uint32_t mcol = tbase + META_COL0 + 4 * (meta_ctr & (META_SLOTS - 1));
             ++meta_ctr;
             tmem_cp_128x128b(mcol, m_desc0 + off + j * (META_STAGE >> 4));
@@ -274,12 +277,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t bj = b_desc0 + off + j * (C::B_SUB >> 4);
             mma_sp_e4m3(d, aj, bj, mcol, idesc_sp, acc0);
             mma_sp_e4m3(d, aj + 2, bj + 4, mcol + 2, idesc_sp, 1u);  // +32 B of A, +64 B of B
+            if (PROMOTE) {
+              mma_commit(&accf[b]);
+              ++acc_cnt;
+            }
           }
+          if (!ok) break;
           mma_commit(&empty[stage]);
-          if (PROMOTE) {
-            mma_commit(&accf[b]);
-            ++acc_cnt;
-          }
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -344,7 +348,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int c = 0; c < COLS; c += 16) tmem_ld16(lane_base + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
           tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(&acce[b]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
           ++acc_cnt;
           // two passes through the half-size staging buffer: tokens [0,128), then [128,256)
 #pragma unroll
@@ -383,7 +388,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int j = 0; j < CH; ++j) __stcg(wpart + (c0 + c + j) * BM + row, __uint_as_float(v[j]));
               }
               tc_fence_before();
-              mbar_arrive(&acce[b]);
+              __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
               ++acc_cnt;
               __threadfence();
               epilogue_bar();
@@ -405,7 +411,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int j = 0; j < CH; ++j) acc[c + j] = __uint_as_float(v[j]);
             }
             tc_fence_before();
-            mbar_arrive(&acce[b]);
+            __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
             ++acc_cnt;
             const float* wtile = p.ws + static_cast<int64_t>(tile_id) * p.splits * (BN * BM);
             for (int sp = 0; sp < p.splits - 1; ++sp) {
@@ -457,10 +464,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&acce[b]);
+        __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
         ++acc_cnt;
         if (SIDE) {
-          mbar_arrive(sacce);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sacce);
           ++side_cnt;
         }
       } else {
@@ -470,34 +479,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < COLS; ++i) acc[i] = 0.0f;
         const bool per_row_w = p.gN_shift == 0;  // gN = 1: weight scale varies by row
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          const uint32_t b = acc_cnt % NACC;
-          const float* ssl = reinterpret_cast<const float*>(ring + e_stage * C::STAGE + C::SCL_OFF);
-          if (ok && !mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
+        for (int kt = t.kt0; kt < t.kt1; kt += KS) {
           if (ok && !mbar_wait(&full[e_stage], e_phase)) ok = false;  // scales visible (already complete)
-          if (ok) {
-            tc_fence_after();
-            const float rowf = per_row_w ? ssl[BN + row] : ssl[BN];
 #pragma unroll
-            for (int c = 0; c < COLS; c += CH) {
-              uint32_t v[CH];
-              tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
+          for (int j = 0; j < KS; ++j) {  // K block kt + j: its partial in buffer b, its scales in slot j
+            const uint32_t b = acc_cnt % NACC;
+            const float* ssl = reinterpret_cast<const float*>(ring + e_stage * C::STAGE + C::SCL_OFF + j * 1024);
+            if (ok && !mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
+            if (ok) {
+              tc_fence_after();
+              const float rowf = per_row_w ? ssl[BN + row] : ssl[BN];
+              // all of this warp's columns of the partial in one round trip to TMEM
+              uint32_t v[COLS];
+#pragma unroll
+              for (int c = 0; c < COLS; c += CH) tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v + c);
               tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < CH; j += 4) {
-                const float4 s4 = *reinterpret_cast<const float4*>(ssl + c0 + c + j);
+              for (int i = 0; i < COLS; i += 4) {
+                const float4 s4 = *reinterpret_cast<const float4*>(ssl + c0 + i);
                 float s0 = s4.x * rowf, s1 = s4.y * rowf, s2 = s4.z * rowf, s3 = s4.w * rowf;
-                ffma2(acc[c + j], acc[c + j + 1], __uint_as_float(v[j]), __uint_as_float(v[j + 1]), s0, s1);
-                ffma2(acc[c + j + 2], acc[c + j + 3], __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), s2,
-                      s3);
+                ffma2(acc[i], acc[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s0, s1);
+                ffma2(acc[i + 2], acc[i + 3], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), s2, s3);
               }
+              tc_fence_before();
             }
-            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);  // partial folded into registers: the MMA may overwrite it
+            ++acc_cnt;
           }
-          mbar_arrive(&acce[b]);  // partial folded into registers: the MMA may overwrite it
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[e_stage]);  // this warp is done with the stage's scales
-          ++acc_cnt;
           if (++e_stage == STAGES) { e_stage = 0; e_phase ^= 1; }
         }
         if (epilogue_bar_any(!ok)) { ok = false; break; }
@@ -514,7 +525,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int j = 0; j < CH; ++j) acc[c + j] += __uint_as_float(s2[j]);
           }
           tc_fence_before();
-          mbar_arrive(sacce);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sacce);
           ++side_cnt;
         }
 #pragma unroll
@@ -564,7 +576,7 @@ sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMa
 
 // Sub-tiles per stage for a token tile: small tiles batch more K per stage.
 constexpr int ks_for(int bn, bool promote) {
-  return promote ? 1 : (bn <= 32 ? 4 : (bn <= 128 ? 2 : 1));
+  return promote ? 2 : (bn <= 32 ? 4 : (bn <= 128 ? 2 : 1));
 }
 
 template <bool PROMOTE, bool SIDE>
@@ -580,6 +592,9 @@ sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& 
           return launch<16, false, SIDE, false, 4>(dev, x, w2, x2, y, args, s);
         }
       }
+      if constexpr (PROMOTE) {
+        if (ks == 2) return launch<16, true, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
+      }
       return launch<16, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
     case 32:
       if constexpr (!PROMOTE) {
@@ -587,6 +602,9 @@ sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& 
           if constexpr (PLAIN) if (split) return launch<32, false, false, true, 4>(dev, x, w2, x2, y, args, s);
           return launch<32, false, SIDE, false, 4>(dev, x, w2, x2, y, args, s);
         }
+      }
+      if constexpr (PROMOTE) {
+        if (ks == 2) return launch<32, true, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
       }
       return launch<32, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
     case 64:
@@ -596,6 +614,9 @@ sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& 
           return launch<64, false, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
         }
       }
+      if constexpr (PROMOTE) {
+        if (ks == 2) return launch<64, true, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
+      }
       return launch<64, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
     case 256:
       if constexpr (PLAIN) return launch<256, false, false, false, 1>(dev, x, w2, x2, y, args, s);
@@ -603,6 +624,9 @@ sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& 
     default:
       if constexpr (!PROMOTE) {
         if (ks == 2) return launch<128, false, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
+      }
+      if constexpr (PROMOTE) {
+        if (ks == 2) return launch<128, true, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
       }
       return launch<128, PROMOTE, SIDE, false, 1>(dev, x, w2, x2, y, args, s);
   }
