@@ -196,7 +196,7 @@ __device__ __forceinline__ void emit_row(const uint4 (&held)[8], const uint16_t*
 }
 
 constexpr int kRowsPerCta = 8;   // gK = 128: one warp per weight row
-constexpr int kPairRowsPerCta = 4;  // gK = K: two warps per weight row
+constexpr int kPairRowsPerCta = 2;  // gK = K: two warps per weight row (128-thread CTAs: a finer last wave)
 constexpr int kHeldChunks = 8;   // per warp: 8 x 16 bytes per lane stay in registers
 
 // gN = 1.  GK128 = false: one scale per row (gK = K); two warps share a row,
@@ -385,7 +385,7 @@ extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, in
   } else {
     if (per_channel) {
       const unsigned grid = static_cast<unsigned>((N + kPairRowsPerCta - 1) / kPairRowsPerCta);
-      if (launch_pdl(compress_rows_kernel<false>, dim3(grid), dim3(256), 0, s, w, (int)N, (int)K, ldw, v, m,
+      if (launch_pdl(compress_rows_kernel<false>, dim3(grid), dim3(32 * 2 * kPairRowsPerCta), 0, s, w, (int)N, (int)K, ldw, v, m,
                      scales) != cudaSuccess)
         return SP24_ERR_CUDA;
     } else {
