@@ -486,25 +486,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t b = acc_cnt % NACC;
             const float* ssl = reinterpret_cast<const float*>(ring + e_stage * C::STAGE + C::SCL_OFF + j * 1024);
             if (ok && !mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            // all of this warp's columns of the partial in one round trip to TMEM
+            uint32_t v[COLS];
             if (ok) {
               tc_fence_after();
-              const float rowf = per_row_w ? ssl[BN + row] : ssl[BN];
-              // all of this warp's columns of the partial in one round trip to TMEM
-              uint32_t v[COLS];
 #pragma unroll
               for (int c = 0; c < COLS; c += CH) tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v + c);
               tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < COLS; i += 4) {
-                const float4 s4 = *reinterpret_cast<const float4*>(ssl + c0 + i);
-                float s0 = s4.x * rowf, s1 = s4.y * rowf, s2 = s4.z * rowf, s3 = s4.w * rowf;
-                ffma2(acc[i], acc[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s0, s1);
-                ffma2(acc[i + 2], acc[i + 3], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), s2, s3);
-              }
               tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acce[b]);  // partial folded into registers: the MMA may overwrite it
+            if (lane == 0) mbar_arrive(&acce[b]);  // the partial is in registers: the MMA may overwrite its buffer
+            if (ok) {
+              const float rowf = per_row_w ? ssl[BN + row] : ssl[BN];
+#pragma unroll
+              for (int i = 0; i < COLS; i += 4) {
+                const float4 s4 = *reinterpret_cast<const float4*>(ssl + c0 + i);
+                const float s0 = s4.x * rowf, s1 = s4.y * rowf, s2 = s4.z * rowf, s3 = s4.w * rowf;
+                ffma2(acc[i], acc[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s0, s1);
+                ffma2(acc[i + 2], acc[i + 3], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), s2, s3);
+              }
+            }
             ++acc_cnt;
           }
           __syncwarp();
