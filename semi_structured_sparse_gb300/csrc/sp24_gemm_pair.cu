@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (flat % PRODUCERS != warp) continue;
         const uint32_t stage = static_cast<uint32_t>(flat % C::STAGES);
         const uint32_t phase = static_cast<uint32_t>((flat / C::STAGES) & 1);
-        const bool got = mbar_wait(&empty[stage], phase ^ 1);
+        const bool got = mbar_wait<true>(&empty[stage], phase ^ 1);
         if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t fb = full0 + 8u * stage;
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t fmax = flat - 1;
       for (int64_t f = fmax; f >= 0 && f > fmax - C::STAGES; --f) {
         if (f % PRODUCERS != warp) continue;
-        (void)mbar_wait(&empty[f % C::STAGES], static_cast<uint32_t>((f / C::STAGES) & 1));
+        (void)mbar_wait<true>(&empty[f % C::STAGES], static_cast<uint32_t>((f / C::STAGES) & 1));
       }
     }
   } else if (warp == MMA_WARP) {
@@ -242,10 +242,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0, meta_ctr = 0, acc_cnt = 0;
       bool ok = true;
       for (int u = pair; u < num_units && ok; u += npairs) {
-        if (!mbar_wait(acce, (acc_cnt & 1) ^ 1)) { ok = false; break; }
+        if (!mbar_wait<true>(acce, (acc_cnt & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         for (int ks = SIDE ? -1 : 0; ks < k_stages; ++ks) {
-          if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
+          if (!mbar_wait<true>(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
           const uint64_t off = stage * STAGE_DESC;
           if (SIDE && ks < 0) {
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) atomicOr(p.err, DEVERR_TIMEOUT_MMA);
       mma_commit_pair(drain, 1);  // every MMA issued must finish before TMEM is freed
-      (void)mbar_wait(drain, 0);
+      (void)mbar_wait<true>(drain, 0);
     }
   } else {
     // ------------------------------------------------------------- epilogue
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // loaded before the accumulator is waited on, so that nothing is
       // outstanding when the accumulator is released (a release arrive waits)
       const float swr = __ldg(&p.sw[n >> p.gN_shift]);
-      if (!mbar_wait(accf, acc_cnt & 1)) ok = false;
+      if (!mbar_wait<true>(accf, acc_cnt & 1)) ok = false;
       if (epilogue_bar_any(!ok)) { ok = false; break; }
       tc_fence_after();
       if constexpr (SIDE) {

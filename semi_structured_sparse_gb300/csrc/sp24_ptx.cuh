@@ -50,14 +50,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait with a suspend-time hint: the thread may sleep until the phase
+// completes (or about 1 ms), instead of returning at once to poll again.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with the given parity to complete.  false = timed out.
+// The sleeping form polls the barrier far less often: in kernels whose shared
+// memory is busy with bulk copies and MMA operand reads, fewer polls leave
+// more of it to them.
+template <bool SLEEP = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() { return SLEEP ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (poll()) return true;
     if (globaltimer_ns() - t0 > SP24_WAIT_TIMEOUT_NS) return false;
   }
 }
