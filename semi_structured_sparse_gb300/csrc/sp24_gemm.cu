@@ -779,6 +779,8 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   // large token counts with plain scaling: 256 x 256 tiles on SM pairs
   if (pair_gemm_applies(M, N, K, !promote, r))
     return launch_pair_gemm(dev, Xq, ldx, Y, ldy, X2, W2, r, a, s);
+  // and with group-wise promotion: 256 x 128 tiles on SM pairs
+  if (promote && pair_promote_applies(M, N, K, r)) return launch_pair_promote(dev, Xq, ldx, Y, ldy, a, s);
 
   const int bn = pl.bn;
   CUtensorMap tm_x, tm_w2, tm_x2, tm_y;

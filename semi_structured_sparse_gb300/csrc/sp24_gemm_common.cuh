@@ -125,5 +125,11 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 bool pair_gemm_applies(int64_t M, int64_t N, int64_t K, bool plain, int64_t r);
 sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
                              const void* X2, const void* W2, int64_t r, const GemmArgs& args, cudaStream_t stream);
+// The same kernel with group-wise promotion (gK = 128): 256 weight rows x 128
+// tokens per pair tile, each K block's partial sum in one of three TMEM
+// accumulators and scaled into fp32 registers by its epilogue.
+bool pair_promote_applies(int64_t M, int64_t N, int64_t K, int64_t r);
+sp24_status launch_pair_promote(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
+                                const GemmArgs& args, cudaStream_t stream);
 
 }  // namespace sp24

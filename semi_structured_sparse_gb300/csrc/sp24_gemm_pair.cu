@@ -59,18 +59,25 @@ constexpr int MROWS = META_STAGE / 128;        // a metadata tile is 16 rows of 
 constexpr int SIDE_COL = 240;                  // first TMEM column of the side accumulator
 constexpr int SIDE_W2_BYTES = BM * 128;        // side stage: W2 tile (128 channels x 64 bf16)
 
-template <int PN_, bool SIDE_>
+template <int PN_, bool SIDE_, bool PROMOTE_ = false>
 struct PairCfg {
   static constexpr int PN = PN_;                    // tokens per pair tile (MMA N)
   static constexpr bool SIDE = SIDE_;
+  static constexpr bool PROMOTE = PROMOTE_;         // group-wise scales: one partial per K block
   static constexpr int HALF_N = PN / 2;             // activation rows each CTA loads
   static constexpr int P_B = HALF_N * BK;           // activations per CTA per K block
   static constexpr int A_OFF = 0;                   // KS values tiles (contiguous in the tiled storage)
   static constexpr int META_OFF = KS * A_STAGE;     // KS metadata tiles
   static constexpr int B_OFF = KS * (A_STAGE + META_STAGE);
-  static constexpr int STAGE = B_OFF + KS * P_B;    // bytes each CTA receives per stage
+  static constexpr int LOAD_BYTES = B_OFF + KS * P_B;  // TMA bytes each CTA receives per stage
+  // promotion: per K block of the stage a 1 KB scale slot, sx of the pair
+  // tile's PN tokens then sw of this CTA's 128 channels (cp.async)
+  static constexpr int SCL_OFF = LOAD_BYTES;
+  static constexpr int STAGE = LOAD_BYTES + (PROMOTE ? KS * 1024 : 0);
+  static constexpr int NACC = PROMOTE ? 3 : 1;      // TMEM accumulators of PN columns
   static constexpr int CHUNK = SIDE ? 24 : 32;      // token chunk: warp half h holds chunks h, h + 2, ...
-  static constexpr int OUT_TOKENS = 2 * CHUNK;      // tokens per staged store pass
+  // tokens per staged store pass (promotion stages the whole tile at once)
+  static constexpr int OUT_TOKENS = PROMOTE ? PN : 2 * CHUNK;
   static constexpr int OUT_BYTES = OUT_TOKENS * BM * 2;
   static constexpr int SCALE_BYTES = 4 * 256;
   static constexpr int FIXED = 1024 + OUT_BYTES + SCALE_BYTES + BAR_BYTES;
@@ -85,7 +92,8 @@ struct PairCfg {
   static constexpr int SIDE_X2_BYTES = HALF_N * 128;  // side stage: this CTA's X2 rows
   static_assert(B_OFF % 1024 == 0 && STAGE % 1024 == 0 && P_B % 1024 == 0, "1024-byte swizzle alignment");
   static_assert(STAGES >= 3 && STAGES <= MAX_STAGES, "pipeline depth");
-  static_assert(SIDE ? (PN <= SIDE_COL && SIDE_COL + PN <= META_BASE) : PN <= META_COL0, "TMEM columns");
+  static_assert(SIDE ? (PN <= SIDE_COL && SIDE_COL + PN <= META_BASE) : NACC * PN <= META_COL0, "TMEM columns");
+  static_assert(!PROMOTE || (!SIDE && PN + BM <= 256), "a scale slot holds PN + 128 floats");
   static_assert(NCHUNK * CHUNK == COLS && CHUNK % 8 == 0 && OUT_TOKENS * NPASS == PN, "epilogue chunks");
   static_assert(STAGES * STAGE >= PN * BM * 2, "the ring holds a whole output tile");
   static_assert(!SIDE || SIDE_W2_BYTES + SIDE_X2_BYTES <= STAGE, "the side operands fit one stage");
@@ -118,14 +126,14 @@ __device__ __forceinline__ void tmem_load_n(uint32_t taddr, uint32_t* r) {
   if constexpr (N % 16 != 0) tmem_ld8(taddr + (N / 16) * 16, r + (N / 16) * 16);
 }
 
-template <int PN, bool SIDE>
+template <int PN, bool SIDE, bool PROMOTE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sp24_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_y,
                           const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x2,
                           const GemmArgs p) {
-  using C = PairCfg<PN, SIDE>;
-  constexpr int HALF_N = C::HALF_N, CHUNK = C::CHUNK;
+  using C = PairCfg<PN, SIDE, PROMOTE>;
+  constexpr int HALF_N = C::HALF_N, CHUNK = C::CHUNK, NACC = C::NACC;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base by pointer arithmetic on the shared array, so that
   // accesses through it compile to shared-memory instructions
@@ -136,9 +144,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(out_tile + C::OUT_BYTES + C::SCALE_BYTES);
   uint64_t* full = bars;                  // [STAGES] leader: both CTAs' loads -> MMA
   uint64_t* empty = bars + MAX_STAGES;    // [STAGES] each CTA: MMA done with the stage -> its loads
-  uint64_t* accf = bars + 2 * MAX_STAGES; // each CTA: accumulator complete -> its epilogue
-  uint64_t* acce = accf + 1;              // leader: both epilogues drained the accumulator -> MMA
-  uint64_t* drain = acce + 1;             // leader: every MMA finished (before TMEM is freed)
+  uint64_t* accf = bars + 2 * MAX_STAGES; // [NACC] each CTA: accumulator complete -> its epilogue
+  uint64_t* acce = accf + 3;              // [NACC] leader: both epilogues drained the accumulator -> MMA
+  uint64_t* sfull = acce + 3;             // [STAGES] promotion, each CTA: the stage's scales landed
+  uint64_t* drain = sfull + MAX_STAGES;   // leader: every MMA finished (before TMEM is freed)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,10 +160,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      // promotion: the epilogue warps also read the stage (its scales)
+      mbar_init(&empty[i], 1 + (PROMOTE ? EPI_WARPS : 0));
+      if (PROMOTE) mbar_init(&sfull[i], 32);  // one cp.async arrival per producer lane
     }
-    mbar_init(accf, 1);
-    mbar_init(acce, 2 * EPI_WARPS);  // one arrival per epilogue warp of each CTA
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(&accf[i], 1);
+      mbar_init(&acce[i], 2 * EPI_WARPS);  // one arrival per epilogue warp of each CTA
+    }
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -207,12 +220,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // block reads the next weight tile's rows (or zero fill past the end)
             // and K coordinates past K (zero fill); the MMA skips it.
             const int kt = ks * KS;
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE);  // both CTAs' bytes
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::LOAD_BYTES);  // both CTAs' bytes
             tma_load_2d_pair(st + C::A_OFF, &tm_v, fb, 0, vrow + kt * VROWS);
             tma_load_2d_pair(st + C::META_OFF, &tm_m, fb, 0, mrow + kt * MROWS);
 #pragma unroll
             for (int j = 0; j < KS; ++j) tma_load_2d_pair(st + C::B_OFF + j * C::P_B, &tm_x, fb, (kt + j) * BK, m0);
           }
+        }
+        if constexpr (PROMOTE) {
+          // every lane: the stage's scales into this CTA's own slots (zero past M)
+          float* scs = reinterpret_cast<float*>(ring + stage * C::STAGE + C::SCL_OFF);
+          const int mt0 = (u / p.n_tiles) * PN;  // the pair tile's first token
+#pragma unroll
+          for (int j = 0; j < KS; ++j) {
+            const float* sxk = p.sx + static_cast<int64_t>(ks * KS + j) * p.ldsx;
+            const float* swk = p.sw + static_cast<int64_t>(ks * KS + j) * p.ldsw;
+            float* ssl = scs + j * 256;
+            for (int i = lane; i < PN; i += 32) {
+              const int m = mt0 + i;
+              cp_async_4(&ssl[i], sxk + ((m < p.M ? m : p.M - 1) >> p.gM_shift), m < p.M ? 4u : 0u);
+            }
+            if (p.gN_shift == 0) {
+              for (int i = lane; i < BM; i += 32) cp_async_4(&ssl[PN + i], swk + n_tile * BM + i, 4u);
+            } else if (lane == 0) {
+              cp_async_4(&ssl[PN], swk + ((n_tile * BM) >> p.gN_shift), 4u);
+            }
+          }
+          cp_async_arrive(&sfull[stage]);
         }
       }
     }
@@ -242,8 +276,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0, meta_ctr = 0, acc_cnt = 0;
       bool ok = true;
       for (int u = pair; u < num_units && ok; u += npairs) {
-        if (!mbar_wait<true>(acce, (acc_cnt & 1) ^ 1)) { ok = false; break; }
-        tc_fence_after();
+        if (!PROMOTE) {
+          if (!mbar_wait<true>(acce, (acc_cnt & 1) ^ 1)) { ok = false; break; }
+          tc_fence_after();
+        }
         for (int ks = SIDE ? -1 : 0; ks < k_stages; ++ks) {
           if (!mbar_wait<true>(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
@@ -258,22 +294,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
               if (j < nsub) {
+                // promotion: each K block's partial into its own accumulator,
+                // once both epilogues have read that accumulator's last partial
+                uint32_t d = tbase, b = 0;
+                if (PROMOTE) {
+                  b = acc_cnt % NACC;
+                  if (!mbar_wait<true>(&acce[b], ((acc_cnt / NACC) & 1) ^ 1)) { ok = false; break; }
+                  tc_fence_after();
+                  d = tbase + b * PN;
+                }
                 const uint32_t mcol = tbase + C::META_BASE + 4 * (meta_ctr & (C::META_RING - 1));
                 ++meta_ctr;
                 tmem_cp_128x128b_pair(mcol, m_desc0 + off + j * (META_STAGE >> 4));
                 const uint64_t aj = a_desc0 + off + j * (A_STAGE >> 4);
                 const uint64_t bj = b_desc0 + off + j * (C::P_B >> 4);
-                mma_sp_e4m3_pair(tbase, aj, bj, mcol, idesc, (ks != 0 || j != 0) ? 1u : 0u);
-                mma_sp_e4m3_pair(tbase, aj + 2, bj + 4, mcol + 2, idesc, 1u);  // +32 B of A, +64 B of B
+                mma_sp_e4m3_pair(d, aj, bj, mcol, idesc, (!PROMOTE && (ks != 0 || j != 0)) ? 1u : 0u);
+                mma_sp_e4m3_pair(d, aj + 2, bj + 4, mcol + 2, idesc, 1u);  // +32 B of A, +64 B of B
+                if (PROMOTE) {
+                  mma_commit_pair(&accf[b], 3);
+                  ++acc_cnt;
+                }
               }
             }
           }
+          if (!ok) break;
           mma_commit_pair(&empty[stage], 3);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        mma_commit_pair(accf, 3);
-        ++acc_cnt;
+        if (!PROMOTE) {
+          mma_commit_pair(accf, 3);
+          ++acc_cnt;
+        }
       }
       if (!ok) atomicOr(p.err, DEVERR_TIMEOUT_MMA);
       mma_commit_pair(drain, 1);  // every MMA issued must finish before TMEM is freed
@@ -288,7 +340,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int et = threadIdx.x - 32 * EPI_WARP0;  // 0..EPI_THREADS-1
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(32 * q) << 16);
     const uint32_t acce_leader = cluster_addr(acce, 0);
-    uint32_t acc_cnt = 0;
+    uint32_t acc_cnt = 0, e_stage = 0, e_phase = 0;
     bool ok = true;
     for (int u = pair; u < num_units && ok; u += npairs) {
       const bool last = u + npairs >= num_units;  // this CTA's final tile: the ring is free afterwards
@@ -296,6 +348,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int m0 = (u / p.n_tiles) * PN;                                  // the tile's tokens
       const int n = n0 + row;
       if (et == 0) bulk_wait_read_all();  // the previous tile's stores have read the staging buffer
+      if constexpr (PROMOTE) {
+        // each K block's partial, times its sx sw, is added into fp32
+        // registers: chunk i of this warp covers tokens CHUNK (half + 2 i) + [0, CHUNK)
+        float acc[C::COLS];
+#pragma unroll
+        for (int i = 0; i < C::COLS; ++i) acc[i] = 0.0f;
+        const bool per_row_w = p.gN_shift == 0;  // gN = 1: weight scale varies by row
+        for (int ks = 0; ks < k_stages; ++ks) {
+          if (ok && !mbar_wait<true>(&sfull[e_stage], e_phase)) ok = false;  // the stage's scales landed
+#pragma unroll
+          for (int j = 0; j < KS; ++j) {
+            const uint32_t b = acc_cnt % NACC;
+            const float* ssl = reinterpret_cast<const float*>(ring + e_stage * C::STAGE + C::SCL_OFF) + j * 256;
+            if (ok && !mbar_wait<true>(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            uint32_t v[C::COLS];
+            if (ok) {
+              tc_fence_after();
+#pragma unroll
+              for (int i = 0; i < C::NCHUNK; ++i)
+                tmem_load_n<CHUNK>(lane_base + b * PN + CHUNK * (half + 2 * i), v + CHUNK * i);
+              tmem_ld_wait();
+              tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader + 8u * b);  // the partial is in registers
+            if (ok) {
+              const float rowf = per_row_w ? ssl[PN + row] : ssl[PN];
+#pragma unroll
+              for (int i = 0; i < C::NCHUNK; ++i)
+#pragma unroll
+                for (int jj = 0; jj < CHUNK; jj += 4) {
+                  const float4 s4 = *reinterpret_cast<const float4*>(ssl + CHUNK * (half + 2 * i) + jj);
+                  const int c = CHUNK * i + jj;
+                  const float s0 = s4.x * rowf, s1 = s4.y * rowf, s2 = s4.z * rowf, s3 = s4.w * rowf;
+                  ffma2(acc[c], acc[c + 1], __uint_as_float(v[c]), __uint_as_float(v[c + 1]), s0, s1);
+                  ffma2(acc[c + 2], acc[c + 3], __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]), s2, s3);
+                }
+            }
+            ++acc_cnt;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[e_stage]);  // this warp is done with the stage's scales
+          if (++e_stage == C::STAGES) { e_stage = 0; e_phase ^= 1; }
+        }
+        if (epilogue_bar_any(!ok)) { ok = false; break; }
+        // the whole tile through the staging buffer: [channel half][PN tokens][64 channels] bf16
+        uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (PN * 64) + (row & 63);
+#pragma unroll
+        for (int i = 0; i < C::NCHUNK; ++i)
+#pragma unroll
+          for (int jj = 0; jj < CHUNK; jj += 4) {
+            const int c = CHUNK * i + jj;
+            st_bf16x4(out_row + (CHUNK * (half + 2 * i) + jj) * 64, 64, bf16x2_rn(acc[c], acc[c + 1]),
+                      bf16x2_rn(acc[c + 2], acc[c + 3]));
+          }
+        fence_proxy_async_smem();
+        epilogue_bar();
+        if (et == 0) {
+          tma_store_2d(&tm_y, out_tile, n0, m0);
+          tma_store_2d(&tm_y, out_tile + PN * 128, n0 + 64, m0);
+          bulk_commit();
+        }
+        continue;
+      }
       if (et < PN) {
         const int m = m0 + et;
         scl[et] = m < p.M ? __ldg(&p.sx[m >> p.gM_shift]) : 0.0f;
@@ -327,7 +444,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acce_leader);  // the next tile's MMAs may overwrite TMEM
+      if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader);  // the next tile's MMAs may overwrite TMEM
       ++acc_cnt;
       if (last) {
         // whole tile through the idle ring: [channel half][PN tokens][64 channels] bf16
@@ -379,7 +496,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acce_leader);  // the next tile's MMAs may overwrite TMEM
+      if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader);  // the next tile's MMAs may overwrite TMEM
       ++acc_cnt;
       if (last) {
         // whole tile through the idle ring: [channel half][256 tokens][64 channels] bf16
@@ -445,12 +562,17 @@ bool pair_gemm_applies(int64_t M, int64_t N, int64_t K, bool plain, int64_t r) {
   return plain && r <= 64 && M > 192 && N % (2 * BM) == 0 && (N / 256) * (K + BK) < (int64_t(1) << 31);
 }
 
+bool pair_promote_applies(int64_t M, int64_t N, int64_t K, int64_t r) {
+  // 128-token pair tiles with a partial per K block; stages hold whole pairs of K blocks
+  return r == 0 && M > 64 && N % (2 * BM) == 0 && (K / BK) % KS == 0 && (N / 256) * (K + BK) < (int64_t(1) << 31);
+}
+
 namespace {
 
-template <int PN, bool SIDE>
+template <int PN, bool SIDE, bool PROMOTE>
 sp24_status launch_pair(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
                         const void* X2, const void* W2, int64_t r, const GemmArgs& args_in, cudaStream_t stream) {
-  using C = PairCfg<PN, SIDE>;
+  using C = PairCfg<PN, SIDE, PROMOTE>;
   GemmArgs a = args_in;
   const int64_t M = a.M, N = a.N, K = a.K;
   a.m_tiles = static_cast<int>((M + PN - 1) / PN);
@@ -485,7 +607,7 @@ sp24_status launch_pair(const DeviceInfo* dev, const void* Xq, int64_t ldx, cons
   }
   if (st != SP24_OK) return st;
 
-  auto kern = sp24_gemm_pair_kernel<PN, SIDE>;
+  auto kern = sp24_gemm_pair_kernel<PN, SIDE, PROMOTE>;
   static int max_pairs[64] = {};  // per device: co-resident pairs (0 = not yet known)
   const int d = dev->ordinal;
   cudaLaunchConfig_t cfg = {};
@@ -522,8 +644,13 @@ sp24_status launch_pair(const DeviceInfo* dev, const void* Xq, int64_t ldx, cons
 
 sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
                              const void* X2, const void* W2, int64_t r, const GemmArgs& args, cudaStream_t stream) {
-  if (r > 0) return launch_pair<240, true>(dev, Xq, ldx, Y, ldy, X2, W2, r, args, stream);
-  return launch_pair<256, false>(dev, Xq, ldx, Y, ldy, X2, W2, 0, args, stream);
+  if (r > 0) return launch_pair<240, true, false>(dev, Xq, ldx, Y, ldy, X2, W2, r, args, stream);
+  return launch_pair<256, false, false>(dev, Xq, ldx, Y, ldy, X2, W2, 0, args, stream);
+}
+
+sp24_status launch_pair_promote(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
+                                const GemmArgs& args, cudaStream_t stream) {
+  return launch_pair<128, false, true>(dev, Xq, ldx, Y, ldy, nullptr, nullptr, 0, args, stream);
 }
 
 }  // namespace sp24

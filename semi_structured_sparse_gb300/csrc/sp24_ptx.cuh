@@ -318,6 +318,13 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
+// The same arrival without release semantics.  Enough where all that the
+// arrival has to order has already completed in this thread (such as TMEM
+// reads after tcgen05.wait::ld): a cluster-scope release costs on the order
+// of a thousand cycles before the arrival lands.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
 // TMA 2D load into this CTA's shared memory, with its transaction bytes
 // signalled on the mbarrier at `bar_cluster`, which may be in the pair peer.
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int x,

@@ -226,6 +226,27 @@ def test_pair_tiles_side_gemm(ora, sp24, M, N, K, r):
     _check_full(ora, sp24, w, "pair side M=%d N=%d K=%d r=%d" % (M, N, K, r))
 
 
+@pytest.mark.parametrize("gM,gN", [(1, 128), (1, 1), (128, 128), (128, 1)])
+@pytest.mark.parametrize("M,N,K", [(65, 256, 256), (130, 512, 768), (300, 768, 1024), (2000, 1536, 512)])
+def test_pair_tiles_groupwise(ora, sp24, gM, gN, M, N, K):
+    """Group-wise promotion (gK = 128) on SM pairs: 256 x 128 tiles, each K
+    block's partial in one of three tensor-memory accumulators, scaled by its
+    own sx sw into fp32 registers.  Per-channel and 128-row block weight
+    scales, per-token and 128-token block activation scales, token tails in
+    either SM's half of a tile, a single stage, four stages per tile
+    (K = 1024), and more tiles than pairs (2000 x 1536: 16 token tiles x 6
+    weight-row tiles = 96)."""
+    w = inputs.Workload("pairgw", M, N, K, gM=gM, gN=gN, gK=128, seed=M + N + K + gM + 3 * gN)
+    _check_full(ora, sp24, w, "pair group-wise g=(%d,%d) M=%d N=%d K=%d" % (gM, gN, M, N, K))
+
+
+def test_groupwise_odd_k_blocks_falls_back(ora, sp24):
+    """An odd number of 128-wide K blocks does not fill the pair kernel's
+    two-block stages: such calls run on the one-CTA kernel, with the same result."""
+    w = inputs.Workload("gwodd", 300, 512, 384, gN=128, gK=128, seed=11)
+    _check_full(ora, sp24, w, "group-wise odd K blocks")
+
+
 @pytest.mark.parametrize("gM,gN", [(128, 128), (1, 128), (128, 1)])
 def test_pair_tiles_coarse_scales(ora, sp24, gM, gN):
     w = inputs.Workload("pairg", 400, 512, 384, gM=gM, gN=gN, seed=gM + 3 * gN)
