@@ -503,9 +503,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int i = 0; i < COLS; i += 4) {
                 const float4 s4 = *reinterpret_cast<const float4*>(ssl + c0 + i);
-                const float s0 = s4.x * rowf, s1 = s4.y * rowf, s2 = s4.z * rowf, s3 = s4.w * rowf;
-                ffma2(acc[i], acc[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s0, s1);
-                ffma2(acc[i + 2], acc[i + 3], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), s2, s3);
+                const float2 s01 = __fmul2_rn(make_float2(s4.x, s4.y), make_float2(rowf, rowf));
+                const float2 s23 = __fmul2_rn(make_float2(s4.z, s4.w), make_float2(rowf, rowf));
+                ffma2(acc[i], acc[i + 1], __uint_as_float(v[i]), __uint_as_float(v[i + 1]), s01.x, s01.y);
+                ffma2(acc[i + 2], acc[i + 3], __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), s23.x, s23.y);
               }
             }
             ++acc_cnt;

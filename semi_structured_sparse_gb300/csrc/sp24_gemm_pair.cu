@@ -356,12 +356,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < C::COLS; ++i) acc[i] = 0.0f;
         const bool per_row_w = p.gN_shift == 0;  // gN = 1: weight scale varies by row
         for (int ks = 0; ks < k_stages; ++ks) {
-          if (ok && !mbar_wait<true>(&sfull[e_stage], e_phase)) ok = false;  // the stage's scales landed
+          // polls (a sleeping wait wakes later, and this warp is the pipeline's slowest stage)
+          if (ok && !mbar_wait<false>(&sfull[e_stage], e_phase)) ok = false;  // the stage's scales landed
 #pragma unroll
           for (int j = 0; j < KS; ++j) {
             const uint32_t b = acc_cnt % NACC;
             const float* ssl = reinterpret_cast<const float*>(ring + e_stage * C::STAGE + C::SCL_OFF) + j * 256;
-            if (ok && !mbar_wait<true>(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
+            if (ok && !mbar_wait<false>(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
             ok = __all_sync(0xFFFFFFFFu, ok);
             uint32_t v[C::COLS];
             if (ok) {
@@ -382,9 +383,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int jj = 0; jj < CHUNK; jj += 4) {
                   const float4 s4 = *reinterpret_cast<const float4*>(ssl + CHUNK * (half + 2 * i) + jj);
                   const int c = CHUNK * i + jj;
-                  const float s0 = s4.x * rowf, s1 = s4.y * rowf, s2 = s4.z * rowf, s3 = s4.w * rowf;
-                  ffma2(acc[c], acc[c + 1], __uint_as_float(v[c]), __uint_as_float(v[c + 1]), s0, s1);
-                  ffma2(acc[c + 2], acc[c + 3], __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]), s2, s3);
+                  const float2 s01 = __fmul2_rn(make_float2(s4.x, s4.y), make_float2(rowf, rowf));
+                  const float2 s23 = __fmul2_rn(make_float2(s4.z, s4.w), make_float2(rowf, rowf));
+                  ffma2(acc[c], acc[c + 1], __uint_as_float(v[c]), __uint_as_float(v[c + 1]), s01.x, s01.y);
+                  ffma2(acc[c + 2], acc[c + 3], __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]), s23.x, s23.y);
                 }
             }
             ++acc_cnt;

@@ -383,14 +383,12 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
 }
 
 // Packed fp32 pair FMA (one instruction for two lanes of work):
-// (a0, a1) = (x0 * s0 + a0, x1 * s1 + a1), each rounded to nearest.
+// (a0, a1) = (x0 * s0 + a0, x1 * s1 + a1), each rounded to nearest.  Written
+// with the float2 builtin, so that the compiler pairs the registers itself.
 __device__ __forceinline__ void ffma2(float& a0, float& a1, float x0, float x1, float s0, float s1) {
-  uint64_t acc, x, sc;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(sc) : "f"(s0), "f"(s1));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(x), "l"(sc));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+  const float2 r = __ffma2_rn(make_float2(x0, x1), make_float2(s0, s1), make_float2(a0, a1));
+  a0 = r.x;
+  a1 = r.y;
 }
 
 }  // namespace sp24
