@@ -48,17 +48,17 @@ DESCR = {
 # capture of the current kernel build (summaries and commands under profiles/).
 # An entry is removed when its kernel changes; absent entries report null.
 CAPTURED_TRAFFIC = {
-    # sp24_gemm_pair_kernel<256,0> on the Llama-style linear (M 2048, N 4096, K 4096)
-    ("llama", 2048, "gemm"): 18941184 + 1024,
+    # sp24_gemm_pair_kernel<256,0,0> on the Llama-style linear (M 2048, N 4096, K 4096)
+    ("llama", 2048, "gemm"): 18941184 + 0,
     # compress_rows_kernel<0> on W[4096, 4096] (Llama-style linear), two rows per CTA
     ("llama", 2048, "compress"): 33597696 + 9728,
     # compress_rows_kernel<0> on W[28672, 4096] (decode workload), two rows per CTA
     ("decode", 16, "compress"): 234962688 + 19037184,
     # sp24_gemm_kernel<16,0,0,0,4>, decode M 16, N 28672, K 4096
     ("decode", 16, "gemm"): 73601792 + 572928,
-    # sp24_gemm_kernel<128,1,0,0,2>, group-wise M 3000, N 14336, K 4096
-    ("groupwise", 3000, "gemm"): 50543616 + 57381376,
-    # sp24_gemm_pair_kernel<240,1>, fused side GEMM M 2048, N 4096, K 4096, r 64
+    # sp24_gemm_pair_kernel<128,0,1>, group-wise M 3000, N 14336, K 4096
+    ("groupwise", 3000, "gemm"): 50562304 + 57765632,
+    # sp24_gemm_pair_kernel<240,1,0>, fused side GEMM M 2048, N 4096, K 4096, r 64
     ("fused", 2048, "gemm"): 19724288 + 0,
 }
 
@@ -318,7 +318,9 @@ def run_ours(args):
     gemm_tflops_alg = alg_flops / (t_gemm * 1e-3) / 1e12
     comp_gbs = comp_bytes / (t_comp * 1e-3) / 1e9
     gemm_tflops_dense = 2 * gemm_tflops_alg
-    pair = w.gk == w.K and w.r <= 64 and w.M > 192 and w.N % 256 == 0  # the library's SM-pair rule
+    # the library's SM-pair rules: plain scaling above 192 tokens, group-wise above 64 with whole stages
+    pair = (w.gk == w.K and w.r <= 64 and w.M > 192 and w.N % 256 == 0) or \
+        (w.gk == 128 and w.K > 128 and w.r == 0 and w.M > 64 and w.N % 256 == 0 and (w.K // 128) % 2 == 0)
     gemm_kernel = "sp24_gemm_pair_kernel" if pair else "sp24_gemm_kernel"
     if t_gemm >= t_comp:
         roofline = {"kernel": gemm_kernel, "bound": "tensor", "achieved": round(gemm_tflops_alg, 1),
