@@ -120,7 +120,7 @@ SP24_API sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K,
  * fused bf16 side GEMM:
  *
  *   Y[m][n] = bf16( sum_kb sx[kb][m/gM] * sw[kb][n/gN] * P_kb[m][n]
- *                   + sum_{j<r} X2[m][j] * W2[n][j] )
+ *                   + sum_{j<r} X2[m][j] * W2[n][j] + bias[n] )
  *   P_kb[m][n] = sum over k in K block kb of xq[m][k] * wq[n][k]  (fp32)
  *
  * where wq is the dense weight that (values, meta) encode.  Internally the
@@ -131,6 +131,9 @@ SP24_API sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K,
  * tile).  Token rows beyond M in the last tile are computed on zero fill and
  * not stored ([2095], predication of partial tiles).  The side GEMM is the
  * small w16a16 term of [2058] (hyx1999: Y = X1 W1^T + X2 W2^T in one kernel).
+ * The bias is that of the linear operation in [3258]
+ * (_linear_fp8_act_fp8_weight_sparse_cutlass_impl(input, weight, bias)),
+ * added in fp32 before the one rounding to bf16.
  *
  *   Xq      (device) uint8 e4m3 [M][K], row stride ldx (ldx % 16 == 0).
  *   sx      (device) fp32 [K/gK][ceil(M/gM)].
@@ -140,6 +143,7 @@ SP24_API sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K,
  *   gN      1 or 128; gK: K or 128.
  *   X2, W2  (device) bf16 [M][r] and [N][r] (row stride r), or NULL with
  *           r = 0 for no side GEMM; r a multiple of 16, at most 64.
+ *   bias    (device) bf16 [N], 2-byte aligned, or NULL for none.
  *   Y       (device, out) bf16 [M][N], row stride ldy >= N, ldy % 8 == 0,
  *           16-byte aligned.
  *   workspace, workspace_bytes: device scratch of at least
@@ -156,8 +160,8 @@ SP24_API sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K,
  */
 SP24_API sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
                           const void* values, const void* meta, const float* sw, int64_t N, int gN, int gK,
-                          const void* X2, const void* W2, int64_t r, void* Y, int64_t ldy, void* workspace,
-                          size_t workspace_bytes, void* stream);
+                          const void* X2, const void* W2, int64_t r, const void* bias, void* Y, int64_t ldy,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * sp24_fp8_gemm_fixed_scratch -- sp24_fp8_gemm for callers that may not
@@ -185,7 +189,7 @@ SP24_API sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, i
 SP24_API sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
                                                  int gM, const void* values, const void* meta, const float* sw,
                                                  int64_t N, int gN, int gK, const void* X2, const void* W2, int64_t r,
-                                                 void* Y, int64_t ldy, void* stream);
+                                                 const void* bias, void* Y, int64_t ldy, void* stream);
 
 /* Device scratch bytes sp24_fp8_gemm needs for this problem (0 = none). */
 SP24_API size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r);

@@ -37,7 +37,7 @@ def lib():
         L.ora_decompress.argtypes = [P, P, I64, I64, P]
         L.ora_quantize_act.argtypes = [P, I64, I64, I64, I, P, P]
         L.ora_gemm.argtypes = [P, P, I64, I64, I64, I, P, P, P, I64, I, I,
-                               P, P, I64, I, P]
+                               P, P, I64, P, I, P]
         for f in ("ora_tile_values", "ora_untile_values", "ora_tile_meta", "ora_untile_meta"):
             getattr(L, f).argtypes = [P, I64, I64, P]
         L.ora_num_threads.restype = ctypes.c_int
@@ -188,11 +188,12 @@ def quantize_act(X, gK: int = None):
 
 # ---------------------------------------------------------------------- GEMM
 def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None,
-         X2=None, W2=None, acc_fp64: bool = False) -> np.ndarray:
-    """Group-wise scaled 2:4 sparse GEMM Y[M,N] = X.W^T (+ X2.W2^T), as float64.
+         X2=None, W2=None, acc_fp64: bool = False, bias=None) -> np.ndarray:
+    """Group-wise scaled 2:4 sparse GEMM Y[M,N] = X.W^T (+ X2.W2^T) (+ bias), as float64.
 
     xq [M,K] e4m3; sx [K/gK, ceil(M/gM)]; values [N,K/2]; meta [N,K/8] logical;
-    sw [K/gK, ceil(N/gN)]; X2 [M,r], W2 [N,r] bf16 bits or None.
+    sw [K/gK, ceil(N/gN)]; X2 [M,r], W2 [N,r] bf16 bits or None; bias [N] bf16
+    bits or None (the linear operation's bias, pytorch/ao PR #3258, added last).
     acc_fp64=False accumulates in fp32 (the reference the path is held to);
     True accumulates in double (used to bound the fp32 reference's own error).
     """
@@ -212,9 +213,12 @@ def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None,
         W2 = _c(W2, np.uint16)
         r = X2.shape[1]
         assert X2.shape == (M, r) and W2.shape == (N, r)
+    if bias is not None:
+        bias = _c(bias, np.uint16)
+        assert bias.shape == (N,)
     Y = np.empty((M, N), dtype=np.float64)
     lib().ora_gemm(_p(xq), _p(sx), M, K, K, gM, _p(values), _p(meta), _p(sw), N, gN, gK,
-                   _p(X2), _p(W2), r, 1 if acc_fp64 else 0, _p(Y))
+                   _p(X2), _p(W2), r, _p(bias), 1 if acc_fp64 else 0, _p(Y))
     return Y
 
 

@@ -323,16 +323,20 @@ void ora_quantize_act(const float *X, int64_t M, int64_t K, int64_t ldx, int gK,
  *       P  = sum over kept k in the block, k ascending, of wq[n][k] * xq[m][k]
  *       acc = acc + (sx[kb][m/gM] * sw[kb][n/gN]) * P
  *   acc = acc + sum_{j<r} X2[m][j] * W2[n][j]          (bf16 side GEMM)
+ *   acc = acc + bias[n]                                (bf16 bias, if any)
+ * The bias is that of the linear operation of pytorch/ao PR #3258
+ * (input, weight, bias), added last, before the output is rounded.
  * Only kept weights are multiplied (the sparse loop); wq comes from values
  * and the metadata nibbles.  Every product of two e4m3 values, and of two
  * bf16 values, is exact in fp32.  acc_fp64 = 0 accumulates in fp32 (each
  * operation rounded, as written above); 1 accumulates in double.
  * Layouts: xq [M][K] row stride ldx; sx [K/gK][ceil(M/gM)]; values [N][K/2];
- * meta [N][K/8]; sw [K/gK][ceil(N/gN)]; X2 [M][r]; W2 [N][r]; Y [M][N]. */
+ * meta [N][K/8]; sw [K/gK][ceil(N/gN)]; X2 [M][r]; W2 [N][r]; bias [N] or
+ * NULL; Y [M][N]. */
 void ora_gemm(const uint8_t *xq, const float *sx, int64_t M, int64_t K, int64_t ldx, int gM,
               const uint8_t *values, const uint8_t *meta, const float *sw, int64_t N,
               int gN, int gK, const uint16_t *X2, const uint16_t *W2, int64_t r,
-              int acc_fp64, double *Y)
+              const uint16_t *bias, int acc_fp64, double *Y)
 {
     int64_t ldsx = (M + gM - 1) / gM, ldsw = (N + gN - 1) / gN, kB = K / gK;
     double dec[256];
@@ -367,6 +371,10 @@ void ora_gemm(const uint8_t *xq, const float *sx, int64_t M, int64_t K, int64_t 
             for (j = 0; j < r; ++j) {
                 double p = (double)ora_bf16_to_f32(X2[m * r + j]) * (double)ora_bf16_to_f32(W2[n * r + j]);
                 if (acc_fp64) accd += p; else accf += (float)p;
+            }
+            if (bias) {
+                float b = ora_bf16_to_f32(bias[n]);
+                if (acc_fp64) accd += (double)b; else accf += b;
             }
             Y[m * N + n] = acc_fp64 ? accd : (double)accf;
         }

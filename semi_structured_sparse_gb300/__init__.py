@@ -31,11 +31,11 @@ SIGNATURES = {
     "sp24_meta_bytes": ([_I64, _I64], _SZ),
     "sp24_fp8_compress": ([_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P], _I),
     "sp24_fp8_quantize_act": ([_P, _I64, _I64, _I64, _I, _P, _P, _P], _I),
-    "sp24_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _I64,
+    "sp24_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P, _I64,
                        _P, _SZ, _P], _I),
     "sp24_fp8_gemm_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
-    "sp24_fp8_gemm_fixed_scratch": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _I64,
-                                     _P], _I),
+    "sp24_fp8_gemm_fixed_scratch": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P,
+                                     _I64, _P], _I),
     "sp24_last_device_error": ([_P], _I),
 }
 
@@ -143,9 +143,10 @@ def quantize_act(x: torch.Tensor, gK: int = None, out=None, stream=None):
 
 
 def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None, x2=None, w2=None,
-         out=None, workspace=None, stream=None):
+         out=None, workspace=None, stream=None, bias=None):
     """Y[M, N] (bf16) = scaled 2:4 sparse e4m3 GEMM of xq [M, K] with the packed weight
-    (values [N, K/2], meta [N, K/8]) plus x2 [M, r] . w2 [N, r]^T when given."""
+    (values [N, K/2], meta [N, K/8]) plus x2 [M, r] . w2 [N, r]^T and a bf16 bias [N]
+    when given."""
     lib = load()
     _dev_tensor(xq, torch.uint8, "xq")
     _dev_tensor(values, torch.uint8, "values")
@@ -164,12 +165,16 @@ def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None, x2=
             raise ValueError("x2 and w2 must be contiguous")
     if not (sx.is_contiguous() and sw.is_contiguous() and values.is_contiguous() and meta.is_contiguous()):
         raise ValueError("scales, values and meta must be contiguous")
+    if bias is not None:
+        _dev_tensor(bias, torch.bfloat16, "bias")
+        if not bias.is_contiguous() or bias.numel() != N:
+            raise ValueError("bias must be a contiguous bf16 vector of N values")
     y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if out is None else out
     ws_bytes = int(lib.sp24_fp8_gemm_workspace_size(M, N, K, r))
     if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=xq.device)
     _check(lib.sp24_fp8_gemm(_ptr(xq), _ptr(sx), M, K, xq.stride(0), gM, _ptr(values), _ptr(meta), _ptr(sw), N,
-                             gN, gK, _ptr(x2), _ptr(w2), r, _ptr(y), y.stride(0), _ptr(workspace),
+                             gN, gK, _ptr(x2), _ptr(w2), r, _ptr(bias), _ptr(y), y.stride(0), _ptr(workspace),
                              0 if workspace is None else workspace.numel() * workspace.element_size(),
                              _stream(stream)), "sp24_fp8_gemm")
     return y

@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (epilogue_bar_any(!ok)) { ok = false; break; }
         tc_fence_after();
         const float swr = __ldg(&p.sw[n >> p.gN_shift]);
+        const float bn = bias_of(p, n);
         if constexpr (BN > 128) {
           // one accumulator: copy this warp's 128 columns to registers and free
           // TMEM at once, so the next tile's MMAs overlap the rest of the epilogue
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (half == pass) {
 #pragma unroll
               for (int j = 0; j < COLS; j += 4)
-                scale4_store<false>(scl + c0 + j, swr, v + j, nullptr, out_row + j * 64, 64);
+                scale4_store<false>(scl + c0 + j, swr, v + j, nullptr, bn, out_row + j * 64, 64);
             }
             fence_proxy_async_smem();
             epilogue_bar();
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int c = 0; c < COLS; c += 4) {
               const uint32_t a4[4] = {__float_as_uint(acc[c]), __float_as_uint(acc[c + 1]), __float_as_uint(acc[c + 2]),
                                       __float_as_uint(acc[c + 3])};
-              scale4_store<false>(scl + c0 + c, swr, a4, nullptr, out_row + (c0 + c) * 64, 64);
+              scale4_store<false>(scl + c0 + c, swr, a4, nullptr, bn, out_row + (c0 + c) * 64, 64);
             }
             fence_proxy_async_smem();
             epilogue_bar();
@@ -455,12 +456,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < CH; j += 4)
-              scale4_store<true>(scl + c0 + c + j, swr, v + j, s2 + j, out_row + (c0 + c + j) * 64, 64);
+              scale4_store<true>(scl + c0 + c + j, swr, v + j, s2 + j, bn, out_row + (c0 + c + j) * 64, 64);
           } else {
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < CH; j += 4)
-              scale4_store<false>(scl + c0 + c + j, swr, v + j, nullptr, out_row + (c0 + c + j) * 64, 64);
+              scale4_store<false>(scl + c0 + c + j, swr, v + j, nullptr, bn, out_row + (c0 + c + j) * 64, 64);
           }
         }
         tc_fence_before();
@@ -533,9 +534,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane == 0) mbar_arrive(sacce);
           ++side_cnt;
         }
+        const float bn = bias_of(p, n);
 #pragma unroll
         for (int j = 0; j < COLS; j += 4)
-          st_bf16x4(out_row + (c0 + j) * 64, 64, bf16x2_rn(acc[j], acc[j + 1]), bf16x2_rn(acc[j + 2], acc[j + 3]));
+          st_bf16x4(out_row + (c0 + j) * 64, 64, bf16x2_rn(acc[j] + bn, acc[j + 1] + bn),
+                    bf16x2_rn(acc[j + 2] + bn, acc[j + 3] + bn));
       }
       // hand the staged tile to the TMA engine: rows past M are clipped by it
       fence_proxy_async_smem();
@@ -726,8 +729,8 @@ extern "C" size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, 
 
 extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
                                      const void* values, const void* meta, const float* sw, int64_t N, int gN,
-                                     int gK, const void* X2, const void* W2, int64_t r, void* Y, int64_t ldy,
-                                     void* workspace, size_t workspace_bytes, void* stream) {
+                                     int gK, const void* X2, const void* W2, int64_t r, const void* bias, void* Y,
+                                     int64_t ldy, void* workspace, size_t workspace_bytes, void* stream) {
   using namespace sp24;
   if (!Xq || !sx || !values || !meta || !sw || !Y) return SP24_ERR_INVALID_ARG;
   if (M < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0) return SP24_ERR_INVALID_ARG;
@@ -744,6 +747,7 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   if (!aligned16(Xq) || !aligned16(values) || !aligned16(meta) || ldx % 16 != 0) return SP24_ERR_ALIGNMENT;
   if ((reinterpret_cast<uintptr_t>(sx) | reinterpret_cast<uintptr_t>(sw)) % 4 != 0) return SP24_ERR_ALIGNMENT;
   if (!aligned16(Y) || ldy % 8 != 0) return SP24_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(bias) % 2 != 0) return SP24_ERR_ALIGNMENT;
   const DeviceInfo* dev = nullptr;
   sp24_status st = current_device(&dev);
   if (st != SP24_OK) return st;
@@ -758,6 +762,7 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   a.meta = static_cast<const uint8_t*>(meta);
   a.sx = sx;
   a.sw = sw;
+  a.bias = static_cast<const uint16_t*>(bias);
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
@@ -858,7 +863,7 @@ sp24_status fixed_scratch_address(void** out) {
 extern "C" sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
                                                    int gM, const void* values, const void* meta, const float* sw,
                                                    int64_t N, int gN, int gK, const void* X2, const void* W2,
-                                                   int64_t r, void* Y, int64_t ldy, void* stream) {
+                                                   int64_t r, const void* bias, void* Y, int64_t ldy, void* stream) {
   using namespace sp24;
   // scratch this shape needs (split-K partials and their flags); more than the
   // fixed array holds is refused rather than silently run another way
@@ -867,6 +872,6 @@ extern "C" sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* 
   const sp24_status st = fixed_scratch_address(&scratch);
   if (st != SP24_OK) return st;
   // Nothing in the scratch needs clearing: split flags carry a per-launch epoch.
-  return sp24_fp8_gemm(Xq, sx, M, K, ldx, gM, values, meta, sw, N, gN, gK, X2, W2, r, Y, ldy, scratch,
+  return sp24_fp8_gemm(Xq, sx, M, K, ldx, gM, values, meta, sw, N, gN, gK, X2, W2, r, bias, Y, ldy, scratch,
                        kFixedScratchBytes, stream);
 }

@@ -16,6 +16,7 @@ struct GemmArgs {
   const uint8_t* meta;    // tiled metadata
   const float* sx;
   const float* sw;
+  const uint16_t* bias;  // bf16 [N] added to every output row, or null
   int M, N, K;
   int ldsx, ldsw;          // row strides (floats) of the scale tensors
   int gM_shift, gN_shift;  // log2 of the granularities (0 or 7)
@@ -76,21 +77,23 @@ __device__ __forceinline__ void st_bf16x4(uint16_t* dst, int stride, uint32_t lo
   dst[2 * stride] = static_cast<uint16_t>(hi & 0xFFFFu);
   dst[3 * stride] = static_cast<uint16_t>(hi >> 16);
 }
-// bf16((s_t sw) acc_t + add_t) for 4 consecutive tokens t; s points at their
-// 4 scales (16-byte aligned shared memory, the same address in every lane).
+// The bias of output channel n as fp32, or -0.0 without a bias: adding -0.0
+// (or folding it into an FMA) leaves every value, the sign of zero included,
+// exactly as it was.
+__device__ __forceinline__ float bias_of(const GemmArgs& p, int n) {
+  return p.bias ? __uint_as_float(static_cast<uint32_t>(__ldg(&p.bias[n])) << 16) : -0.0f;
+}
+// bf16((s_t sw) acc_t + add_t + bias) for 4 consecutive tokens t; s points at
+// their 4 scales (16-byte aligned shared memory, the same address in every lane).
 template <bool ADD>
 __device__ __forceinline__ void scale4_store(const float* s, float sw, const uint32_t* acc, const uint32_t* add,
-                                             uint16_t* dst, int stride) {
+                                             float bias, uint16_t* dst, int stride) {
   const float4 s4 = *reinterpret_cast<const float4*>(s);
-  float y[4] = {(s4.x * sw) * __uint_as_float(acc[0]), (s4.y * sw) * __uint_as_float(acc[1]),
-                (s4.z * sw) * __uint_as_float(acc[2]), (s4.w * sw) * __uint_as_float(acc[3])};
-  if constexpr (ADD) {
-    y[0] = fmaf(s4.x * sw, __uint_as_float(acc[0]), __uint_as_float(add[0]));
-    y[1] = fmaf(s4.y * sw, __uint_as_float(acc[1]), __uint_as_float(add[1]));
-    y[2] = fmaf(s4.z * sw, __uint_as_float(acc[2]), __uint_as_float(add[2]));
-    y[3] = fmaf(s4.w * sw, __uint_as_float(acc[3]), __uint_as_float(add[3]));
-  }
-  st_bf16x4(dst, stride, bf16x2_rn(y[0], y[1]), bf16x2_rn(y[2], y[3]));
+  const float a0 = ADD ? __uint_as_float(add[0]) + bias : bias, a1 = ADD ? __uint_as_float(add[1]) + bias : bias;
+  const float a2 = ADD ? __uint_as_float(add[2]) + bias : bias, a3 = ADD ? __uint_as_float(add[3]) + bias : bias;
+  const float y0 = fmaf(s4.x * sw, __uint_as_float(acc[0]), a0), y1 = fmaf(s4.y * sw, __uint_as_float(acc[1]), a1);
+  const float y2 = fmaf(s4.z * sw, __uint_as_float(acc[2]), a2), y3 = fmaf(s4.w * sw, __uint_as_float(acc[3]), a3);
+  st_bf16x4(dst, stride, bf16x2_rn(y0, y1), bf16x2_rn(y2, y3));
 }
 
 // Loads `N8 * 8` consecutive accumulator columns of this warp's lanes.

@@ -99,22 +99,15 @@ struct PairCfg {
   static_assert(!SIDE || SIDE_W2_BYTES + SIDE_X2_BYTES <= STAGE, "the side operands fit one stage");
 };
 
-// bf16((s_t sw) acc_t [+ add_t]) of 4 consecutive tokens, as two packed words.
+// bf16((s_t sw) acc_t [+ add_t] + bias) of 4 consecutive tokens, as two packed words.
 template <bool ADD>
-__device__ __forceinline__ uint2 scale4_pack(const float* s, float sw, const uint32_t* acc, const uint32_t* add) {
+__device__ __forceinline__ uint2 scale4_pack(const float* s, float sw, const uint32_t* acc, const uint32_t* add,
+                                             float bias) {
   const float4 s4 = *reinterpret_cast<const float4*>(s);
-  float y0, y1, y2, y3;
-  if constexpr (ADD) {
-    y0 = fmaf(s4.x * sw, __uint_as_float(acc[0]), __uint_as_float(add[0]));
-    y1 = fmaf(s4.y * sw, __uint_as_float(acc[1]), __uint_as_float(add[1]));
-    y2 = fmaf(s4.z * sw, __uint_as_float(acc[2]), __uint_as_float(add[2]));
-    y3 = fmaf(s4.w * sw, __uint_as_float(acc[3]), __uint_as_float(add[3]));
-  } else {
-    y0 = (s4.x * sw) * __uint_as_float(acc[0]);
-    y1 = (s4.y * sw) * __uint_as_float(acc[1]);
-    y2 = (s4.z * sw) * __uint_as_float(acc[2]);
-    y3 = (s4.w * sw) * __uint_as_float(acc[3]);
-  }
+  const float a0 = ADD ? __uint_as_float(add[0]) + bias : bias, a1 = ADD ? __uint_as_float(add[1]) + bias : bias;
+  const float a2 = ADD ? __uint_as_float(add[2]) + bias : bias, a3 = ADD ? __uint_as_float(add[3]) + bias : bias;
+  const float y0 = fmaf(s4.x * sw, __uint_as_float(acc[0]), a0), y1 = fmaf(s4.y * sw, __uint_as_float(acc[1]), a1);
+  const float y2 = fmaf(s4.z * sw, __uint_as_float(acc[2]), a2), y3 = fmaf(s4.w * sw, __uint_as_float(acc[3]), a3);
   return make_uint2(bf16x2_rn(y0, y1), bf16x2_rn(y2, y3));
 }
 
@@ -398,13 +391,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (epilogue_bar_any(!ok)) { ok = false; break; }
         // the whole tile through the staging buffer: [channel half][PN tokens][64 channels] bf16
         uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (PN * 64) + (row & 63);
+        const float bn = bias_of(p, n0 + row);
 #pragma unroll
         for (int i = 0; i < C::NCHUNK; ++i)
 #pragma unroll
           for (int jj = 0; jj < CHUNK; jj += 4) {
             const int c = CHUNK * i + jj;
-            st_bf16x4(out_row + (CHUNK * (half + 2 * i) + jj) * 64, 64, bf16x2_rn(acc[c], acc[c + 1]),
-                      bf16x2_rn(acc[c + 2], acc[c + 3]));
+            st_bf16x4(out_row + (CHUNK * (half + 2 * i) + jj) * 64, 64, bf16x2_rn(acc[c] + bn, acc[c + 1] + bn),
+                      bf16x2_rn(acc[c + 2] + bn, acc[c + 3] + bn));
           }
         fence_proxy_async_smem();
         epilogue_bar();
@@ -422,6 +416,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // loaded before the accumulator is waited on, so that nothing is
       // outstanding when the accumulator is released (a release arrive waits)
       const float swr = __ldg(&p.sw[n >> p.gN_shift]);
+      const float bn = bias_of(p, n);
       if (!mbar_wait<true>(accf, acc_cnt & 1)) ok = false;
       if (epilogue_bar_any(!ok)) { ok = false; break; }
       tc_fence_after();
@@ -439,7 +434,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float* sc = scl + CHUNK * (half + 2 * i);
 #pragma unroll
         for (int j = 0; j < CHUNK; j += 4) {
-          const uint2 w = scale4_pack<true>(sc + j, swr, v + j, s2 + j);
+          const uint2 w = scale4_pack<true>(sc + j, swr, v + j, s2 + j, bn);
           pk[(CHUNK * i + j) / 2] = w.x;
           pk[(CHUNK * i + j) / 2 + 1] = w.y;
         }
@@ -508,7 +503,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int t0 = CHUNK * (half + 2 * i);
 #pragma unroll
           for (int j = 0; j < CHUNK; j += 4)
-            scale4_store<false>(scl + t0 + j, swr, v + CHUNK * i + j, nullptr, ring_row + (t0 + j) * 64, 64);
+            scale4_store<false>(scl + t0 + j, swr, v + CHUNK * i + j, nullptr, bn, ring_row + (t0 + j) * 64, 64);
         }
         fence_proxy_async_smem();
         epilogue_bar();
@@ -529,7 +524,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int t0 = C::OUT_TOKENS * s + CHUNK * half;
 #pragma unroll
           for (int j = 0; j < CHUNK; j += 4)
-            scale4_store<false>(scl + t0 + j, swr, v + CHUNK * s + j, nullptr, out_row + (CHUNK * half + j) * 64, 64);
+            scale4_store<false>(scl + t0 + j, swr, v + CHUNK * s + j, nullptr, bn, out_row + (CHUNK * half + j) * 64,
+                                64);
           fence_proxy_async_smem();
           epilogue_bar();
           if (et == 0) {

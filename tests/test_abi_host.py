@@ -78,12 +78,12 @@ def test_compress_argument_errors(lib):
 def test_gemm_argument_errors(lib):
     f = lib.sp24_fp8_gemm
     ok = dict(X=FAKE, sx=FAKE, M=64, K=512, ldx=512, gM=1, v=FAKE, m=FAKE, sw=FAKE, N=256, gN=1, gK=512,
-              X2=None, W2=None, r=0, Y=FAKE, ldy=256)
+              X2=None, W2=None, r=0, bias=None, Y=FAKE, ldy=256)
 
     def call(**kw):
         a = dict(ok, **kw)
         return f(a["X"], a["sx"], a["M"], a["K"], a["ldx"], a["gM"], a["v"], a["m"], a["sw"], a["N"], a["gN"],
-                 a["gK"], a["X2"], a["W2"], a["r"], a["Y"], a["ldy"], None, 0, None)
+                 a["gK"], a["X2"], a["W2"], a["r"], a["bias"], a["Y"], a["ldy"], None, 0, None)
 
     assert call(X=None) == 1
     assert call(Y=None) == 1
@@ -100,6 +100,7 @@ def test_gemm_argument_errors(lib):
     assert call(X=FAKE_ODD) == 3
     assert call(ldx=520) == 3
     assert call(ldy=260) == 3        # output rows must stay 16-byte aligned
+    assert call(bias=ctypes.c_void_p(0x10001)) == 3  # bf16 bias: 2-byte aligned
 
 
 def test_quantize_argument_errors(lib):

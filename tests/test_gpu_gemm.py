@@ -84,6 +84,50 @@ def test_side_gemm(ora, sp24, r, M, gK):
     _check_full(ora, sp24, w, "side r=%d M=%d" % (r, M))
 
 
+@pytest.mark.parametrize("M,N,K,gN,gK,r", [
+    (40, 384, 512, 1, None, 0),     # one-CTA kernel, 64-token tiles
+    (16, 1024, 1024, 1, None, 0),   # decode tiles with K split across CTAs
+    (300, 384, 512, 1, None, 0),    # one-CTA 256-token tiles (N not a multiple of 256)
+    (300, 512, 512, 1, None, 0),    # SM pairs
+    (300, 512, 512, 1, None, 32),   # SM pairs with the side GEMM
+    (40, 256, 512, 1, None, 16),    # one-CTA side GEMM
+    (130, 384, 768, 128, 128, 0),   # one-CTA group-wise promotion
+    (300, 512, 768, 128, 128, 0),   # SM-pair group-wise promotion
+    (130, 256, 512, 1, 128, 16),    # promotion with the side GEMM
+])
+def test_bias(ora, sp24, M, N, K, gN, gK, r):
+    """The linear operation's bias (pytorch/ao PR #3258: input, weight, bias),
+    added in fp32 before the one rounding to bf16, on every epilogue path."""
+    w = inputs.Workload("bias", M, N, K, gN=gN, gK=gK, r=r, seed=M + N + K + r)
+    xq, sx, values, meta, sw, x2, w2 = _prep(ora, w)
+    rng = np.random.default_rng(w.seed)
+    bias = inputs.bf16_bits(torch.from_numpy(rng.normal(0.0, 0.5, N).astype(np.float32)).to(torch.bfloat16))
+    tv, tm = _abi(ora, values, meta)
+    y = sp24.gemm(dev(xq), dev(sx), dev(tv), dev(tm), dev(sw), w.gM, w.gN, w.gk,
+                  None if x2 is None else dev(x2), None if w2 is None else dev(w2), bias=dev(bias))
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    ref = ora.gemm(xq, sx, values, meta, sw, w.gM, w.gN, w.gk, x2, w2, bias=bias)
+    assert_close(bf16_to_f64(y), ref, "bias M=%d N=%d K=%d gK=%s r=%d" % (M, N, K, gK, r))
+    assert np.abs(ref - ora.gemm(xq, sx, values, meta, sw, w.gM, w.gN, w.gk, x2, w2)).max() > 0.1
+
+
+def test_zero_bias_matches_no_bias(ora, sp24):
+    """A zero bias gives the values of no bias (the kernels fold -0.0 in when
+    there is none, which changes no value; +0.0 may only turn -0.0 into +0.0,
+    which compares equal)."""
+    w = inputs.Workload("nobias", 300, 512, 512, seed=5)
+    xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+    tv, tm = _abi(ora, values, meta)
+    a = sp24.gemm(dev(xq), dev(sx), dev(tv), dev(tm), dev(sw))
+    z = torch.zeros(w.N, dtype=torch.bfloat16, device="cuda")
+    b = sp24.gemm(dev(xq), dev(sx), dev(tv), dev(tm), dev(sw), bias=z)
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    assert np.array_equal(a.float().cpu().numpy(), b.float().cpu().numpy())
+    assert_close(bf16_to_f64(a), ora.gemm(xq, sx, values, meta, sw), "no bias")
+
+
 def test_k_equals_128(ora, sp24):
     _check_full(ora, sp24, inputs.Workload("k128", 70, 128, 128, seed=3), "K=128")
     _check_full(ora, sp24, inputs.Workload("k128g", 70, 128, 128, gN=128, gK=128, seed=4), "K=128 gK=128")

@@ -299,6 +299,32 @@ def test_side_gemm(ora):
     assert not np.allclose(Y, Y0, rtol=1e-3, atol=1e-3)  # the side term matters
 
 
+def test_bias_is_added_per_channel(ora):
+    """The linear operation's bias (pytorch/ao PR #3258: input, weight, bias):
+    with an all-zero weight Y[m, n] is bias[n] exactly in both accumulation
+    modes; with a weight, the fp64 result moves by exactly bias[n] (half-integer
+    biases on a problem of unit scales and integer products, so that every sum
+    is exact in double), column by column, never by row."""
+    M, N, K = 8, 128, 256
+    bias_f = np.array([(j % 17) - 8 for j in range(N)], dtype=np.float32) * 0.5
+    bias = _bf16_bits_from_f32(bias_f)
+    v0, m0, sw0 = ora.compress(np.zeros((N, K), np.uint16))
+    xq = np.full((M, K), 0x38, np.uint8)  # 1.0
+    sx = np.ones((1, M), np.float32)
+    for acc64 in (False, True):
+        Y = ora.gemm(xq, sx, v0, m0, sw0, bias=bias, acc_fp64=acc64)
+        assert np.array_equal(Y, np.broadcast_to(bias_f.astype(np.float64), (M, N)))
+    # small integer weights (e4m3 codes of 1 and 2) with unit weight scales
+    rng = np.random.default_rng(3)
+    Wf = rng.choice([-2.0, -1.0, 0.0, 1.0, 2.0], size=(N, K)).astype(np.float32)
+    v, m, _ = ora.compress(_bf16_bits_from_f32(Wf))
+    sw = np.ones((1, N), np.float32)
+    Y0 = ora.gemm(xq, sx, v, m, sw, acc_fp64=True)
+    Yb = ora.gemm(xq, sx, v, m, sw, bias=bias, acc_fp64=True)
+    assert np.array_equal(Yb - Y0, np.broadcast_to(bias_f.astype(np.float64), (M, N)))
+    assert np.all(Y0 == np.round(Y0))  # the products and sums above are exact integers
+
+
 def test_identity_dequantize(ora):
     """Dequantize by multiplying with an identity (torchao PR #3258, jcaip's
     review of dequantize): X = I (code 0x38 = 1.0), unit activation scales

@@ -47,7 +47,7 @@ def _stream():
 def _gemm_with_workspace(lib, d, M, N, K, ws):
     xq, sx, tv, tm, sw = d
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    st = lib.sp24_fp8_gemm(_p(xq), _p(sx), M, K, K, 1, _p(tv), _p(tm), _p(sw), N, 1, K, None, None, 0,
+    st = lib.sp24_fp8_gemm(_p(xq), _p(sx), M, K, K, 1, _p(tv), _p(tm), _p(sw), N, 1, K, None, None, 0, None,
                            _p(y), N, _p(ws), ws.numel(), _stream())
     return st, y
 
@@ -56,7 +56,7 @@ def _gemm_fixed_scratch(lib, d, M, N, K):
     xq, sx, tv, tm, sw = d
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     st = lib.sp24_fp8_gemm_fixed_scratch(_p(xq), _p(sx), M, K, K, 1, _p(tv), _p(tm), _p(sw), N, 1, K, None, None,
-                                         0, _p(y), N, _stream())
+                                         0, None, _p(y), N, _stream())
     return st, y
 
 
