@@ -116,6 +116,15 @@ SP24_API sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K,
                                   float* sx, void* stream);
 
 /*
+ * sp24_fp8_quantize_act_bf16 -- the same for bf16 activations (the dtype of
+ * the bf16 models the pages quantize): X (device) bf16 [M][K], row stride
+ * ldx >= K with ldx*2 a multiple of 16.  Every bf16 value is an fp32 value,
+ * so the result is that of sp24_fp8_quantize_act on X widened to fp32.
+ */
+SP24_API sp24_status sp24_fp8_quantize_act_bf16(const void* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
+                                       float* sx, void* stream);
+
+/*
  * sp24_fp8_gemm -- group-wise scaled 2:4 sparse FP8 GEMM with an optional
  * fused bf16 side GEMM:
  *

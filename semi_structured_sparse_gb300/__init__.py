@@ -31,6 +31,7 @@ SIGNATURES = {
     "sp24_meta_bytes": ([_I64, _I64], _SZ),
     "sp24_fp8_compress": ([_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P], _I),
     "sp24_fp8_quantize_act": ([_P, _I64, _I64, _I64, _I, _P, _P, _P], _I),
+    "sp24_fp8_quantize_act_bf16": ([_P, _I64, _I64, _I64, _I, _P, _P, _P], _I),
     "sp24_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P, _I64,
                        _P, _SZ, _P], _I),
     "sp24_fp8_gemm_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
@@ -127,9 +128,11 @@ def compress(w: torch.Tensor, gN: int = 1, gK: int = None, out=None, stream=None
 
 
 def quantize_act(x: torch.Tensor, gK: int = None, out=None, stream=None):
-    """Dynamic e4m3 quantization of fp32 activations [M, K]: returns (xq uint8 [M, K], sx fp32 [K/gK, M])."""
+    """Dynamic e4m3 quantization of fp32 or bf16 activations [M, K]: returns
+    (xq uint8 [M, K], sx fp32 [K/gK, M])."""
     lib = load()
-    _dev_tensor(x, torch.float32, "x")
+    bf16 = isinstance(x, torch.Tensor) and x.dtype == torch.bfloat16
+    _dev_tensor(x, torch.bfloat16 if bf16 else torch.float32, "x")
     M, K = x.shape
     gK = K if gK is None else gK
     if out is None:
@@ -137,8 +140,9 @@ def quantize_act(x: torch.Tensor, gK: int = None, out=None, stream=None):
         sx = torch.empty((K // gK, M), dtype=torch.float32, device=x.device)
     else:
         xq, sx = out
-    _check(lib.sp24_fp8_quantize_act(_ptr(x), M, K, x.stride(0), gK, _ptr(xq), _ptr(sx), _stream(stream)),
-           "sp24_fp8_quantize_act")
+    f, name = ((lib.sp24_fp8_quantize_act_bf16, "sp24_fp8_quantize_act_bf16") if bf16
+               else (lib.sp24_fp8_quantize_act, "sp24_fp8_quantize_act"))
+    _check(f(_ptr(x), M, K, x.stride(0), gK, _ptr(xq), _ptr(sx), _stream(stream)), name)
     return xq, sx
 
 

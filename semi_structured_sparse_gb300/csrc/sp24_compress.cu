@@ -313,16 +313,26 @@ __global__ void __launch_bounds__(256) compress_blocks_kernel(const uint16_t* __
   pdl_trigger();
 }
 
+// Four consecutive activations as fp32: fp32 input as is, bf16 input widened
+// (exactly: every bf16 value is an fp32 value).
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const uint16_t* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xFFFF0000u));
+}
+
 // Activation quantization: one warp per token row; 128 elements per warp
-// step (4 fp32 per lane).  GK128: each step is one scale block.
-template <bool GK128>
-__global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ X, int M, int K, int64_t ldx,
+// step (4 per lane).  GK128: each step is one scale block.  T: float, or
+// uint16_t holding bf16 (the activations of a bf16 model).
+template <bool GK128, typename T>
+__global__ void __launch_bounds__(256) quantize_act_kernel(const T* __restrict__ X, int M, int K, int64_t ldx,
                                                            uint8_t* __restrict__ xq, float* __restrict__ sx) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * 8 + warp;
   pdl_wait();
   if (m >= M) return;
-  const float* row = X + static_cast<int64_t>(m) * ldx;
+  const T* row = X + static_cast<int64_t>(m) * ldx;
   uint8_t* qrow = xq + static_cast<int64_t>(m) * K;
   const int nsteps = K / 128;
   auto quant4 = [&](const float4& f, float s) -> uint32_t {
@@ -331,7 +341,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
   auto amax4 = [](const float4& f) { return fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))); };
   if (GK128) {
     for (int c = 0; c < nsteps; ++c) {
-      const float4 f = *reinterpret_cast<const float4*>(row + c * 128 + lane * 4);
+      const float4 f = load4(row + c * 128 + lane * 4);
       float a = amax4(f);
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
@@ -341,13 +351,13 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
     }
   } else {
     float a = 0.0f;
-    for (int c = 0; c < nsteps; ++c) a = fmaxf(a, amax4(*reinterpret_cast<const float4*>(row + c * 128 + lane * 4)));
+    for (int c = 0; c < nsteps; ++c) a = fmaxf(a, amax4(load4(row + c * 128 + lane * 4)));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
     const float s = a == 0.0f ? 1.0f : __fdiv_rn(a, kE4M3Max);
     if (lane == 0) sx[m] = s;
     for (int c = 0; c < nsteps; ++c) {
-      const float4 f = *reinterpret_cast<const float4*>(row + c * 128 + lane * 4);
+      const float4 f = load4(row + c * 128 + lane * 4);
       *reinterpret_cast<uint32_t*>(qrow + c * 128 + lane * 4) = quant4(f, s);
     }
   }
@@ -398,13 +408,15 @@ extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, in
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }
 
-extern "C" sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
-                                             float* sx, void* stream) {
-  using namespace sp24;
+namespace sp24 {
+namespace {
+
+template <typename T>
+sp24_status quantize_act(const T* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq, float* sx, void* stream) {
   if (!X || !xq || !sx) return SP24_ERR_INVALID_ARG;
   if (M < 1 || K < 128 || K % 128 != 0 || ldx < K || M > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
   if (gK != K && gK != 128) return SP24_ERR_UNSUPPORTED;
-  if (!aligned16(X) || !aligned16(xq) || (ldx * 4) % 16 != 0) return SP24_ERR_ALIGNMENT;
+  if (!aligned16(X) || !aligned16(xq) || (ldx * static_cast<int64_t>(sizeof(T))) % 16 != 0) return SP24_ERR_ALIGNMENT;
   if (reinterpret_cast<uintptr_t>(sx) % 4 != 0) return SP24_ERR_ALIGNMENT;
   const DeviceInfo* dev = nullptr;
   sp24_status st = current_device(&dev);
@@ -412,11 +424,24 @@ extern "C" sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>((M + 7) / 8);
   if (gK == 128)
-    st = launch_pdl(quantize_act_kernel<true>, dim3(grid), dim3(256), 0, s, X, (int)M, (int)K, ldx,
+    st = launch_pdl(quantize_act_kernel<true, T>, dim3(grid), dim3(256), 0, s, X, (int)M, (int)K, ldx,
                     static_cast<uint8_t*>(xq), sx) == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
   else
-    st = launch_pdl(quantize_act_kernel<false>, dim3(grid), dim3(256), 0, s, X, (int)M, (int)K, ldx,
+    st = launch_pdl(quantize_act_kernel<false, T>, dim3(grid), dim3(256), 0, s, X, (int)M, (int)K, ldx,
                     static_cast<uint8_t*>(xq), sx) == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
   if (st != SP24_OK) return st;
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace sp24
+
+extern "C" sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
+                                             float* sx, void* stream) {
+  return sp24::quantize_act(X, M, K, ldx, gK, xq, sx, stream);
+}
+
+extern "C" sp24_status sp24_fp8_quantize_act_bf16(const void* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
+                                                  float* sx, void* stream) {
+  return sp24::quantize_act(static_cast<const uint16_t*>(X), M, K, ldx, gK, xq, sx, stream);
 }

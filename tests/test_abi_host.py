@@ -109,6 +109,12 @@ def test_quantize_argument_errors(lib):
     assert f(FAKE, 4, 100, 128, 128, FAKE, FAKE, None) == 1
     assert f(FAKE, 4, 256, 256, 64, FAKE, FAKE, None) == 2
     assert f(FAKE_ODD, 4, 256, 256, 128, FAKE, FAKE, None) == 3
+    g = lib.sp24_fp8_quantize_act_bf16
+    assert g(None, 4, 128, 128, 128, FAKE, FAKE, None) == 1
+    assert g(FAKE, 4, 256, 200, 128, FAKE, FAKE, None) == 1   # ldx < K
+    assert g(FAKE, 4, 256, 256, 64, FAKE, FAKE, None) == 2
+    assert g(FAKE, 4, 256, 260, 128, FAKE, FAKE, None) == 3   # bf16 rows: 16-byte multiples
+    assert g(FAKE_ODD, 4, 256, 256, 128, FAKE, FAKE, None) == 3
 
 
 def test_workspace_size(lib):

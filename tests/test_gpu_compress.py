@@ -108,6 +108,38 @@ def test_quantize_act_bit_exact(ora, sp24, name, gK):
     assert np.array_equal(host_bits(gq), oq)
 
 
+@pytest.mark.parametrize("gK", [None, 128])
+@pytest.mark.parametrize("M,K", [(1, 128), (7, 512), (300, 4096), (2048, 4096)])
+def test_quantize_act_bf16_bit_exact(ora, sp24, M, K, gK):
+    """bf16 activations (the inference dtype of the pages' models): quantized
+    exactly as their fp32 widening, which the oracle quantizes.  Rows of
+    zeros, bf16 subnormals and values near the bf16 maximum included."""
+    g = torch.Generator().manual_seed(M + K)
+    X = (torch.randn(M, K, generator=g) * 3.0).to(torch.bfloat16)
+    X[0, :64] = 0.0
+    if M > 2:
+        X[1] = 0.0                                    # an all-zero row: scale 1.0
+        X[2, :8] = torch.tensor([1e-39, -1e-39, 3e-40, 3.3e38, -3.3e38, 1e-38, 0.0, -0.0]).to(torch.bfloat16)
+    gk = K if gK is None else gK
+    oq, osx = ora.quantize_act(ora.bf16_bits_to_f32(inputs.bf16_bits(X)), gk)
+    gq, gsx = sp24.quantize_act(X.cuda(), gk)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(gsx).view(np.uint32), osx.view(np.uint32))
+    assert np.array_equal(host_bits(gq), oq)
+
+
+def test_quantize_act_bf16_strided_rows(ora, sp24):
+    """A bf16 view with a row stride larger than K (a slice of a wider tensor)."""
+    g = torch.Generator().manual_seed(9)
+    big = torch.randn(40, 768, generator=g).to(torch.bfloat16)
+    X = big[:, :512]
+    oq, osx = ora.quantize_act(ora.bf16_bits_to_f32(inputs.bf16_bits(X.contiguous())), 128)
+    gq, gsx = sp24.quantize_act(big.cuda()[:, :512], 128)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(gsx).view(np.uint32), osx.view(np.uint32))
+    assert np.array_equal(host_bits(gq), oq)
+
+
 def test_e4m3_rounding_boundaries_on_gpu(ora, sp24):
     """Rows whose amax is 448 have scale exactly 1, so the GPU's e4m3 cast is
     seen directly: every code value, every midpoint and one ulp either side,
