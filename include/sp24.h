@@ -101,6 +101,23 @@ SP24_API sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, int6
                               void* values, void* meta, float* scales, void* stream);
 
 /*
+ * sp24_fp8_decompress -- the dense dequantized weight from the compressed
+ * storage: W[n][k] = bf16(sw[k/gK][n/gN] * decode(value)) at the two kept
+ * positions of every group of four along K, +0 at the other two.  It is what
+ * sp24_fp8_gemm returns for an identity activation with unit scales ([3258],
+ * jcaip's review: dequantize by multiplying with an identity), computed
+ * directly: the product is rounded to fp32, then to bf16.
+ *
+ *   values, meta, scales (device) as produced by sp24_fp8_compress for [N][K]
+ *           with granularities gN, gK (the same combinations).
+ *   W       (device, out) bf16 [N][K], row stride ldw >= K, ldw*2 a multiple
+ *           of 16, 16-byte aligned.
+ * Preconditions: N a positive multiple of 128; K a positive multiple of 128.
+ */
+SP24_API sp24_status sp24_fp8_decompress(const void* values, const void* meta, const float* scales, int64_t N,
+                                int64_t K, int gN, int gK, void* W, int64_t ldw, void* stream);
+
+/*
  * sp24_fp8_quantize_act -- dynamic activation quantization to e4m3.
  * Follows [3258] (the activation path divides by the scale, then casts to
  * e4m3) with the per-token / 1x128 granularities of [2095].

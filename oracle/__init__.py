@@ -226,3 +226,28 @@ def bf16_bits_to_f32(bits) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float32."""
     b = _c(bits, np.uint16).astype(np.uint32) << 16
     return b.view(np.float32)
+
+
+def f32_to_bf16_bits(x) -> np.ndarray:
+    """float32 -> bf16 bit patterns, rounded to nearest, ties to even (finite
+    inputs): add half an ulp of the kept 16 bits, plus the kept LSB for ties,
+    then truncate."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+def dequantize(values, meta, scales, gN: int = 1, gK: int = None) -> np.ndarray:
+    """The dense dequantized weight as bf16 bits [N, K]: at the kept positions
+    of every group of four, the e4m3 value times its block's weight scale
+    (exact in double, then rounded to fp32, then to bf16); +0 at the pruned
+    ones.  This is what the GEMM returns for an identity activation with unit
+    activation scales (pytorch/ao PR #3258, dequantize by multiplying with an
+    identity)."""
+    codes = decompress(values, meta)
+    N, K = codes.shape
+    gK = K if gK is None else gK
+    scales = _c(scales, np.float32)
+    s = np.repeat(np.repeat(scales.astype(np.float64), gK, axis=0)[:K], gN, axis=1)[:, :N].T  # [N, K]
+    prod = e4m3_decode(codes) * s          # exact: 4 x 24 significant bits
+    return f32_to_bf16_bits(prod.astype(np.float32))

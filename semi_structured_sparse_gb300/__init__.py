@@ -32,6 +32,7 @@ SIGNATURES = {
     "sp24_fp8_compress": ([_P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P], _I),
     "sp24_fp8_quantize_act": ([_P, _I64, _I64, _I64, _I, _P, _P, _P], _I),
     "sp24_fp8_quantize_act_bf16": ([_P, _I64, _I64, _I64, _I, _P, _P, _P], _I),
+    "sp24_fp8_decompress": ([_P, _P, _P, _I64, _I64, _I, _I, _P, _I64, _P], _I),
     "sp24_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P, _I64,
                        _P, _SZ, _P], _I),
     "sp24_fp8_gemm_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
@@ -125,6 +126,21 @@ def compress(w: torch.Tensor, gN: int = 1, gK: int = None, out=None, stream=None
     _check(lib.sp24_fp8_compress(_ptr(w), N, K, w.stride(0), gN, gK, _ptr(values), _ptr(meta), _ptr(scales),
                                  _stream(stream)), "sp24_fp8_compress")
     return values, meta, scales
+
+
+def decompress(values, meta, scales, gN: int = 1, gK: int = None, out=None, stream=None):
+    """The dense dequantized weight bf16 [N, K] from compress()'s output: at the
+    kept positions bf16(scale * e4m3 value), 0 elsewhere."""
+    lib = load()
+    _dev_tensor(values, torch.uint8, "values")
+    _dev_tensor(meta, torch.uint8, "meta")
+    _dev_tensor(scales, torch.float32, "scales")
+    N, K = values.shape[0], values.shape[1] * 2
+    gK = K if gK is None else gK
+    W = torch.empty((N, K), dtype=torch.bfloat16, device=values.device) if out is None else out
+    _check(lib.sp24_fp8_decompress(_ptr(values), _ptr(meta), _ptr(scales), N, K, gN, gK, _ptr(W), W.stride(0),
+                                   _stream(stream)), "sp24_fp8_decompress")
+    return W
 
 
 def quantize_act(x: torch.Tensor, gK: int = None, out=None, stream=None):

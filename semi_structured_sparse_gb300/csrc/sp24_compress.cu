@@ -411,6 +411,49 @@ extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, in
 namespace sp24 {
 namespace {
 
+// Two e4m3 codes (low byte first) as floats: e4m3 -> f16 is exact, f16 -> f32 too.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t codes) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(codes)));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// The dense dequantized weight from the library's storage: W[n][k] =
+// bf16(sw * decode(value)) at the two kept positions of every group of four,
+// 0 at the other two -- what the GEMM returns for an identity activation
+// (pytorch/ao PR #3258, dequantize by multiplying with an identity), without
+// the GEMM.  One warp per row and 1024 consecutive k: each lane expands one
+// 16-byte chunk of kept values and 4 metadata bytes into 64 output bytes.
+__global__ void __launch_bounds__(256) decompress_kernel(const uint8_t* __restrict__ values,
+                                                         const uint8_t* __restrict__ meta,
+                                                         const float* __restrict__ scales, int N, int K, int gN_shift,
+                                                         int gK, int ldsc, uint16_t* __restrict__ W, int64_t ldw) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + warp;
+  const int k0 = blockIdx.y * 1024 + lane * 32;
+  pdl_wait();
+  if (n >= N || k0 >= K) return;
+  const uint4 v = *reinterpret_cast<const uint4*>(values + values_offset(n, k0 / 2, K));
+  const uint32_t mw = *reinterpret_cast<const uint32_t*>(meta + meta_offset(n, k0 / 8, K));
+  const float s = scales[static_cast<int64_t>(k0 / gK) * ldsc + (n >> gN_shift)];
+  const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[16];  // 32 bf16, two per word
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {  // weights k0 + 4g + [0, 4): kept values 2g (position i0) and 2g + 1 (i1 > i0)
+    const uint32_t nib = (mw >> (4 * g)) & 0xFu;
+    const uint32_t i0 = nib & 3u, i1 = nib >> 2;
+    const float2 f = e4m3x2_to_float2(vw[g / 2] >> (16 * (g & 1)));
+    const uint32_t b = bf16x2_rn(__fmul_rn(f.x, s), __fmul_rn(f.y, s));
+    const uint32_t b0 = b & 0xFFFFu, b1 = b >> 16;
+    out[2 * g] = (i0 < 2 ? b0 << (16 * i0) : 0u) | (i1 < 2 ? b1 << (16 * i1) : 0u);
+    out[2 * g + 1] = (i0 >= 2 ? b0 << (16 * (i0 - 2)) : 0u) | (i1 >= 2 ? b1 << (16 * (i1 - 2)) : 0u);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(W + static_cast<int64_t>(n) * ldw + k0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+  pdl_trigger();
+}
+
 template <typename T>
 sp24_status quantize_act(const T* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq, float* sx, void* stream) {
   if (!X || !xq || !sx) return SP24_ERR_INVALID_ARG;
@@ -444,4 +487,25 @@ extern "C" sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t 
 extern "C" sp24_status sp24_fp8_quantize_act_bf16(const void* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
                                                   float* sx, void* stream) {
   return sp24::quantize_act(static_cast<const uint16_t*>(X), M, K, ldx, gK, xq, sx, stream);
+}
+
+extern "C" sp24_status sp24_fp8_decompress(const void* values, const void* meta, const float* scales, int64_t N,
+                                           int64_t K, int gN, int gK, void* W, int64_t ldw, void* stream) {
+  using namespace sp24;
+  if (!values || !meta || !scales || !W) return SP24_ERR_INVALID_ARG;
+  if (N < 1 || K < 128 || K % 128 != 0 || ldw < K || N > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
+  if (!((gN == 1 && gK == K) || (gN == 1 && gK == 128) || (gN == 128 && gK == 128))) return SP24_ERR_UNSUPPORTED;
+  if (N % 128 != 0) return SP24_ERR_INVALID_ARG;  // tiled storage: whole 128-row bands
+  if (!aligned16(values) || !aligned16(meta) || !aligned16(W) || (ldw * 2) % 16 != 0) return SP24_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(scales) % 4 != 0) return SP24_ERR_ALIGNMENT;
+  const DeviceInfo* dev = nullptr;
+  sp24_status st = current_device(&dev);
+  if (st != SP24_OK) return st;
+  const dim3 grid(static_cast<unsigned>((N + 7) / 8), static_cast<unsigned>((K + 1023) / 1024));
+  const int ldsc = static_cast<int>((N + gN - 1) / gN);
+  if (launch_pdl(decompress_kernel, grid, dim3(256), 0, static_cast<cudaStream_t>(stream),
+                 static_cast<const uint8_t*>(values), static_cast<const uint8_t*>(meta), scales, (int)N, (int)K,
+                 gN == 128 ? 7 : 0, gK, ldsc, static_cast<uint16_t*>(W), ldw) != cudaSuccess)
+    return SP24_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }

@@ -62,14 +62,6 @@ __device__ __forceinline__ bool epilogue_bar_any(bool pred) {
 }
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
 
-// Packed round-to-nearest-even of two fp32 values to bf16 (lo in the low
-// half): one conversion instruction for two outputs, which matters because
-// the scalar conversion runs at a fraction of the FP32 rate.
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 // Writes the four bf16 in (lo, hi) to dst[0], dst[stride], dst[2 stride], dst[3 stride].
 __device__ __forceinline__ void st_bf16x4(uint16_t* dst, int stride, uint32_t lo, uint32_t hi) {
   dst[0] = static_cast<uint16_t>(lo & 0xFFFFu);

@@ -391,4 +391,12 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, float x0, float x1, 
   a1 = r.y;
 }
 
+// Packed round-to-nearest-even of two fp32 values to bf16 (lo in the low
+// half): one conversion instruction for two outputs, which matters because
+// the scalar conversion runs at a fraction of the FP32 rate.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 }  // namespace sp24

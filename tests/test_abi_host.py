@@ -117,6 +117,17 @@ def test_quantize_argument_errors(lib):
     assert g(FAKE_ODD, 4, 256, 256, 128, FAKE, FAKE, None) == 3
 
 
+def test_decompress_argument_errors(lib):
+    f = lib.sp24_fp8_decompress
+    assert f(None, FAKE, FAKE, 128, 256, 1, 256, FAKE, 256, None) == 1
+    assert f(FAKE, FAKE, FAKE, 100, 256, 1, 256, FAKE, 256, None) == 1   # whole 128-row bands
+    assert f(FAKE, FAKE, FAKE, 128, 200, 1, 200, FAKE, 256, None) == 1
+    assert f(FAKE, FAKE, FAKE, 128, 256, 1, 256, FAKE, 128, None) == 1   # ldw < K
+    assert f(FAKE, FAKE, FAKE, 128, 256, 128, 256, FAKE, 256, None) == 2  # 128 x K blocks: not a compress output
+    assert f(FAKE, FAKE, FAKE, 128, 256, 1, 256, FAKE, 260, None) == 3   # bf16 rows: 16-byte multiples
+    assert f(FAKE, FAKE, FAKE, 128, 256, 1, 256, FAKE_ODD, 256, None) == 3
+
+
 def test_workspace_size(lib):
     assert lib.sp24_fp8_gemm_workspace_size(2048, 4096, 4096, 0) >= 0
 

@@ -239,3 +239,40 @@ def test_every_bf16_magnitude_against_many_scales(ora, sp24):
     gvb = host_bits(gv).ravel()
     bad = np.flatnonzero(gvb != ov)
     assert bad.size == 0, "%d value bytes differ, first at %s" % (bad.size, bad[:8])
+
+
+@pytest.mark.parametrize("gN,gK", [(1, None), (1, 128), (128, 128)])
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 640), (384, 2176), (1024, 4096)])
+def test_decompress_bit_exact(ora, sp24, N, K, gN, gK):
+    """GPU dequantize (the dense weight bf16(sw * e4m3) with zeros at the
+    pruned positions) from the GPU's own compression: bit-exact against the
+    oracle's dequantize of the oracle's compression.  K values that are not
+    a multiple of 1024 leave part of the last column of warps idle."""
+    g = torch.Generator().manual_seed(N + K)
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    gk = K if gK is None else gK
+    v, m, s = sp24.compress(W.cuda(), gN, gk)
+    D = sp24.decompress(v, m, s, gN, gk)
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    ov, om, os_ = ora.compress(inputs.bf16_bits(W), gN, gk)
+    assert np.array_equal(host_bits(D), ora.dequantize(ov, om, os_, gN, gk))
+
+
+def test_decompress_strided_output_and_zero_weight(ora, sp24):
+    """Output rows wider than K (a view into a larger buffer; the columns
+    past K untouched), and an all-zero weight (scale 1, every output +0)."""
+    N, K = 256, 512
+    g = torch.Generator().manual_seed(4)
+    W = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    W[:128] = 0.0
+    v, m, s = sp24.compress(W.cuda())
+    big = torch.full((N, K + 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    sp24.decompress(v, m, s, out=big[:, :K])
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    ov, om, os_ = ora.compress(inputs.bf16_bits(W))
+    ref = ora.dequantize(ov, om, os_)
+    assert np.array_equal(host_bits(big[:, :K].contiguous()), ref)
+    assert np.all(host_bits(big[:, :K].contiguous())[:128] == 0)
+    assert torch.all(big[:, K:] == 7.0)

@@ -325,6 +325,38 @@ def test_bias_is_added_per_channel(ora):
     assert np.all(Y0 == np.round(Y0))  # the products and sums above are exact integers
 
 
+def test_f32_to_bf16_matches_torch(ora):
+    """Round to nearest even, from fp32 to bf16: against torch's cast on
+    random values, exact ties and the values next to them."""
+    rng = np.random.default_rng(12)
+    x = np.concatenate([rng.normal(0, 1, 4096), rng.normal(0, 1e-30, 256), rng.normal(0, 1e30, 256)])
+    ties = (np.arange(1, 513, dtype=np.uint32) << 16) | 0x8000  # exactly halfway, odd and even kept LSB
+    near = np.concatenate([ties - 1, ties + 1])
+    x = np.concatenate([x.astype(np.float32), ties.view(np.float32), near.view(np.float32),
+                        np.array([0.0, -0.0, 3.3e38, -3.3e38], np.float32)])
+    ref = inputs.bf16_bits(torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16))
+    assert np.array_equal(ora.f32_to_bf16_bits(x), ref)
+
+
+@pytest.mark.parametrize("gN,gK", [(1, None), (1, 128), (128, 128)])
+def test_dequantize_is_the_identity_gemm(ora, gN, gK):
+    """Dequantize = the GEMM of an identity activation with unit scales,
+    rounded to bf16 by torch (pytorch/ao PR #3258, dequantize by multiplying
+    with an identity); +0 exactly where the metadata drops a weight."""
+    N, K = 128, 256
+    _, W, _, _ = inputs.generate(inputs.with_shape(inputs.WORKLOADS["tiny"], N=N, K=K, seed=8))
+    v, m, sw = ora.compress(inputs.bf16_bits(W), gN, gK)
+    gk = K if gK is None else gK
+    D = ora.dequantize(v, m, sw, gN, gk)
+    xq = np.where(np.eye(K, dtype=bool), 0x38, 0).astype(np.uint8)
+    sx = np.ones((K // gk, K), np.float32)
+    Y = ora.gemm(xq, sx, v, m, sw, 1, gN, gk)                  # [K tokens, N channels]
+    ref = inputs.bf16_bits(torch.from_numpy(Y.astype(np.float32).T.copy()).to(torch.bfloat16))
+    assert np.array_equal(D, ref)
+    assert np.all(D[ora.decompress(v, m) == 0] == 0)
+    assert np.count_nonzero(ora.decompress(v, m)) <= N * K // 2
+
+
 def test_identity_dequantize(ora):
     """Dequantize by multiplying with an identity (torchao PR #3258, jcaip's
     review of dequantize): X = I (code 0x38 = 1.0), unit activation scales
