@@ -313,26 +313,18 @@ __global__ void __launch_bounds__(256) compress_blocks_kernel(const uint16_t* __
   pdl_trigger();
 }
 
-// Four consecutive activations as fp32: fp32 input as is, bf16 input widened
-// (exactly: every bf16 value is an fp32 value).
 __device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ float4 load4(const uint16_t* p) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
-                     __uint_as_float(u.y & 0xFFFF0000u));
-}
 
-// Activation quantization: one warp per token row; 128 elements per warp
-// step (4 per lane).  GK128: each step is one scale block.  T: float, or
-// uint16_t holding bf16 (the activations of a bf16 model).
-template <bool GK128, typename T>
-__global__ void __launch_bounds__(256) quantize_act_kernel(const T* __restrict__ X, int M, int K, int64_t ldx,
+// Activation quantization (fp32 input): one warp per token row; 128
+// elements per warp step (4 per lane).  GK128: each step is one scale block.
+template <bool GK128>
+__global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ X, int M, int K, int64_t ldx,
                                                            uint8_t* __restrict__ xq, float* __restrict__ sx) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * 8 + warp;
   pdl_wait();
   if (m >= M) return;
-  const T* row = X + static_cast<int64_t>(m) * ldx;
+  const float* row = X + static_cast<int64_t>(m) * ldx;
   uint8_t* qrow = xq + static_cast<int64_t>(m) * K;
   const int nsteps = K / 128;
   auto quant4 = [&](const float4& f, float s) -> uint32_t {
@@ -454,6 +446,97 @@ __global__ void __launch_bounds__(256) decompress_kernel(const uint8_t* __restri
   pdl_trigger();
 }
 
+// x / s for 8 bf16 values (one 16-byte chunk) as 8 e4m3 codes, with the
+// correctly rounded division of the weight path (div_scale; exact division
+// for scales below kMinFastScale, where the reciprocal would overflow).
+__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t q[4];
+  if (s >= kMinFastScale) {
+    const float r = __frcp_rn(s);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      q[i] = to_e4m3x2(div_scale(bf16_bits_to_float(w[i] & 0xFFFFu), s, r), div_scale(bf16_bits_to_float(w[i] >> 16), s, r));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      q[i] = to_e4m3x2(__fdiv_rn(bf16_bits_to_float(w[i] & 0xFFFFu), s), __fdiv_rn(bf16_bits_to_float(w[i] >> 16), s));
+  }
+  return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
+// Activation quantization from bf16 (the dtype of the pages' models): one
+// CTA of 4 warps per token row; warp w takes the steps w, w + 4, ... of 256
+// elements (one 16-byte load per lane), so a 128-wide scale block is a half
+// warp.  Rows of up to 4096 elements stay in registers between the amax and
+// the quantization; per token, the 4 warps' maxima meet in shared memory.
+constexpr int kActWarps = 4;
+constexpr int kHeldSteps = 4;  // per warp: K <= kActWarps * kHeldSteps * 256 = 4096 held
+template <bool GK128>
+__global__ void __launch_bounds__(32 * kActWarps) quantize_act_bf16_kernel(const uint16_t* __restrict__ X, int M,
+                                                                           int K, int64_t ldx,
+                                                                           uint8_t* __restrict__ xq,
+                                                                           float* __restrict__ sx) {
+  __shared__ uint32_t wmax[kActWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x;
+  pdl_wait();
+  const uint16_t* row = X + static_cast<int64_t>(m) * ldx;
+  uint8_t* qrow = xq + static_cast<int64_t>(m) * K;
+  const int nsteps = (K + 255) / 256;  // a last step of 128 elements uses lanes 0-15
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 held[kHeldSteps];
+  uint32_t acc = 0;
+#pragma unroll
+  for (int i = 0; i < kHeldSteps; ++i) {
+    const int c = warp + kActWarps * i, k = c * 256 + lane * 8;
+    held[i] = (c < nsteps && k < K) ? ldg_stream(row + k) : zero;
+    if (!GK128) acc = amax2_acc(acc, held[i]);
+  }
+  if (GK128) {
+    auto block = [&](int c, const uint4& v) {  // one step: two 128-wide scale blocks, a half warp each
+      const int k = c * 256 + lane * 8;
+      uint32_t a = amax2_bits(amax2_acc(0u, v));
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+      const float s = weight_scale(a);
+      if (k < K && (lane & 15) == 0) sx[static_cast<int64_t>(k / 128) * M + m] = s;
+      if (k < K) *reinterpret_cast<uint2*>(qrow + k) = quant8(v, s);
+    };
+#pragma unroll
+    for (int i = 0; i < kHeldSteps; ++i)
+      if (warp + kActWarps * i < nsteps) block(warp + kActWarps * i, held[i]);
+    for (int c = warp + kActWarps * kHeldSteps; c < nsteps; c += kActWarps) {
+      const int k = c * 256 + lane * 8;
+      block(c, k < K ? ldg_stream(row + k) : zero);
+    }
+  } else {
+    for (int c = warp + kActWarps * kHeldSteps; c < nsteps; c += kActWarps) {
+      const int k = c * 256 + lane * 8;
+      if (k < K) acc = amax2_acc(acc, ldg_stream(row + k));
+    }
+    uint32_t a = amax2_bits(acc);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+    if (lane == 0) wmax[warp] = a;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kActWarps; ++w) a = max(a, wmax[w]);
+    const float s = weight_scale(a);
+    if (threadIdx.x == 0) sx[m] = s;
+#pragma unroll
+    for (int i = 0; i < kHeldSteps; ++i) {
+      const int c = warp + kActWarps * i, k = c * 256 + lane * 8;
+      if (c < nsteps && k < K) *reinterpret_cast<uint2*>(qrow + k) = quant8(held[i], s);
+    }
+    for (int c = warp + kActWarps * kHeldSteps; c < nsteps; c += kActWarps) {
+      const int k = c * 256 + lane * 8;
+      if (k < K) *reinterpret_cast<uint2*>(qrow + k) = quant8(ldg_stream(row + k), s);
+    }
+  }
+  pdl_trigger();
+}
+
 template <typename T>
 sp24_status quantize_act(const T* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq, float* sx, void* stream) {
   if (!X || !xq || !sx) return SP24_ERR_INVALID_ARG;
@@ -466,12 +549,17 @@ sp24_status quantize_act(const T* X, int64_t M, int64_t K, int64_t ldx, int gK, 
   if (st != SP24_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>((M + 7) / 8);
-  if (gK == 128)
-    st = launch_pdl(quantize_act_kernel<true, T>, dim3(grid), dim3(256), 0, s, X, (int)M, (int)K, ldx,
-                    static_cast<uint8_t*>(xq), sx) == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
-  else
-    st = launch_pdl(quantize_act_kernel<false, T>, dim3(grid), dim3(256), 0, s, X, (int)M, (int)K, ldx,
-                    static_cast<uint8_t*>(xq), sx) == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+  auto kern = [&](auto k, unsigned blocks, unsigned threads) {
+    return launch_pdl(k, dim3(blocks), dim3(threads), 0, s, X, (int)M, (int)K, ldx, static_cast<uint8_t*>(xq),
+                      sx) == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+  };
+  if constexpr (sizeof(T) == 2) {
+    const unsigned rows = static_cast<unsigned>(M), threads = 32 * kActWarps;
+    st = gK == 128 ? kern(quantize_act_bf16_kernel<true>, rows, threads)
+                   : kern(quantize_act_bf16_kernel<false>, rows, threads);
+  } else {
+    st = gK == 128 ? kern(quantize_act_kernel<true>, grid, 256) : kern(quantize_act_kernel<false>, grid, 256);
+  }
   if (st != SP24_OK) return st;
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }
