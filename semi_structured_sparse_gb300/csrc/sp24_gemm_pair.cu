@@ -104,11 +104,15 @@ template <bool ADD>
 __device__ __forceinline__ uint2 scale4_pack(const float* s, float sw, const uint32_t* acc, const uint32_t* add,
                                              float bias) {
   const float4 s4 = *reinterpret_cast<const float4*>(s);
-  const float a0 = ADD ? __uint_as_float(add[0]) + bias : bias, a1 = ADD ? __uint_as_float(add[1]) + bias : bias;
-  const float a2 = ADD ? __uint_as_float(add[2]) + bias : bias, a3 = ADD ? __uint_as_float(add[3]) + bias : bias;
-  const float y0 = fmaf(s4.x * sw, __uint_as_float(acc[0]), a0), y1 = fmaf(s4.y * sw, __uint_as_float(acc[1]), a1);
-  const float y2 = fmaf(s4.z * sw, __uint_as_float(acc[2]), a2), y3 = fmaf(s4.w * sw, __uint_as_float(acc[3]), a3);
-  return make_uint2(bf16x2_rn(y0, y1), bf16x2_rn(y2, y3));
+  const float2 b2 = make_float2(bias, bias);
+  const float2 a01 = ADD ? __fadd2_rn(make_float2(__uint_as_float(add[0]), __uint_as_float(add[1])), b2) : b2;
+  const float2 a23 = ADD ? __fadd2_rn(make_float2(__uint_as_float(add[2]), __uint_as_float(add[3])), b2) : b2;
+  const float2 w2 = make_float2(sw, sw);
+  const float2 y01 = __ffma2_rn(__fmul2_rn(make_float2(s4.x, s4.y), w2),
+                                make_float2(__uint_as_float(acc[0]), __uint_as_float(acc[1])), a01);
+  const float2 y23 = __ffma2_rn(__fmul2_rn(make_float2(s4.z, s4.w), w2),
+                                make_float2(__uint_as_float(acc[2]), __uint_as_float(acc[3])), a23);
+  return make_uint2(bf16x2_rn(y01.x, y01.y), bf16x2_rn(y23.x, y23.y));
 }
 
 // Loads N consecutive accumulator columns (N a multiple of 8) of this warp's lanes.
