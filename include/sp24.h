@@ -190,6 +190,30 @@ SP24_API sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, i
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sp24_fp8_gemm_batched -- L independent problems of one shape in one call:
+ * Y_l = sp24_fp8_gemm(Xq_l, sx_l, values_l, meta_l, sw_l, bias_l) for
+ * l < L, with problem l's operands at base + l * stride (the batched L mode
+ * of CUTLASS's (M, N, K, L) problem shape, [2095]).  No side GEMM.
+ *
+ *   stride_x, stride_values, stride_meta: bytes between problems (multiples
+ *           of 16; Xq, values and meta of one problem at least M*ldx,
+ *           N*K/2 and N*K/8 bytes);
+ *   stride_sx, stride_sw, stride_bias, stride_y: elements between problems
+ *           (fp32, fp32, bf16, bf16; stride_y*2 a multiple of 16).
+ *   workspace: L times the single problem's sp24_fp8_gemm_workspace_size
+ *           for split K (less: the problems run unsplit).
+ * Problems small enough to leave SMs idle run in one launch whose persistent
+ * CTAs take work units from every problem; problems that fill the GPU on
+ * their own (the SM-pair cases) run as back-to-back launches.
+ */
+SP24_API sp24_status sp24_fp8_gemm_batched(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
+                                  const void* values, const void* meta, const float* sw, int64_t N, int gN, int gK,
+                                  const void* bias, void* Y, int64_t ldy, int64_t L, int64_t stride_x,
+                                  int64_t stride_sx, int64_t stride_values, int64_t stride_meta, int64_t stride_sw,
+                                  int64_t stride_bias, int64_t stride_y, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
  * sp24_fp8_gemm_fixed_scratch -- sp24_fp8_gemm for callers that may not
  * allocate.  The pages have no counterpart to this entry point.
  *

@@ -36,6 +36,8 @@ SIGNATURES = {
     "sp24_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P, _I64,
                        _P, _SZ, _P], _I),
     "sp24_fp8_gemm_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
+    "sp24_fp8_gemm_batched": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _I64,
+                               _I64, _I64, _I64, _I64, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "sp24_fp8_gemm_fixed_scratch": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P,
                                      _I64, _P], _I),
     "sp24_last_device_error": ([_P], _I),
@@ -197,6 +199,37 @@ def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None, x2=
                              gN, gK, _ptr(x2), _ptr(w2), r, _ptr(bias), _ptr(y), y.stride(0), _ptr(workspace),
                              0 if workspace is None else workspace.numel() * workspace.element_size(),
                              _stream(stream)), "sp24_fp8_gemm")
+    return y
+
+
+def gemm_batched(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None, bias=None, out=None,
+                 workspace=None, stream=None):
+    """L independent problems of one shape: xq [L, M, K], sx [L, K/gK, ceil(M/gM)],
+    values [L, N, K/2], meta [L, N, K/8], sw [L, K/gK, ceil(N/gN)], bias [L, N] or
+    None -> Y [L, M, N] bf16, Y[l] = gemm(xq[l], ..., bias[l])."""
+    lib = load()
+    for t, dt, nm in ((xq, torch.uint8, "xq"), (values, torch.uint8, "values"), (meta, torch.uint8, "meta"),
+                      (sx, torch.float32, "sx"), (sw, torch.float32, "sw")):
+        _dev_tensor(t, dt, nm)
+        if t.dim() != 3 or not t[0].is_contiguous():
+            raise ValueError("%s must be [L, ...] with contiguous problems" % nm)
+    L, M, K = xq.shape
+    N = values.shape[1]
+    gK = K if gK is None else gK
+    if bias is not None:
+        _dev_tensor(bias, torch.bfloat16, "bias")
+        if bias.shape != (L, N):
+            raise ValueError("bias must be [L, N]")
+    y = torch.empty((L, M, N), dtype=torch.bfloat16, device=xq.device) if out is None else out
+    ws_bytes = L * int(lib.sp24_fp8_gemm_workspace_size(M, N, K, 0))
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=xq.device)
+    _check(lib.sp24_fp8_gemm_batched(
+        _ptr(xq), _ptr(sx), M, K, xq.stride(1), gM, _ptr(values), _ptr(meta), _ptr(sw), N, gN, gK, _ptr(bias),
+        _ptr(y), y.stride(1), L, xq.stride(0), sx.stride(0), values.stride(0), meta.stride(0), sw.stride(0),
+        0 if bias is None else bias.stride(0), y.stride(0), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream)),
+        "sp24_fp8_gemm_batched")
     return y
 
 

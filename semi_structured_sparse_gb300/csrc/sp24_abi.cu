@@ -68,6 +68,20 @@ sp24_status make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
   return r == CUDA_SUCCESS ? SP24_OK : SP24_ERR_CUDA;
 }
 
+sp24_status make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t cols, uint64_t rows,
+                         uint64_t depth, uint64_t row_stride_bytes, uint64_t depth_stride_bytes, uint32_t box_cols,
+                         uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  if (!g_encode) return SP24_ERR_CUDA;
+  cuuint64_t dims[3] = {cols, rows, depth};
+  cuuint64_t strides[2] = {row_stride_bytes, depth_stride_bytes};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SP24_OK : SP24_ERR_CUDA;
+}
+
 }  // namespace sp24
 
 extern "C" {

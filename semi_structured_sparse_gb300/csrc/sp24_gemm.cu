@@ -75,17 +75,19 @@ struct Cfg {
 };
 
 // Work schedule: a unit is (token tile, weight tile, K split); units are
-// numbered weight tile fastest, then split, then token tile, and dealt to the
-// persistent CTAs round-robin.
+// numbered weight tile fastest, then split, then token tile, then problem of
+// the batch, and dealt to the persistent CTAs round-robin.
 struct Unit {
-  int m_tile, n_tile, split, kt0, kt1;
+  int b, m_tile, n_tile, split, kt0, kt1;
 };
 __device__ __forceinline__ Unit unit_of(const GemmArgs& p, int u) {
   Unit r;
   r.n_tile = u % p.n_tiles;
   const int rest = u / p.n_tiles;
   r.split = rest % p.splits;
-  r.m_tile = rest / p.splits;
+  const int rest2 = rest / p.splits;
+  r.m_tile = rest2 % p.m_tiles;
+  r.b = rest2 / p.m_tiles;
   r.kt0 = r.split * p.kt_per_split;
   r.kt1 = min(r.kt0 + p.kt_per_split, p.k_tiles);
   return r;
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_units = p.m_tiles * p.n_tiles * p.splits;
+  const int num_units = p.L * p.m_tiles * p.n_tiles * p.splits;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1 + (PROMOTE ? 32 : 0));
@@ -174,8 +176,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int n_tile = t.n_tile;
       const int n0 = n_tile * BM;
       const int m0 = t.m_tile * BN;
-      const uint8_t* vsrc = p.values + static_cast<int64_t>(n_tile) * p.k_tiles * A_STAGE;
-      const uint8_t* msrc = p.meta + static_cast<int64_t>(n_tile) * p.k_tiles * META_STAGE;
+      const uint8_t* vsrc = p.values + t.b * p.bs_values + static_cast<int64_t>(n_tile) * p.k_tiles * A_STAGE;
+      const uint8_t* msrc = p.meta + t.b * p.bs_meta + static_cast<int64_t>(n_tile) * p.k_tiles * META_STAGE;
       for (int kt = t.kt0; kt < t.kt1; kt += KS, ++flat) {
         if (flat % PRODUCERS != pw) continue;
         const uint32_t stage = static_cast<uint32_t>(flat % STAGES);
@@ -189,18 +191,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bulk_load(sA + C::META_OFF, msrc + static_cast<int64_t>(kt) * META_STAGE, KS * META_STAGE, &full[stage]);
 #pragma unroll
           for (int j = 0; j < KS; ++j)
-            tma_load_2d(sA + C::B_OFF + j * C::B_SUB, &tm_x, &full[stage], (kt + j) * BK, m0);
+            tma_load_3d(sA + C::B_OFF + j * C::B_SUB, &tm_x, &full[stage], (kt + j) * BK, m0, t.b);
         }
         if (PROMOTE) {
 #pragma unroll
           for (int j = 0; j < KS; ++j) {  // the scales of each K block of the stage, in its own slot
             float* ssl = reinterpret_cast<float*>(sA + C::SCL_OFF + j * 1024);
-            const float* sxk = p.sx + static_cast<int64_t>(kt + j) * p.ldsx;
+            const float* sxk = p.sx + t.b * p.bs_sx + static_cast<int64_t>(kt + j) * p.ldsx;
             for (int i = lane; i < BN; i += 32) {
               const int m = m0 + i;
               cp_async_4(&ssl[i], sxk + ((m < p.M ? m : p.M - 1) >> p.gM_shift), m < p.M ? 4u : 0u);
             }
-            const float* swk = p.sw + static_cast<int64_t>(kt + j) * p.ldsw;
+            const float* swk = p.sw + t.b * p.bs_sw + static_cast<int64_t>(kt + j) * p.ldsw;
             if (p.gN_shift == 0) {
               for (int i = lane; i < BM; i += 32) cp_async_4(&ssl[BN + i], swk + n0 + i, 4u);
             } else if (lane == 0) {
@@ -333,14 +335,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t b = acc_cnt % NACC;
         if (et < BN) {
           const int m = m0 + et;
-          scl[et] = m < p.M ? __ldg(&p.sx[m >> p.gM_shift]) : 0.0f;
+          scl[et] = m < p.M ? __ldg(&p.sx[t.b * p.bs_sx + (m >> p.gM_shift)]) : 0.0f;
         }
         if (!mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
         if (SIDE && ok && !mbar_wait(saccf, side_cnt & 1)) ok = false;
         if (epilogue_bar_any(!ok)) { ok = false; break; }
         tc_fence_after();
-        const float swr = __ldg(&p.sw[n >> p.gN_shift]);
-        const float bn = bias_of(p, n);
+        const float swr = __ldg(&p.sw[t.b * p.bs_sw + (n >> p.gN_shift)]);
+        const float bn = bias_of(p, t.b * p.bs_bias + n);
         if constexpr (BN > 128) {
           // one accumulator: copy this warp's 128 columns to registers and free
           // TMEM at once, so the next tile's MMAs overlap the rest of the epilogue
@@ -363,8 +365,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();
             epilogue_bar();
             if (et == 0) {
-              tma_store_2d(&tm_y, out_tile, n0, m0 + pass * C::OUT_TOKENS);
-              tma_store_2d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0 + pass * C::OUT_TOKENS);
+              tma_store_3d(&tm_y, out_tile, n0, m0 + pass * C::OUT_TOKENS, t.b);
+              tma_store_3d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0 + pass * C::OUT_TOKENS, t.b);
               bulk_commit();
               if (pass == 0) bulk_wait_read_all();
             }
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if constexpr (SPLIT) {
           if (p.splits > 1) {
             // unscaled fp32 partials of the K splits of a tile, [tile][split][col][row]
-            const int tile_id = t.m_tile * p.n_tiles + t.n_tile;
+            const int tile_id = (t.b * p.m_tiles + t.m_tile) * p.n_tiles + t.n_tile;
             unsigned long long* tflags = p.flags + static_cast<int64_t>(tile_id) * p.splits;
             if (t.split < p.splits - 1) {
               // an earlier split: publish the partial for the tile's last split
@@ -439,8 +441,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();
             epilogue_bar();
             if (et == 0) {
-              tma_store_2d(&tm_y, out_tile, n0, m0);
-              tma_store_2d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0);
+              tma_store_3d(&tm_y, out_tile, n0, m0, t.b);
+              tma_store_3d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0, t.b);
               bulk_commit();
             }
             continue;
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane == 0) mbar_arrive(sacce);
           ++side_cnt;
         }
-        const float bn = bias_of(p, n);
+        const float bn = bias_of(p, t.b * p.bs_bias + n);
 #pragma unroll
         for (int j = 0; j < COLS; j += 4)
           st_bf16x4(out_row + (c0 + j) * 64, 64, bf16x2_rn(acc[j] + bn, acc[j + 1] + bn),
@@ -544,8 +546,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       fence_proxy_async_smem();
       epilogue_bar();
       if (et == 0) {
-        tma_store_2d(&tm_y, out_tile, n0, m0);
-        tma_store_2d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0);
+        tma_store_3d(&tm_y, out_tile, n0, m0, t.b);
+        tma_store_3d(&tm_y, out_tile + C::OUT_TOKENS * 128, n0 + 64, m0, t.b);
         bulk_commit();
       }
     }
@@ -727,11 +729,20 @@ extern "C" size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, 
   return make_plan(M, N, K, false, r > 0, sms).ws_bytes;
 }
 
-extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
-                                     const void* values, const void* meta, const float* sw, int64_t N, int gN,
-                                     int gK, const void* X2, const void* W2, int64_t r, const void* bias, void* Y,
-                                     int64_t ldy, void* workspace, size_t workspace_bytes, void* stream) {
-  using namespace sp24;
+namespace sp24 {
+namespace {
+
+// A batch of L problems of one shape: per-problem offsets of every operand
+// (bytes for Xq, values and meta; elements for the scales, the bias and Y).
+struct Batch {
+  int64_t L = 1;
+  int64_t x = 0, values = 0, meta = 0, sx = 0, sw = 0, bias = 0, y = 0;
+};
+
+sp24_status gemm_impl(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM, const void* values,
+                      const void* meta, const float* sw, int64_t N, int gN, int gK, const void* X2, const void* W2,
+                      int64_t r, const void* bias, void* Y, int64_t ldy, const Batch& bt, void* workspace,
+                      size_t workspace_bytes, void* stream) {
   if (!Xq || !sx || !values || !meta || !sw || !Y) return SP24_ERR_INVALID_ARG;
   if (M < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0) return SP24_ERR_INVALID_ARG;
   if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
@@ -753,7 +764,23 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   if (st != SP24_OK) return st;
 
   const bool promote = (gK == 128 && K != 128);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (bt.L > 1 && (pair_gemm_applies(M, N, K, !promote, r) || (promote && pair_promote_applies(M, N, K, r)))) {
+    // problems that fill the GPU on their own: one SM-pair launch each, back
+    // to back on the stream (each launch's prologue overlaps the previous tail)
+    for (int64_t b = 0; b < bt.L; ++b) {
+      const sp24_status e = gemm_impl(
+          static_cast<const uint8_t*>(Xq) + b * bt.x, sx + b * bt.sx, M, K, ldx, gM,
+          static_cast<const uint8_t*>(values) + b * bt.values, static_cast<const uint8_t*>(meta) + b * bt.meta,
+          sw + b * bt.sw, N, gN, gK, X2, W2, r, bias ? static_cast<const uint16_t*>(bias) + b * bt.bias : nullptr,
+          static_cast<uint16_t*>(Y) + b * bt.y, ldy, Batch{}, workspace, workspace_bytes, stream);
+      if (e != SP24_OK) return e;
+    }
+    return SP24_OK;
+  }
   Plan pl = make_plan(M, N, K, promote, side, dev->sm_count);
+  pl.ws_partials *= bt.L;  // split-K partials and flags of every problem
+  pl.ws_bytes *= bt.L;
   if (pl.splits > 1 && (workspace == nullptr || workspace_bytes < pl.ws_bytes || !aligned16(workspace))) {
     pl.splits = 1;  // no (or too small a) workspace: run unsplit
   }
@@ -763,6 +790,12 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   a.sx = sx;
   a.sw = sw;
   a.bias = static_cast<const uint16_t*>(bias);
+  a.L = static_cast<int>(bt.L);
+  a.bs_values = bt.values;
+  a.bs_meta = bt.meta;
+  a.bs_sx = bt.sx;
+  a.bs_sw = bt.sw;
+  a.bs_bias = bt.bias;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
@@ -780,8 +813,7 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
   a.flags = nullptr;
   a.epoch = 0;
   a.err = dev->err_word;
-  if (static_cast<int64_t>(a.m_tiles) * a.n_tiles * a.splits > (1 << 30)) return SP24_ERR_UNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (bt.L * a.m_tiles * a.n_tiles * a.splits > (1 << 30)) return SP24_ERR_UNSUPPORTED;
   // large token counts with plain scaling: 256 x 256 tiles on SM pairs
   if (pair_gemm_applies(M, N, K, !promote, r))
     return launch_pair_gemm(dev, Xq, ldx, Y, ldy, X2, W2, r, a, s);
@@ -790,10 +822,13 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
 
   const int bn = pl.bn;
   CUtensorMap tm_x, tm_w2, tm_x2, tm_y;
-  st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  // [L][M][K] activations and [L][M][N] outputs: a problem's tail rows read
+  // zeros and are not stored, whatever its neighbour in the batch holds
+  st = make_tmap_3d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, bt.L, ldx, bt.L > 1 ? bt.x : M * ldx, BK, bn,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == SP24_OK)
-    st = make_tmap_2d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, ldy * 2, 64, bn > 128 ? bn / 2 : bn,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    st = make_tmap_3d(&tm_y, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, bt.L, ldy * 2,
+                      (bt.L > 1 ? bt.y : M * ldy) * 2, 64, bn > 128 ? bn / 2 : bn, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st == SP24_OK && side) {
     st = make_tmap_2d(&tm_w2, W2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, N, r * 2, 64, BM,
                       CU_TENSOR_MAP_SWIZZLE_128B);
@@ -819,6 +854,50 @@ extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M,
                 : launch_bn<true, false>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
   return side ? launch_bn<false, true>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
               : launch_bn<false, false>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s);
+}
+
+}  // namespace
+}  // namespace sp24
+
+extern "C" sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx, int gM,
+                                     const void* values, const void* meta, const float* sw, int64_t N, int gN,
+                                     int gK, const void* X2, const void* W2, int64_t r, const void* bias, void* Y,
+                                     int64_t ldy, void* workspace, size_t workspace_bytes, void* stream) {
+  return sp24::gemm_impl(Xq, sx, M, K, ldx, gM, values, meta, sw, N, gN, gK, X2, W2, r, bias, Y, ldy, sp24::Batch{},
+                         workspace, workspace_bytes, stream);
+}
+
+extern "C" sp24_status sp24_fp8_gemm_batched(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
+                                             int gM, const void* values, const void* meta, const float* sw, int64_t N,
+                                             int gN, int gK, const void* bias, void* Y, int64_t ldy, int64_t L,
+                                             int64_t stride_x, int64_t stride_sx, int64_t stride_values,
+                                             int64_t stride_meta, int64_t stride_sw, int64_t stride_bias,
+                                             int64_t stride_y, void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+  using namespace sp24;
+  if (L < 1 || L > (1 << 20)) return SP24_ERR_INVALID_ARG;
+  if (M < 1 || N < 128 || K < 128 || ldx < K || ldy < N) return SP24_ERR_INVALID_ARG;
+  if (gK != K && gK != 128) return SP24_ERR_UNSUPPORTED;
+  const int64_t nsx = (K / gK) * ((M + gM - 1) / gM), nsw = (K / gK) * ((N + gN - 1) / gN);
+  if (L > 1) {
+    // problems may not overlap: each stride covers at least one problem
+    if (stride_x < M * ldx || stride_values < N * K / 2 || stride_meta < N * K / 8 || stride_sx < nsx ||
+        stride_sw < nsw || stride_y < M * ldy || (bias && stride_bias < N))
+      return SP24_ERR_INVALID_ARG;
+    if (stride_x % 16 != 0 || stride_values % 16 != 0 || stride_meta % 16 != 0 || (stride_y * 2) % 16 != 0)
+      return SP24_ERR_ALIGNMENT;
+  }
+  Batch bt;
+  bt.L = L;
+  bt.x = stride_x;
+  bt.values = stride_values;
+  bt.meta = stride_meta;
+  bt.sx = stride_sx;
+  bt.sw = stride_sw;
+  bt.bias = stride_bias;
+  bt.y = stride_y;
+  return gemm_impl(Xq, sx, M, K, ldx, gM, values, meta, sw, N, gN, gK, nullptr, nullptr, 0, bias, Y, ldy, bt,
+                   workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

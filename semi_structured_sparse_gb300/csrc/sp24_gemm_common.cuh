@@ -18,6 +18,10 @@ struct GemmArgs {
   const float* sw;
   const uint16_t* bias;  // bf16 [N] added to every output row, or null
   int M, N, K;
+  // batch (one-CTA kernel): L problems of the same shape; per-problem
+  // offsets of the weight storage (bytes), scales (floats) and bias (values)
+  int L;
+  int64_t bs_values, bs_meta, bs_sx, bs_sw, bs_bias;
   int ldsx, ldsw;          // row strides (floats) of the scale tensors
   int gM_shift, gN_shift;  // log2 of the granularities (0 or 7)
   int m_tiles, n_tiles, k_tiles;

@@ -33,6 +33,10 @@ sp24_status current_device(const DeviceInfo** out);
 // 2D tensor map over a row-major [rows][cols] array of `elem_bytes`-sized
 // elements with row stride `row_stride_bytes`; box {box_cols, box_rows};
 // out-of-range elements read as zero.
+// 3D: [depth][rows][cols] with row and depth strides in bytes (a batch of 2D views).
+sp24_status make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t cols, uint64_t rows,
+                         uint64_t depth, uint64_t row_stride_bytes, uint64_t depth_stride_bytes, uint32_t box_cols,
+                         uint32_t box_rows, CUtensorMapSwizzle swizzle);
 sp24_status make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t cols,
                          uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
                          CUtensorMapSwizzle swizzle);

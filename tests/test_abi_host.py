@@ -128,6 +128,21 @@ def test_decompress_argument_errors(lib):
     assert f(FAKE, FAKE, FAKE, 128, 256, 1, 256, FAKE_ODD, 256, None) == 3
 
 
+def test_gemm_batched_argument_errors(lib):
+    f = lib.sp24_fp8_gemm_batched
+
+    def call(L=2, sxq=64 * 512, sv=256 * 256, sm=256 * 64, ssx=64, ssw=256, sb=0, sy=64 * 256, bias=None):
+        return f(FAKE, FAKE, 64, 512, 512, 1, FAKE, FAKE, FAKE, 256, 1, 512, bias, FAKE, 256, L,
+                 sxq, ssx, sv, sm, ssw, sb, sy, None, 0, None)
+
+    assert call(L=0) == 1
+    assert call(sxq=64 * 512 - 16) == 1   # problems overlap
+    assert call(sv=100) == 1
+    assert call(bias=FAKE, sb=100) == 1   # bias rows overlap
+    assert call(sxq=64 * 512 + 8) == 3    # not a 16-byte multiple
+    assert call(sy=64 * 256 + 4) == 3
+
+
 def test_workspace_size(lib):
     assert lib.sp24_fp8_gemm_workspace_size(2048, 4096, 4096, 0) >= 0
 

@@ -334,3 +334,41 @@ def test_split_k_without_workspace_runs_unsplit(ora, sp24):
     torch.cuda.synchronize()
     sp24.last_device_error()
     assert_close(bf16_to_f64(y), ora.gemm(xq, sx, values, meta, sw), "unsplit fallback")
+
+
+@pytest.mark.parametrize("L,M,N,K,gN,gK,with_bias", [
+    (3, 16, 512, 512, 1, None, False),     # decode-size problems: one launch over all of them
+    (4, 40, 384, 512, 128, 128, True),     # group-wise promotion, ragged token tails
+    (2, 100, 1024, 1024, 1, None, True),   # few tiles: K split across CTAs, per problem
+    (3, 300, 512, 512, 1, None, True),     # SM-pair problems: one launch each
+    (2, 200, 512, 768, 128, 128, False),   # SM-pair group-wise problems
+])
+def test_gemm_batched(ora, sp24, L, M, N, K, gN, gK, with_bias):
+    """L independent problems of one shape (CUTLASS's batched L mode): each
+    output equals the oracle on that problem's own operands.  The activations
+    come from a taller buffer, so consecutive problems are not adjacent."""
+    gk = K if gK is None else gK
+    probs = []
+    for l in range(L):
+        w = inputs.Workload("batch", M, N, K, gN=gN, gK=gK, seed=100 * l + M + N)
+        probs.append((w,) + _prep(ora, w))
+    pad = 8
+    xq_big = torch.zeros((L, M + pad, K), dtype=torch.uint8)
+    for l, p in enumerate(probs):
+        xq_big[l, :M] = torch.from_numpy(p[1])
+    xq = xq_big.cuda()[:, :M]
+    sx = torch.stack([torch.from_numpy(p[2]) for p in probs]).cuda()
+    tiled = [_abi(ora, p[3], p[4]) for p in probs]
+    values = torch.stack([torch.from_numpy(t[0]) for t in tiled]).cuda()
+    meta = torch.stack([torch.from_numpy(t[1]) for t in tiled]).cuda()
+    sw = torch.stack([torch.from_numpy(p[5]) for p in probs]).cuda()
+    rng = np.random.default_rng(L + M)
+    bias_bits = [inputs.bf16_bits(torch.from_numpy(rng.normal(0, 0.5, N).astype(np.float32)).to(torch.bfloat16))
+                 for _ in range(L)]
+    bias = torch.stack([dev(b) for b in bias_bits]) if with_bias else None
+    y = sp24.gemm_batched(xq, sx, values, meta, sw, 1, gN, gk, bias=bias)
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+    for l, p in enumerate(probs):
+        ref = ora.gemm(p[1], p[2], p[3], p[4], p[5], 1, gN, gk, bias=bias_bits[l] if with_bias else None)
+        assert_close(bf16_to_f64(y[l]), ref, "batched L=%d problem %d" % (L, l))
