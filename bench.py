@@ -70,8 +70,9 @@ def captured_traffic(workload, M, kernel):
 # ---------------------------------------------------------------- utilities
 def next_rows(sp24, w, gk, sets, stream, ws, steps, pk):
     """The kernels beyond the timed step, each alone, K launches back to back
-    over the rotating sets between one event pair: the GEMM with a bf16 bias,
-    the activation quantization from bf16, and the GPU dequantize."""
+    (one CUDA graph) over the rotating sets between one event pair: the GEMM
+    with a bf16 bias, a batch of 4 problems, the activation quantization from
+    bf16, and the GPU dequantize."""
     n = max(steps, 3)
     bias = [torch.randn(w.N, device=s["y"].device).to(torch.bfloat16) for s in sets]
     xb = [torch.randn(w.M, w.K, device=s["y"].device).to(torch.bfloat16) for s in sets]
@@ -82,10 +83,19 @@ def next_rows(sp24, w, gk, sets, stream, ws, steps, pk):
         for i in range(3):
             fn(i % len(sets))
         torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()  # n launches replayed back to back, as the step is
+        cs = torch.cuda.Stream(stream.device)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                for i in range(n):
+                    fn(i % len(sets))
+        stream.wait_stream(cs)
+        g.replay()
+        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for i in range(n):
-            fn(i % len(sets))
+        g.replay()
         b.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b) / n
@@ -96,13 +106,31 @@ def next_rows(sp24, w, gk, sets, stream, ws, steps, pk):
                   workspace=ws, bias=bias[i])
 
     t_bias = timed(gemm_bias)
+    # a batch of 4 problems of this shape (no side GEMM), stacked
+    L = 4
+    s0 = sets[0]
+    bx = s0["xq"].unsqueeze(0).repeat(L, 1, 1)
+    bsx = s0["sx"].unsqueeze(0).repeat(L, 1, 1)
+    bv = s0["v"].unsqueeze(0).repeat(L, 1, 1)
+    bm = s0["m"].unsqueeze(0).repeat(L, 1, 1)
+    bsw = s0["sw"].unsqueeze(0).repeat(L, 1, 1)
+    by = torch.empty((L, w.M, w.N), dtype=torch.bfloat16, device=bx.device)
+    bws = torch.empty(max(16, L * sp24.workspace_size(w.M, w.N, w.K)), dtype=torch.uint8, device=bx.device)
+    t_batch = timed(lambda i: sp24.gemm_batched(bx, bsx, bv, bm, bsw, w.gM, w.gN, gk, out=by, workspace=bws))
+    one = (bx[0], bsx[0], bv[0], bm[0], bsw[0], by[0])
+    t_one = timed(lambda i: sp24.gemm(one[0], one[1], one[2], one[3], one[4], w.gM, w.gN, gk, out=one[5],
+                                      workspace=ws))
     t_q = timed(lambda i: sp24.quantize_act(xb[i], gk, out=qx[i]))
     t_d = timed(lambda i: sp24.decompress(sets[i]["v"], sets[i]["m"], sets[i]["sw"], w.gN, gk, out=dq[i]))
     sp24.last_device_error()
     q_bytes = w.M * w.K * 2 + w.M * w.K + 4 * (w.K // gk) * w.M
     d_bytes = w.N * w.K // 2 + w.N * w.K // 8 + 4 * (w.K // gk) * ((w.N + w.gN - 1) // w.gN) + 2 * w.N * w.K
     hbm = pk["hbm_gbs"]
+    batch_bytes = L * (w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.K + 2 * w.M * w.N)
     return {
+        "gemm_batched": {"L": L, "ms": round(t_batch, 5), "ms_one_problem": round(t_one, 5),
+                         "tflops_dense_equiv": round(L * 2 * w.M * w.N * w.K / (t_batch * 1e-3) / 1e12, 1),
+                         "gbs_operands": round(batch_bytes / (t_batch * 1e-3) / 1e9, 1)},
         "gemm_with_bias": {"ms": round(t_bias, 5),
                            "tflops_dense_equiv": round(w.dense_flops() / (t_bias * 1e-3) / 1e12, 1)},
         "quantize_act_bf16": {"ms": round(t_q, 5), "gbs": round(q_bytes / (t_q * 1e-3) / 1e9, 1),
@@ -238,25 +266,53 @@ def run_ours(args):
     torch.cuda.synchronize()
     sp24.last_device_error()
 
+    def capture(fn):
+        """A CUDA graph of fn()'s launches: replayed, the kernels run back to back
+        with their programmatic-launch edges, without the host in between."""
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                fn()
+        stream.wait_stream(cs)
+        torch.cuda.synchronize()
+        return g
+
+    def compress_only(s):
+        sp24.compress(s["W"], w.gN, gk, out=(s["v"], s["m"], s["sw"]))
+
+    def gemm_only(s):
+        sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"],
+                  workspace=ws)
+
+    g_steps = capture(lambda: [step(sets[i % nsets]) for i in range(args.steps)])
+    g_comp = capture(lambda: [compress_only(sets[i % nsets]) for i in range(args.steps)])
+    g_gemm = capture(lambda: [gemm_only(sets[i % nsets]) for i in range(args.steps)])
+    for g in (g_steps, g_comp, g_gemm):  # warm replays, untimed
+        g.replay()
+    torch.cuda.synchronize()
+    sp24.last_device_error()
+
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         # keep the GPU busy ~1 s so the clock samples see it under load, untimed
         t_end = time.time() + (0.0 if args.quick else 1.0)
         i = 0
         while time.time() < t_end:
-            step(sets[i % nsets])
+            g_steps.replay()
             i += 1
-            if i % 64 == 0:
+            if i % 8 == 0:
                 torch.cuda.synchronize()
         if pg:
             pg.barrier()
         torch.cuda.synchronize()
-        # the timed region: K whole steps back to back, nothing between the
-        # kernels (an event between two launches would stop the next kernel's
-        # prologue from overlapping the previous kernel's tail)
+        # the timed region: K whole steps back to back, replayed from a CUDA
+        # graph, nothing between the kernels (an event between two launches
+        # would stop the next kernel's prologue from overlapping the previous
+        # kernel's tail)
         start.record(stream)
-        for i in range(args.steps):
-            step(sets[i % nsets])
+        g_steps.replay()
         stop.record(stream)
         torch.cuda.synchronize()
         if pg:
@@ -267,14 +323,9 @@ def run_ours(args):
         # every launch would also time the launch gap it creates)
         kev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         kev[0].record(stream)
-        for i in range(args.steps):
-            s = sets[i % nsets]
-            sp24.compress(s["W"], w.gN, gk, out=(s["v"], s["m"], s["sw"]))
+        g_comp.replay()
         kev[1].record(stream)
-        for i in range(args.steps):
-            s = sets[i % nsets]
-            sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"],
-                      workspace=ws)
+        g_gemm.replay()
         kev[2].record(stream)
         torch.cuda.synchronize()
     sp24.last_device_error()
@@ -402,8 +453,9 @@ def run_ours(args):
                    "step": "compress(W) + sparse GEMM", "flops_per_step": "2*M*N*K dense-equivalent",
                    "l2": "rotating %d input sets of %.1f MB (> L2 %.0f MB)" % (nsets, set_bytes / 1e6, l2 / 1e6),
                    "parallelism": "replicas" if world > 1 else "single",
-                   "timing": "value: K back-to-back steps between one event pair; kernels/roofline: each kernel "
-                             "alone, K back-to-back launches over the same rotating sets between one event pair"},
+                   "timing": "value: K back-to-back steps replayed from one CUDA graph between one event pair; "
+                             "kernels/roofline: each kernel alone, a graph of K launches over the same rotating "
+                             "sets between one event pair; e2e: eager calls through the public API"},
         "kernels": {
             "gemm": {"ms": round(t_gemm, 5), "tflops_dense_equiv": round(gemm_tflops_dense, 1),
                      "frac_fp8_sparse_peak": round(gemm_tflops_alg / fp8_dense_peak, 4)},

@@ -178,7 +178,9 @@ SP24_API sp24_status sp24_fp8_quantize_act_bf16(const void* X, int64_t M, int64_
  *           range is split across CTAs (when the tiles alone would leave SMs
  *           idle in the last wave) and one flag per split; it needs no
  *           clearing, but calls that overlap on the GPU must not share it.
- *           With less than the queried size the call runs unsplit.
+ *           With less than the queried size the call runs unsplit, and so
+ *           does a call made while its stream is being captured into a CUDA
+ *           graph (the split's per-launch epoch is taken on the host).
  * Preconditions: M >= 1; N a positive multiple of 128; K a positive multiple
  * of 128; all scales finite and > 0; device pointers 16-byte aligned.
  * Errors: SP24_ERR_* as above; device-side wait timeouts are reported by

@@ -781,6 +781,11 @@ sp24_status gemm_impl(const void* Xq, const float* sx, int64_t M, int64_t K, int
   Plan pl = make_plan(M, N, K, promote, side, dev->sm_count);
   pl.ws_partials *= bt.L;  // split-K partials and flags of every problem
   pl.ws_bytes *= bt.L;
+  // Split K publishes partials under a per-launch epoch taken on the host; a
+  // captured graph would replay one epoch forever, so captured calls run unsplit.
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (pl.splits > 1 && cudaStreamIsCapturing(s, &capture) == cudaSuccess && capture != cudaStreamCaptureStatusNone)
+    pl.splits = 1;
   if (pl.splits > 1 && (workspace == nullptr || workspace_bytes < pl.ws_bytes || !aligned16(workspace))) {
     pl.splits = 1;  // no (or too small a) workspace: run unsplit
   }
