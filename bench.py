@@ -115,7 +115,7 @@ def next_rows(sp24, w, gk, sets, stream, ws, steps, pk):
     bm = s0["m"].unsqueeze(0).repeat(L, 1, 1)
     bsw = s0["sw"].unsqueeze(0).repeat(L, 1, 1)
     by = torch.empty((L, w.M, w.N), dtype=torch.bfloat16, device=bx.device)
-    bws = torch.empty(max(16, L * sp24.workspace_size(w.M, w.N, w.K)), dtype=torch.uint8, device=bx.device)
+    bws = torch.zeros(max(16, L * sp24.workspace_size(w.M, w.N, w.K)), dtype=torch.uint8, device=bx.device)
     t_batch = timed(lambda i: sp24.gemm_batched(bx, bsx, bv, bm, bsw, w.gM, w.gN, gk, out=by, workspace=bws))
     one = (bx[0], bsx[0], bv[0], bm[0], bsw[0], by[0])
     t_one = timed(lambda i: sp24.gemm(one[0], one[1], one[2], one[3], one[4], w.gM, w.gN, gk, out=one[5],
@@ -254,7 +254,7 @@ def run_ours(args):
         sets.append(s)
     stream = torch.cuda.current_stream()
     ws_bytes = sp24.workspace_size(w.M, w.N, w.K, w.r)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def step(s):
         sp24.compress(s["W"], w.gN, gk, out=(s["v"], s["m"], s["sw"]))

@@ -173,14 +173,20 @@ SP24_API sp24_status sp24_fp8_quantize_act_bf16(const void* X, int64_t M, int64_
  *   Y       (device, out) bf16 [M][N], row stride ldy >= N, ldy % 8 == 0,
  *           16-byte aligned.
  *   workspace, workspace_bytes: device scratch of at least
- *           sp24_fp8_gemm_workspace_size(M, N, K, r) bytes (may be NULL when
- *           that size is 0).  It holds the fp32 partial sums of tiles whose K
- *           range is split across CTAs (when the tiles alone would leave SMs
- *           idle in the last wave) and one flag per split; it needs no
- *           clearing, but calls that overlap on the GPU must not share it.
- *           With less than the queried size the call runs unsplit, and so
- *           does a call made while its stream is being captured into a CUDA
- *           graph (the split's per-launch epoch is taken on the host).
+ *           sp24_fp8_gemm_workspace_size(M, N, K, r) bytes, 16-byte aligned
+ *           (may be NULL when that size is 0).  Used when the small-token
+ *           tiles alone would leave SMs idle in the last wave: the launch
+ *           then deals the (tile, K block) work out to one CTA per SM in
+ *           equal contiguous ranges (stream-K), and a tile cut between CTAs
+ *           is finished by the CTA holding its first K blocks, which adds the
+ *           others' fp32 partials in a fixed order (the result does not
+ *           depend on timing).  The workspace holds a launch counter, one
+ *           flag per CTA and one partial tile per CTA.  Zero it once before
+ *           its first use; each launch leaves it consistent for the next,
+ *           whatever the shape, CUDA graph replays included (after a
+ *           device error reported by sp24_last_device_error, zero it again).
+ *           Calls that overlap on the GPU must not share it.  With less than the
+ *           queried size the call runs with whole tiles per CTA.
  * Preconditions: M >= 1; N a positive multiple of 128; K a positive multiple
  * of 128; all scales finite and > 0; device pointers 16-byte aligned.
  * Errors: SP24_ERR_* as above; device-side wait timeouts are reported by
@@ -203,7 +209,8 @@ SP24_API sp24_status sp24_fp8_gemm(const void* Xq, const float* sx, int64_t M, i
  *   stride_sx, stride_sw, stride_bias, stride_y: elements between problems
  *           (fp32, fp32, bf16, bf16; stride_y*2 a multiple of 16).
  *   workspace: L times the single problem's sp24_fp8_gemm_workspace_size
- *           for split K (less: the problems run unsplit).
+ *           for stream-K, zeroed before its first use as for sp24_fp8_gemm
+ *           (less: whole tiles per CTA).
  * Problems small enough to leave SMs idle run in one launch whose persistent
  * CTAs take work units from every problem; problems that fill the GPU on
  * their own (the SM-pair cases) run as back-to-back launches.
@@ -223,7 +230,7 @@ SP24_API sp24_status sp24_fp8_gemm_batched(const void* Xq, const float* sx, int6
  * they run (serving loops that plan every buffer at start-up, code hosted in
  * a framework whose allocator this library cannot reach).  This call takes
  * the same arguments as sp24_fp8_gemm minus the workspace and computes the
- * same result; the split-K scratch comes from a fixed 4 MiB array inside the
+ * same result; the stream-K scratch comes from a fixed 8 MiB array inside the
  * library's device image instead.  It calls no allocating routine.
  *   - Every GPU that loads the library holds that array until the process
  *     exits, and all calls on a device share it: calls that overlap on the
@@ -233,10 +240,10 @@ SP24_API sp24_status sp24_fp8_gemm_batched(const void* Xq, const float* sx, int6
  *     one-time set-up with that device current); make that first call before
  *     any stream capture.
  *   - A shape whose scratch need (sp24_fp8_gemm_workspace_size) exceeds
- *     4 MiB is refused with SP24_ERR_WORKSPACE; shapes that need no scratch
- *     always run.
- * Nothing in the scratch needs clearing between calls: the split flags carry
- * a per-launch epoch, and the partial sums are overwritten.
+ *     8 MiB is refused with SP24_ERR_WORKSPACE (none does on a 152-SM part);
+ *     shapes that need no scratch always run.
+ * The array starts zeroed, and the stream-K counter and flags keep it
+ * consistent from call to call.
  */
 SP24_API sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
                                                  int gM, const void* values, const void* meta, const float* sw,
@@ -245,6 +252,26 @@ SP24_API sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* sx
 
 /* Device scratch bytes sp24_fp8_gemm needs for this problem (0 = none). */
 SP24_API size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r);
+
+/*
+ * sp24_set_decomposition -- how later GEMM calls of this process deal out
+ * the tiles' K ranges (CUTLASS's stream-K decomposition modes, [2095]'s
+ * kernel schedules).  Process-wide; sp24_fp8_gemm_workspace_size answers for
+ * the mode in force, so query it after setting the mode.
+ *   SP24_DECOMP_HEURISTIC     (default) stream-K where the library's cost
+ *                             model expects it to be faster: few weight
+ *                             tiles with long K ranges;
+ *   SP24_DECOMP_DATA_PARALLEL whole tiles only (no workspace needed);
+ *   SP24_DECOMP_STREAM_K      stream-K wherever it applies.
+ * Stream-K applies to per-tensor-K scaling without a side GEMM and at most
+ * 64 tokens (the one-SM kernel's small-token tiles), when a tile's K range
+ * spans at least two pipeline stages (a stage holds up to four 128-wide K
+ * blocks for up to 32 tokens, two above); other calls ignore the mode.  Results are the same within rounding (each mode has a
+ * fixed summation order, so each is deterministic).
+ * Errors: SP24_ERR_INVALID_ARG for an unknown mode.
+ */
+enum { SP24_DECOMP_HEURISTIC = 0, SP24_DECOMP_DATA_PARALLEL = 1, SP24_DECOMP_STREAM_K = 2 };
+SP24_API sp24_status sp24_set_decomposition(int mode);
 
 /*
  * sp24_last_device_error -- synchronise `stream`, then read and clear the

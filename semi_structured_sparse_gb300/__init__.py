@@ -9,6 +9,7 @@ is not an sm_103 GPU, every call raises.
     xq, sx          = quantize_act(x_fp32, gK=None)            # per-token / 1x128 e4m3
     y               = gemm(xq, sx, values, meta, sw, gM=1, gN=1, gK=None, x2=None, w2=None)
 """
+import contextlib
 import ctypes
 import os
 
@@ -36,6 +37,7 @@ SIGNATURES = {
     "sp24_fp8_gemm": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P, _I64,
                        _P, _SZ, _P], _I),
     "sp24_fp8_gemm_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
+    "sp24_set_decomposition": ([_I], _I),
     "sp24_fp8_gemm_batched": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _I64,
                                _I64, _I64, _I64, _I64, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "sp24_fp8_gemm_fixed_scratch": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P,
@@ -104,6 +106,27 @@ def workspace_size(M: int, N: int, K: int, r: int = 0) -> int:
     return int(load().sp24_fp8_gemm_workspace_size(M, N, K, r))
 
 
+DECOMP_HEURISTIC, DECOMP_DATA_PARALLEL, DECOMP_STREAM_K = 0, 1, 2
+
+
+def set_decomposition(mode: int) -> None:
+    """How later GEMM calls deal out the tiles' K ranges: DECOMP_HEURISTIC
+    (default), DECOMP_DATA_PARALLEL (whole tiles) or DECOMP_STREAM_K
+    (process-wide; workspace_size() follows the mode)."""
+    _check(load().sp24_set_decomposition(int(mode)), "sp24_set_decomposition")
+
+
+@contextlib.contextmanager
+def decomposition(mode: int):
+    """Run a block of GEMM calls under one decomposition mode, then restore
+    the heuristic."""
+    set_decomposition(mode)
+    try:
+        yield
+    finally:
+        set_decomposition(DECOMP_HEURISTIC)
+
+
 def meta_bytes(N: int, K: int) -> int:
     return int(load().sp24_meta_bytes(N, K))
 
@@ -168,7 +191,9 @@ def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None, x2=
          out=None, workspace=None, stream=None, bias=None):
     """Y[M, N] (bf16) = scaled 2:4 sparse e4m3 GEMM of xq [M, K] with the packed weight
     (values [N, K/2], meta [N, K/8]) plus x2 [M, r] . w2 [N, r]^T and a bf16 bias [N]
-    when given."""
+    when given.  `workspace` (uint8, at least workspace_size(M, N, K, r) bytes) must be
+    zeroed before its first use and may then be reused by later calls of any shape on
+    the same stream; without one, each call that needs scratch allocates a zeroed one."""
     lib = load()
     _dev_tensor(xq, torch.uint8, "xq")
     _dev_tensor(values, torch.uint8, "values")
@@ -194,7 +219,7 @@ def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None, x2=
     y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if out is None else out
     ws_bytes = int(lib.sp24_fp8_gemm_workspace_size(M, N, K, r))
     if ws_bytes and workspace is None:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=xq.device)
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=xq.device)
     _check(lib.sp24_fp8_gemm(_ptr(xq), _ptr(sx), M, K, xq.stride(0), gM, _ptr(values), _ptr(meta), _ptr(sw), N,
                              gN, gK, _ptr(x2), _ptr(w2), r, _ptr(bias), _ptr(y), y.stride(0), _ptr(workspace),
                              0 if workspace is None else workspace.numel() * workspace.element_size(),
@@ -223,7 +248,7 @@ def gemm_batched(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = N
     y = torch.empty((L, M, N), dtype=torch.bfloat16, device=xq.device) if out is None else out
     ws_bytes = L * int(lib.sp24_fp8_gemm_workspace_size(M, N, K, 0))
     if ws_bytes and workspace is None:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=xq.device)
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=xq.device)
     _check(lib.sp24_fp8_gemm_batched(
         _ptr(xq), _ptr(sx), M, K, xq.stride(1), gM, _ptr(values), _ptr(meta), _ptr(sw), N, gN, gK, _ptr(bias),
         _ptr(y), y.stride(1), L, xq.stride(0), sx.stride(0), values.stride(0), meta.stride(0), sw.stride(0),

@@ -71,26 +71,69 @@ struct Cfg {
   static_assert(COLS % 8 == 0, "epilogue chunking");
   static_assert(BN <= 128 || (!PROMOTE && !SIDE), "256-token tiles: plain per-tensor-K scaling only");
   static_assert(!PROMOTE || (BN <= 128 && KS <= 2), "a scale slot holds BN + 128 floats per K block");
-  static_assert(!SPLIT || (!PROMOTE && !SIDE && BN <= 128), "split-K: plain per-tensor-K scaling only");
+  static_assert(!SPLIT || (!PROMOTE && !SIDE && BN <= 128), "stream-K: plain per-tensor-K scaling only");
 };
 
-// Work schedule: a unit is (token tile, weight tile, K split); units are
-// numbered weight tile fastest, then split, then token tile, then problem of
-// the batch, and dealt to the persistent CTAs round-robin.
+// Work schedule.  A tile is (problem of the batch, token tile, weight tile),
+// numbered weight tile fastest.  Without stream-K the persistent CTAs take
+// whole tiles round-robin.  With stream-K (SPLIT) the S stages of all tiles'
+// stage sequences are dealt out to the C CTAs in contiguous ranges, the
+// first S mod C CTAs taking one stage more than the rest, and each range is
+// cut where the tile changes: a piece that starts at a tile's first stage
+// completes that tile (adding the partials of the CTAs that hold its later
+// stages, which start their ranges with them); any other piece is published
+// as this CTA's partial.  The host keeps S (and the tile count) below 2^31,
+// so all of this is 32-bit arithmetic.
 struct Unit {
-  int b, m_tile, n_tile, split, kt0, kt1;
+  int b, m_tile, n_tile, kt0, kt1;
+  uint32_t tile;
+  int role;  // 0: a whole tile; 1: a tile's first stages, completes it; 2: later stages, published
 };
-__device__ __forceinline__ Unit unit_of(const GemmArgs& p, int u) {
-  Unit r;
-  r.n_tile = u % p.n_tiles;
-  const int rest = u / p.n_tiles;
-  r.split = rest % p.splits;
-  const int rest2 = rest / p.splits;
-  r.m_tile = rest2 % p.m_tiles;
-  r.b = rest2 / p.m_tiles;
-  r.kt0 = r.split * p.kt_per_split;
-  r.kt1 = min(r.kt0 + p.kt_per_split, p.k_tiles);
-  return r;
+struct WorkIter {
+  uint32_t pos, end;
+};
+template <bool STREAMK>
+__device__ __forceinline__ WorkIter work_begin(const GemmArgs& p) {
+  if (STREAMK) {
+    const uint32_t units = static_cast<uint32_t>(p.sk_units), q = units / gridDim.x, r = units % gridDim.x;
+    const uint32_t c = blockIdx.x;
+    const uint32_t begin = c * q + (c < r ? c : r);
+    return {begin, begin + q + (c < r ? 1u : 0u)};
+  }
+  return {blockIdx.x, static_cast<uint32_t>(p.L) * static_cast<uint32_t>(p.m_tiles) * static_cast<uint32_t>(p.n_tiles)};
+}
+template <bool STREAMK, int KS>
+__device__ __forceinline__ bool work_next(const GemmArgs& p, WorkIter& w, Unit& t) {
+  if (w.pos >= w.end) return false;
+  if (STREAMK) {
+    const uint32_t kst = static_cast<uint32_t>(p.kst);
+    t.tile = w.pos / kst;
+    const uint32_t s0 = w.pos - t.tile * kst;
+    const uint32_t s1 = min(kst, s0 + (w.end - w.pos));
+    w.pos += s1 - s0;
+    t.kt0 = static_cast<int>(s0) * KS;
+    t.kt1 = min(static_cast<int>(s1) * KS, p.k_tiles);
+    t.role = (s0 == 0 && s1 == kst) ? 0 : (s0 == 0 ? 1 : 2);
+  } else {
+    t.tile = w.pos;
+    w.pos += gridDim.x;
+    t.kt0 = 0;
+    t.kt1 = p.k_tiles;
+    t.role = 0;
+  }
+  const uint32_t nt = static_cast<uint32_t>(p.n_tiles), mt = static_cast<uint32_t>(p.m_tiles);
+  const uint32_t rest = t.tile / nt;
+  t.n_tile = static_cast<int>(t.tile - rest * nt);
+  const uint32_t b = rest / mt;
+  t.m_tile = static_cast<int>(rest - b * mt);
+  t.b = static_cast<int>(b);
+  return true;
+}
+// The CTA whose stream-K range holds stage s (the inverse of work_begin).
+__device__ __forceinline__ int sk_owner(const GemmArgs& p, uint32_t s) {
+  const uint32_t units = static_cast<uint32_t>(p.sk_units), q = units / gridDim.x, r = units % gridDim.x;
+  const uint32_t big = r * (q + 1);  // stages held by the CTAs with one stage more
+  return static_cast<int>(s < big ? s / (q + 1) : r + (s - big) / q);
 }
 
 template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS>
@@ -103,6 +146,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int NACC = C::NACC;
   constexpr int COLS = C::COLS;
   constexpr int CH = COLS >= 16 ? 16 : COLS;  // columns per TMEM load
+  constexpr int SK_GRP = COLS <= 8 ? 8 : 64 / COLS;  // stream-K partials gathered ahead (64 floats)
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base by pointer arithmetic on the shared array, so that
   // accesses through it compile to shared-memory instructions
@@ -125,7 +169,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_units = p.L * p.m_tiles * p.n_tiles * p.splits;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1 + (PROMOTE ? 32 : 0));
@@ -171,8 +214,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int64_t flat = 0;  // stage index over this CTA's whole tile sequence
     uint32_t side_phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const Unit t = unit_of(p, u);
+    WorkIter work = work_begin<SPLIT>(p);
+    Unit t;
+    while (ok && work_next<SPLIT, KS>(p, work, t)) {
       const int n_tile = t.n_tile;
       const int n0 = n_tile * BM;
       const int m0 = t.m_tile * BN;
@@ -250,8 +294,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0, side_cnt = 0, meta_ctr = 0;
       uint32_t acc_cnt = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const Unit t = unit_of(p, u);
+      WorkIter work = work_begin<SPLIT>(p);
+      Unit t;
+      while (ok && work_next<SPLIT, KS>(p, work, t)) {
         uint32_t d = 0;
         if (!PROMOTE) {
           const uint32_t b = acc_cnt % NACC;
@@ -325,8 +370,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (C::OUT_TOKENS * 64) + (row & 63);
     uint32_t acc_cnt = 0, side_cnt = 0, e_stage = 0, e_phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const Unit t = unit_of(p, u);
+    // stream-K: this launch's epoch (the counter changes only after every CTA
+    // of the launch has finished; the previous launch is complete here)
+    const unsigned long long epoch = SPLIT ? (*reinterpret_cast<volatile unsigned long long*>(p.sk_word) >> 20) + 1 : 0;
+    WorkIter work = work_begin<SPLIT>(p);
+    Unit t;
+    while (ok && work_next<SPLIT, KS>(p, work, t)) {
       const int n0 = t.n_tile * BM;
       const int m0 = t.m_tile * BN;
       const int n = n0 + row;
@@ -336,6 +385,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (et < BN) {
           const int m = m0 + et;
           scl[et] = m < p.M ? __ldg(&p.sx[t.b * p.bs_sx + (m >> p.gM_shift)]) : 0.0f;
+        }
+        // stream-K, a tile's first stages: gather the other CTAs' partials
+        // while this CTA's own stages are still being loaded and multiplied.
+        // Those CTAs publish their partials at the start of their ranges, so
+        // the waits are usually already over.  One thread per partial watches
+        // its flag (the waits overlap); the first SK_GRP partials are read
+        // into registers at once, the rest (rare) after the accumulator.
+        int nparts = 0;
+        float pre[SPLIT ? SK_GRP : 1][SPLIT ? COLS : 1];
+        const float* wsp = nullptr;
+        if constexpr (SPLIT) {
+          if (t.role == 1) {
+            const int first = static_cast<int>(blockIdx.x) + 1;
+            nparts = sk_owner(p, t.tile * static_cast<uint32_t>(p.kst) + p.kst - 1) + 1 - first;
+            bool got = true;
+            for (int i = et; i < nparts; i += EPI_THREADS) {
+              const uint64_t t0 = globaltimer_ns();
+              while (ld_acquire_u64(&p.flags[first + i]) != epoch) {
+                if (globaltimer_ns() - t0 > SP24_WAIT_TIMEOUT_NS) { got = false; break; }
+              }
+            }
+            if (epilogue_bar_any(!got)) { ok = false; break; }
+            wsp = p.ws + static_cast<int64_t>(first) * (BN * BM) + c0 * BM + row;
+#pragma unroll
+            for (int g = 0; g < SK_GRP; ++g)
+              if (g < nparts) {
+#pragma unroll
+                for (int c = 0; c < COLS; ++c) pre[g][c] = __ldcg(wsp + static_cast<int64_t>(g) * (BN * BM) + c * BM);
+              }
+          }
         }
         if (!mbar_wait(&accf[b], (acc_cnt / NACC) & 1)) ok = false;
         if (SIDE && ok && !mbar_wait(saccf, side_cnt & 1)) ok = false;
@@ -375,35 +454,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           continue;
         }
         if constexpr (SPLIT) {
-          if (p.splits > 1) {
-            // unscaled fp32 partials of the K splits of a tile, [tile][split][col][row]
-            const int tile_id = (t.b * p.m_tiles + t.m_tile) * p.n_tiles + t.n_tile;
-            unsigned long long* tflags = p.flags + static_cast<int64_t>(tile_id) * p.splits;
-            if (t.split < p.splits - 1) {
-              // an earlier split: publish the partial for the tile's last split
-              float* wpart = p.ws + (static_cast<int64_t>(tile_id) * p.splits + t.split) * (BN * BM);
+          if (t.role == 2) {
+            // later stages of a tile: publish the unscaled fp32 partial in this
+            // CTA's slot, [col][row], for the CTA that holds the tile's start
+            float* wpart = p.ws + static_cast<int64_t>(blockIdx.x) * (BN * BM);
 #pragma unroll
-              for (int c = 0; c < COLS; c += CH) {
-                uint32_t v[CH];
-                tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
-                tmem_ld_wait();
+            for (int c = 0; c < COLS; c += CH) {
+              uint32_t v[CH];
+              tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
+              tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < CH; ++j) __stcg(wpart + (c0 + c + j) * BM + row, __uint_as_float(v[j]));
-              }
-              tc_fence_before();
-              __syncwarp();
-          if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
-              ++acc_cnt;
-              __threadfence();
-              epilogue_bar();
-              if (et == 0) st_release_u64(&tflags[t.split], p.epoch);
-              continue;
+              for (int j = 0; j < CH; ++j) __stcg(wpart + (c0 + c + j) * BM + row, __uint_as_float(v[j]));
             }
-            // The tile's last split completes it: its own accumulator, then the
-            // earlier splits' partials in split order (a fixed summation order,
-            // whatever the arrival order).  Units are ordered split-major within
-            // a token tile, so every earlier split was handed to a CTA no later
-            // than this one and all CTAs are resident: the waits end.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
+            ++acc_cnt;
+            // the barrier orders every thread's partial before thread 0's
+            // releasing store (cumulative at GPU scope): no per-thread fence
+            epilogue_bar();
+            if (et == 0) st_release_u64(&p.flags[blockIdx.x], epoch);
+            continue;
+          }
+          if (t.role == 1) {
+            // a tile's first stages complete it: this accumulator, then the
+            // partials of the CTAs that hold its later stages, in stage order
+            // (a fixed summation order, whatever the arrival order).  Those
+            // CTAs start their ranges with these stages and all CTAs are
+            // resident, so the waits end.
             float acc[COLS];
 #pragma unroll
             for (int c = 0; c < COLS; c += CH) {
@@ -415,21 +493,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-          if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
+            if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
             ++acc_cnt;
-            const float* wtile = p.ws + static_cast<int64_t>(tile_id) * p.splits * (BN * BM);
-            for (int sp = 0; sp < p.splits - 1; ++sp) {
-              bool got = true;
-              if (et == 0) {
-                const uint64_t t0 = globaltimer_ns();
-                while (ld_acquire_u64(&tflags[sp]) != p.epoch) {
-                  if (globaltimer_ns() - t0 > SP24_WAIT_TIMEOUT_NS) { got = false; break; }
-                }
-              }
-              if (epilogue_bar_any(!got)) { ok = false; break; }
-              const float* wsp = wtile + sp * (BN * BM) + c0 * BM + row;  // all columns of one split: COLS loads in flight
+            // add the partials in CTA order: the gathered group, then the rest
 #pragma unroll
-              for (int c = 0; c < COLS; ++c) acc[c] += __ldcg(wsp + c * BM);
+            for (int g = 0; g < SK_GRP; ++g)
+              if (g < nparts) {
+#pragma unroll
+                for (int c = 0; c < COLS; ++c) acc[c] += pre[g][c];
+              }
+            for (int i = SK_GRP; i < nparts; ++i) {
+#pragma unroll
+              for (int c = 0; c < COLS; ++c) acc[c] += __ldcg(wsp + static_cast<int64_t>(i) * (BN * BM) + c * BM);
             }
             if (!ok) break;
 #pragma unroll
@@ -468,7 +543,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-          if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
+        if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
         ++acc_cnt;
         if (SIDE) {
           __syncwarp();
@@ -558,6 +633,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   pdl_trigger();  // only teardown is left: the next kernel may begin launching
   tc_fence_before();
   __syncthreads();
+  if (SPLIT && threadIdx.x == 0) {
+    // count this CTA out (low 20 bits); the launch's last CTA starts the next
+    // epoch with a zero count.  Every CTA read the epoch before any CTA got
+    // here, so the whole launch used one epoch, and the next launch (after
+    // this one is complete) sees the next.  The counter orders no data (the
+    // next launch reads it after this grid has completed), so no fence.
+    const unsigned long long old = atomicAdd(p.sk_word, 1ull);
+    if ((old & 0xFFFFFull) == gridDim.x - 1) atomicExch(p.sk_word, ((old >> 20) + 1) << 20);
+  }
   if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
@@ -576,8 +660,10 @@ sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMa
       return SP24_ERR_CUDA;
     attr_done[dev->ordinal] = true;
   }
-  const int units = args.m_tiles * args.n_tiles * args.splits;
-  const int grid = units < dev->sm_count ? units : dev->sm_count;
+  // stream-K: one CTA per range of stages (at most one per SM); otherwise
+  // persistent CTAs over whole tiles
+  const int64_t units = SPLIT ? args.sk_units : static_cast<int64_t>(args.L) * args.m_tiles * args.n_tiles;
+  const int grid = static_cast<int>(units < dev->sm_count ? units : dev->sm_count);
   if (launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), C::SMEM, stream, x, w2, x2, y, args) != cudaSuccess)
     return SP24_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
@@ -591,7 +677,7 @@ constexpr int ks_for(int bn, bool promote) {
 template <bool PROMOTE, bool SIDE>
 sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2,
                       const CUtensorMap& x2, const CUtensorMap& y, const GemmArgs& args, cudaStream_t s) {
-  const bool split = args.splits > 1;
+  const bool split = args.sk_units > 0;
   constexpr bool PLAIN = !PROMOTE && !SIDE;
   switch (bn) {
     case 16:
@@ -651,50 +737,33 @@ int pick_bn(int64_t M, bool plain) {
   return 128;
 }
 
-// K splits for small-token shapes whose weight tiles alone leave SMs idle:
-// the smallest split count (up to 8, at least 4 K steps each) whose units
-// fill the SMs at least 5 % better than no split.  (When the tiles already
-// occupy half the SMs or more, splitting only to even out the last wave does
-// not pay: fewer SMs still pull the weights at full HBM rate.)
-int pick_splits(int tiles, int k_stages, int sm_count, bool splittable) {
-  if (!splittable || 2 * tiles >= sm_count) return 1;  // at least half the SMs busy without splitting
-  auto fill = [&](int s) {
-    const int units = tiles * s;
-    const int rounds = (units + sm_count - 1) / sm_count;
-    return static_cast<double>(units) / (static_cast<double>(rounds) * sm_count);
-  };
-  int best = 1;
-  double best_fill = fill(1);
-  for (int s = 2; s <= 8 && k_stages / s >= 4; ++s) {
-    if (fill(s) > best_fill + 0.05) {
-      best = s;
-      best_fill = fill(s);
-    }
-  }
-  return best;
-}
-
-std::atomic<unsigned long long> g_epoch{0};
-
-// A fresh 64-bit epoch per split launch: larger than the value of any flag an
-// earlier launch in this process published, and, from a clock-derived base,
-// not a plausible leftover of another process.
-unsigned long long next_epoch() {
-  unsigned long long e = g_epoch.load();
-  if (e == 0) {
-    const unsigned long long base =
-        (static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) << 8) | 1ull;
-    g_epoch.compare_exchange_strong(e, base);
-  }
-  return ++g_epoch;
-}
-
 struct Plan {
-  int bn, ks, m_tiles, n_tiles, k_tiles, splits;
-  size_t ws_partials, ws_bytes;  // partials bytes; total with the split flags (0 when not splitting)
+  int bn, ks, m_tiles, n_tiles, k_tiles;
+  bool streamk;
+  int grid;                      // stream-K: CTAs (one range each)
+  size_t ws_ctrl, ws_bytes;  // stream-K: control bytes (counter, flags); total with the partials
 };
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, bool promote, bool side, int sm_count) {
+// Bytes of the stream-K control region: the launch counter, then one flag per
+// possible CTA (at most one per SM), rounded up to 1 KiB.  It depends on the
+// device only, so every shape finds its counter and flags at the same place.
+size_t streamk_ctrl_bytes(int sm_count) {
+  return (64 + 8 * static_cast<size_t>(sm_count) + 1023) & ~size_t(1023);
+}
+
+// How the tiles' K ranges are dealt out (sp24_set_decomposition): the
+// heuristic below, whole tiles only, or stream-K wherever it applies.
+std::atomic<int> g_decomposition{SP24_DECOMP_HEURISTIC};
+
+// Stream-K applies to the HBM-bound small-token tiles (plain scaling, BN <= 64,
+// at least two stages per tile).  The heuristic takes it when balancing the
+// weight stream saves more than it costs.  With whole tiles the busiest CTA
+// streams `rounds` tiles' weights at the rate one SM sustains alone (about
+// 80 GB/s measured on the 152-SM part); with stream-K all SMs stream the
+// weights at the HBM rate (about 6.5 TB/s), but publishing and gathering the
+// partials lengthens the launch by about 3.5 us.  (The activations are read
+// from L2 by every tile and count in neither.)
+Plan make_plan(int64_t M, int64_t N, int64_t K, bool promote, bool side, int sm_count, int64_t L) {
   Plan pl;
   pl.bn = pick_bn(M, !promote && !side);
   pl.m_tiles = static_cast<int>((M + pl.bn - 1) / pl.bn);
@@ -702,10 +771,28 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bool promote, bool side, int sm_
   pl.k_tiles = static_cast<int>(K / BK);
   pl.ks = ks_for(pl.bn, promote);
   while (pl.ks > 1 && pl.k_tiles % pl.ks != 0) pl.ks /= 2;  // stages hold whole sub-tile groups
-  pl.splits = pick_splits(pl.m_tiles * pl.n_tiles, pl.k_tiles / pl.ks, sm_count, !promote && !side && pl.bn <= 64);
-  const size_t tiles = static_cast<size_t>(pl.m_tiles) * pl.n_tiles;
-  pl.ws_partials = pl.splits > 1 ? tiles * pl.splits * pl.bn * BM * sizeof(float) : 0;
-  pl.ws_bytes = pl.splits > 1 ? pl.ws_partials + tiles * pl.splits * sizeof(unsigned long long) : 0;
+  const int64_t tiles = L * pl.m_tiles * pl.n_tiles;
+  const int64_t kst = pl.k_tiles / pl.ks;
+  pl.streamk = false;
+  pl.grid = 0;
+  pl.ws_ctrl = pl.ws_bytes = 0;
+  const int mode = g_decomposition.load(std::memory_order_relaxed);
+  if (!promote && !side && pl.bn <= 64 && kst >= 2 && sm_count > 0 && mode != SP24_DECOMP_DATA_PARALLEL) {
+    if (mode == SP24_DECOMP_STREAM_K) {
+      pl.streamk = true;
+    } else if (kst >= 4) {
+      const double rounds = static_cast<double>((tiles + sm_count - 1) / sm_count);
+      const double tile_bytes = static_cast<double>(pl.k_tiles) * (BM * BK / 2 + BM * BK / 8);
+      const double t_whole_us = rounds * tile_bytes / 80e3;
+      const double t_streamk_us = static_cast<double>(tiles) * tile_bytes / 6.5e6;
+      pl.streamk = t_whole_us - t_streamk_us > 3.5;
+    }
+  }
+  if (pl.streamk) {
+    pl.grid = static_cast<int>(std::min<int64_t>(tiles * kst, sm_count));
+    pl.ws_ctrl = streamk_ctrl_bytes(sm_count);
+    pl.ws_bytes = pl.ws_ctrl + static_cast<size_t>(pl.grid) * pl.bn * BM * sizeof(float);
+  }
   return pl;
 }
 
@@ -719,6 +806,13 @@ int current_sm_count() {
 }  // namespace
 }  // namespace sp24
 
+extern "C" sp24_status sp24_set_decomposition(int mode) {
+  if (mode != SP24_DECOMP_HEURISTIC && mode != SP24_DECOMP_DATA_PARALLEL && mode != SP24_DECOMP_STREAM_K)
+    return SP24_ERR_INVALID_ARG;
+  sp24::g_decomposition.store(mode, std::memory_order_relaxed);
+  return SP24_OK;
+}
+
 extern "C" size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r) {
   using namespace sp24;
   if (M < 1 || N < BM || N % BM != 0 || K < BK || K % BK != 0 || r < 0) return 0;
@@ -726,7 +820,7 @@ extern "C" size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, 
   if (sms <= 0) return 0;
   // the workspace depends on the scale granularity only through promotion; size it for the
   // per-tensor-K case, which is the one that splits
-  return make_plan(M, N, K, false, r > 0, sms).ws_bytes;
+  return make_plan(M, N, K, false, r > 0, sms, 1).ws_bytes;
 }
 
 namespace sp24 {
@@ -778,17 +872,9 @@ sp24_status gemm_impl(const void* Xq, const float* sx, int64_t M, int64_t K, int
     }
     return SP24_OK;
   }
-  Plan pl = make_plan(M, N, K, promote, side, dev->sm_count);
-  pl.ws_partials *= bt.L;  // split-K partials and flags of every problem
-  pl.ws_bytes *= bt.L;
-  // Split K publishes partials under a per-launch epoch taken on the host; a
-  // captured graph would replay one epoch forever, so captured calls run unsplit.
-  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
-  if (pl.splits > 1 && cudaStreamIsCapturing(s, &capture) == cudaSuccess && capture != cudaStreamCaptureStatusNone)
-    pl.splits = 1;
-  if (pl.splits > 1 && (workspace == nullptr || workspace_bytes < pl.ws_bytes || !aligned16(workspace))) {
-    pl.splits = 1;  // no (or too small a) workspace: run unsplit
-  }
+  Plan pl = make_plan(M, N, K, promote, side, dev->sm_count, bt.L);
+  if (pl.streamk && (workspace == nullptr || workspace_bytes < pl.ws_bytes || !aligned16(workspace)))
+    pl.streamk = false;  // no (or too small a) workspace: whole tiles
   GemmArgs a;
   a.values = static_cast<const uint8_t*>(values);
   a.meta = static_cast<const uint8_t*>(meta);
@@ -812,13 +898,13 @@ sp24_status gemm_impl(const void* Xq, const float* sx, int64_t M, int64_t K, int
   a.n_tiles = pl.n_tiles;
   a.k_tiles = pl.k_tiles;
   a.side_ksteps = static_cast<int>(r / 16);
-  a.splits = pl.splits;
-  a.kt_per_split = ((pl.k_tiles / pl.ks + pl.splits - 1) / pl.splits) * pl.ks;
+  a.kst = pl.k_tiles / pl.ks;
+  a.sk_units = 0;
   a.ws = nullptr;
   a.flags = nullptr;
-  a.epoch = 0;
+  a.sk_word = nullptr;
   a.err = dev->err_word;
-  if (bt.L * a.m_tiles * a.n_tiles * a.splits > (1 << 30)) return SP24_ERR_UNSUPPORTED;
+  if (bt.L * a.m_tiles * a.n_tiles * a.kst >= (int64_t(1) << 31)) return SP24_ERR_UNSUPPORTED;  // 32-bit schedule
   // large token counts with plain scaling: 256 x 256 tiles on SM pairs
   if (pair_gemm_applies(M, N, K, !promote, r))
     return launch_pair_gemm(dev, Xq, ldx, Y, ldy, X2, W2, r, a, s);
@@ -846,13 +932,17 @@ sp24_status gemm_impl(const void* Xq, const float* sx, int64_t M, int64_t K, int
   }
   if (st != SP24_OK) return st;
 
-  if (pl.splits > 1) {
-    // the partials, then one 8-byte flag per (tile, split); a fresh epoch per
-    // launch makes every flag left by an earlier launch read as unpublished,
-    // so the workspace needs no clearing
-    a.ws = static_cast<float*>(workspace);
-    a.flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + pl.ws_partials);
-    a.epoch = next_epoch();
+  if (pl.streamk) {
+    // control words first, at offsets that depend on the device only: the
+    // launch counter, whose epoch advances with every launch (on the device,
+    // so graph replays advance it too), and one flag per CTA.  A flag an
+    // earlier launch left, of any shape, never reads as this launch's, so a
+    // workspace zeroed once needs no clearing between calls.  Then one
+    // partial tile per CTA.
+    a.sk_units = bt.L * a.m_tiles * a.n_tiles * static_cast<int64_t>(a.kst);
+    a.sk_word = static_cast<unsigned long long*>(workspace);
+    a.flags = a.sk_word + 8;
+    a.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_ctrl);
   }
   if (promote)
     return side ? launch_bn<true, true>(bn, pl.ks, dev, tm_x, tm_w2, tm_x2, tm_y, a, s)
@@ -911,7 +1001,7 @@ extern "C" sp24_status sp24_fp8_gemm_batched(const void* Xq, const float* sx, in
 // Some callers own their device-memory budget outright and must not allocate
 // once they are running: serving loops that plan every buffer at start-up,
 // or code hosted inside a framework whose allocator this library cannot
-// reach.  For them the split-K scratch of sp24_fp8_gemm comes from the fixed
+// reach.  For them the stream-K scratch of sp24_fp8_gemm comes from the fixed
 // array below instead of a caller-provided workspace.  The array lives in
 // this library's device image, so every GPU that loads the library holds it
 // (kFixedScratchBytes) until the process exits, and all calls on a device
@@ -919,7 +1009,7 @@ extern "C" sp24_status sp24_fp8_gemm_batched(const void* Xq, const float* sx, in
 namespace sp24 {
 namespace {
 
-constexpr size_t kFixedScratchBytes = size_t(4) << 20;  // 4 MiB per device
+constexpr size_t kFixedScratchBytes = size_t(8) << 20;  // 8 MiB per device
 static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
 
 std::mutex g_fixed_scratch_mutex;
@@ -949,13 +1039,14 @@ extern "C" sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* 
                                                    int64_t N, int gN, int gK, const void* X2, const void* W2,
                                                    int64_t r, const void* bias, void* Y, int64_t ldy, void* stream) {
   using namespace sp24;
-  // scratch this shape needs (split-K partials and their flags); more than the
+  // scratch this shape needs (stream-K partials, flags and counter); more than the
   // fixed array holds is refused rather than silently run another way
   if (sp24_fp8_gemm_workspace_size(M, N, K, r) > kFixedScratchBytes) return SP24_ERR_WORKSPACE;
   void* scratch = nullptr;
   const sp24_status st = fixed_scratch_address(&scratch);
   if (st != SP24_OK) return st;
-  // Nothing in the scratch needs clearing: split flags carry a per-launch epoch.
+  // The scratch starts zeroed (a static device array) and the stream-K
+  // control words keep it consistent from call to call.
   return sp24_fp8_gemm(Xq, sx, M, K, ldx, gM, values, meta, sw, N, gN, gK, X2, W2, r, bias, Y, ldy, scratch,
                        kFixedScratchBytes, stream);
 }

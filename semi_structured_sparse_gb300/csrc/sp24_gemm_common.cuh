@@ -26,11 +26,13 @@ struct GemmArgs {
   int gM_shift, gN_shift;  // log2 of the granularities (0 or 7)
   int m_tiles, n_tiles, k_tiles;
   int side_ksteps;  // r / 16
-  int splits;       // K splits per output tile (1 = none)
-  int kt_per_split; // 128-K sub-tiles per split (a multiple of the stage's KS)
-  float* ws;        // split-K partials [tile][split][BN][128] (fp32, unscaled)
-  unsigned long long* flags;  // split-K: [tile][split], the epoch at which that partial was published
-  unsigned long long epoch;   // this launch's epoch (split-K), larger than any earlier launch's
+  // stream-K (one-CTA kernel, SPLIT instances): the stage sequence of all
+  // tiles, tile-major, cut into one contiguous range per CTA
+  int kst;          // stages per tile
+  int64_t sk_units; // stages in all (tiles x kst)
+  float* ws;        // per CTA: one unscaled fp32 partial [BN][128]
+  unsigned long long* flags;  // per CTA: the epoch at which its partial was published
+  unsigned long long* sk_word;  // launch counter: epoch << 20 | CTAs that finished this launch
   unsigned int* err;
 };
 

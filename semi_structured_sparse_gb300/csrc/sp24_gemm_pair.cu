@@ -580,8 +580,6 @@ sp24_status launch_pair(const DeviceInfo* dev, const void* Xq, int64_t ldx, cons
   a.m_tiles = static_cast<int>((M + PN - 1) / PN);
   a.n_tiles = static_cast<int>(N / (2 * BM));
   a.k_tiles = static_cast<int>(K / BK);
-  a.splits = 1;
-  a.kt_per_split = a.k_tiles;
   a.side_ksteps = SIDE ? static_cast<int>(r / 16) : 0;
   CUtensorMap tm_x, tm_v, tm_m, tm_y, tm_w2, tm_x2;
   sp24_status st = make_tmap_2d(&tm_x, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, ldx, BK, C::HALF_N,

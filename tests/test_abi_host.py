@@ -147,6 +147,18 @@ def test_workspace_size(lib):
     assert lib.sp24_fp8_gemm_workspace_size(2048, 4096, 4096, 0) >= 0
 
 
+def test_set_decomposition_modes(lib):
+    """The three modes are accepted, anything else refused; the heuristic is
+    left in force."""
+    try:
+        for mode in (1, 2, 0):
+            assert lib.sp24_set_decomposition(mode) == 0
+        for bad in (-1, 3, 100):
+            assert lib.sp24_set_decomposition(bad) == 1  # SP24_ERR_INVALID_ARG
+    finally:
+        lib.sp24_set_decomposition(0)
+
+
 def test_product_path_has_no_cpu_fallback():
     """The binding never routes through the oracle or a CPU implementation."""
     pkg = os.path.join(ROOT, "semi_structured_sparse_gb300", "__init__.py")

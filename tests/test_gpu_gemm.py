@@ -309,18 +309,95 @@ def test_pair_tiles_deterministic(ora, sp24):
     assert torch.equal(y1, y2)
 
 
-# ------------------------------------------------------------------ split-K
-@pytest.mark.parametrize("M,N,K", [(16, 5120, 4096), (1, 5120, 4096), (64, 4096, 4096), (33, 6144, 2048)])
+# ------------------------------------------------------------------ stream-K
+@pytest.mark.parametrize("M,N,K", [(16, 5120, 4096), (1, 5120, 4096), (64, 4096, 4096), (33, 6144, 2048),
+                                   (16, 256, 2048),     # fewer work units than SMs: one per CTA
+                                   (7, 14336, 4096)])   # about six units per CTA, cut across tiles
 def test_split_k(ora, sp24, M, N, K):
-    """Few token tiles and few weight tiles: K is split across CTAs and the
-    last one to finish a tile sums the partials in a fixed order."""
+    """Stream-K forced on small-token shapes: the (tile, K block) work is dealt
+    out in equal ranges, and the CTA holding a tile's first K blocks adds the
+    other CTAs' partials in a fixed order."""
     w = inputs.Workload("sk", M, N, K, seed=M + N)
-    assert sp24.workspace_size(M, N, K) > 0, "this shape is expected to split K"
-    y, ref = _check_full(ora, sp24, w, "split-K M=%d N=%d K=%d" % (M, N, K))
-    # deterministic: same bits on a second run
-    xq, sx, values, meta, sw, _, _ = _prep(ora, w)
-    y2 = _run_gpu(sp24, w, xq, sx, values, meta, sw, None, None)
+    with sp24.decomposition(sp24.DECOMP_STREAM_K):
+        assert sp24.workspace_size(M, N, K) > 0, "this shape is expected to split K"
+        y, ref = _check_full(ora, sp24, w, "split-K M=%d N=%d K=%d" % (M, N, K))
+        # deterministic: same bits on a second run
+        xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+        y2 = _run_gpu(sp24, w, xq, sx, values, meta, sw, None, None)
     assert np.array_equal(y, y2)
+    # and whole tiles give the same values within rounding
+    with sp24.decomposition(sp24.DECOMP_DATA_PARALLEL):
+        assert sp24.workspace_size(M, N, K) == 0
+        y3 = _run_gpu(sp24, w, xq, sx, values, meta, sw, None, None)
+    assert_close(y3, ref, "whole tiles M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("M,N,K,expect", [
+    (16, 4096, 14336, True),    # few weight tiles, long K: the weight stream is balanced
+    (64, 4096, 14336, True),
+    (16, 4096, 4096, False),    # short K: the partials' exchange costs more than it saves
+    (16, 28672, 4096, False),   # enough tiles for whole rounds
+    (128, 4096, 14336, False),  # 128-token tiles: whole tiles only
+])
+def test_heuristic_decomposition(sp24, M, N, K, expect):
+    """The default mode takes stream-K only where its cost model expects a gain."""
+    assert (sp24.workspace_size(M, N, K) > 0) == expect
+
+
+def test_heuristic_streamk_shape(ora, sp24):
+    """A shape the heuristic itself splits, through the default path."""
+    M, N, K = 5, 1024, 16384
+    assert sp24.workspace_size(M, N, K) > 0
+    w = inputs.Workload("skh", M, N, K, seed=77)
+    _check_full(ora, sp24, w, "heuristic stream-K")
+
+
+def test_streamk_workspace_reuse_and_graph_replay(ora, sp24):
+    """One workspace, zeroed once, serves calls of different shapes in turn,
+    eagerly and as CUDA graph replays: the launch counter's epoch advances on
+    the device with every launch, so no flag an earlier launch left is taken
+    for a later one's.  Every replay gives the eager result's bits."""
+    shapes = [(16, 5120, 4096), (64, 4096, 2048), (7, 2560, 4096)]
+    sp24.set_decomposition(sp24.DECOMP_STREAM_K)
+    try:
+        _reuse_and_replay(ora, sp24, shapes)
+    finally:
+        sp24.set_decomposition(sp24.DECOMP_HEURISTIC)
+
+
+def _reuse_and_replay(ora, sp24, shapes):
+    ws = torch.zeros(max(sp24.workspace_size(*s) for s in shapes), dtype=torch.uint8, device="cuda")
+    cases = []
+    for i, (M, N, K) in enumerate(shapes):
+        w = inputs.Workload("skr", M, N, K, seed=40 + i)
+        xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+        tv, tm = _abi(ora, values, meta)
+        ops = [dev(t) for t in (xq, sx, tv, tm, sw)]
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        cases.append((ops, y, ora.gemm(xq, sx, values, meta, sw)))
+    first = []
+    for rep_ in range(2):
+        for i, (ops, y, ref) in enumerate(cases):
+            sp24.gemm(*ops, out=y, workspace=ws)
+            torch.cuda.synchronize()
+            sp24.last_device_error()
+            if rep_ == 0:
+                assert_close(bf16_to_f64(y), ref, "stream-K shape %d" % i)
+                first.append(y.clone())
+            else:
+                assert torch.equal(y, first[i]), "shape %d changed on reuse" % i
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for ops, y, _ in cases:
+            sp24.gemm(*ops, out=y, workspace=ws)
+    for _ in range(3):
+        for _, y, _ in cases:
+            y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        sp24.last_device_error()
+        for i, (_, y, _) in enumerate(cases):
+            assert torch.equal(y, first[i]), "graph replay of shape %d" % i
 
 
 def test_split_k_without_workspace_runs_unsplit(ora, sp24):
@@ -330,20 +407,22 @@ def test_split_k_without_workspace_runs_unsplit(ora, sp24):
     xq, sx, values, meta, sw, _, _ = _prep(ora, w)
     tv, tm = _abi(ora, values, meta)
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
-    y = sp24.gemm(dev(xq), dev(sx), dev(tv), dev(tm), dev(sw), workspace=small)
+    with sp24.decomposition(sp24.DECOMP_STREAM_K):
+        y = sp24.gemm(dev(xq), dev(sx), dev(tv), dev(tm), dev(sw), workspace=small)
     torch.cuda.synchronize()
     sp24.last_device_error()
     assert_close(bf16_to_f64(y), ora.gemm(xq, sx, values, meta, sw), "unsplit fallback")
 
 
-@pytest.mark.parametrize("L,M,N,K,gN,gK,with_bias", [
-    (3, 16, 512, 512, 1, None, False),     # decode-size problems: one launch over all of them
-    (4, 40, 384, 512, 128, 128, True),     # group-wise promotion, ragged token tails
-    (2, 100, 1024, 1024, 1, None, True),   # few tiles: K split across CTAs, per problem
-    (3, 300, 512, 512, 1, None, True),     # SM-pair problems: one launch each
-    (2, 200, 512, 768, 128, 128, False),   # SM-pair group-wise problems
+@pytest.mark.parametrize("L,M,N,K,gN,gK,with_bias,sk", [
+    (3, 16, 512, 512, 1, None, False, False),     # decode-size problems: one launch over all of them
+    (4, 40, 384, 512, 128, 128, True, False),     # group-wise promotion, ragged token tails
+    (2, 40, 1024, 2048, 1, None, True, True),     # few tiles: stream-K, each tile cut between 8 CTAs
+    (3, 16, 2560, 4096, 1, None, False, True),    # stream-K ranges that cross tiles and problems
+    (3, 300, 512, 512, 1, None, True, False),     # SM-pair problems: one launch each
+    (2, 200, 512, 768, 128, 128, False, False),   # SM-pair group-wise problems
 ])
-def test_gemm_batched(ora, sp24, L, M, N, K, gN, gK, with_bias):
+def test_gemm_batched(ora, sp24, L, M, N, K, gN, gK, with_bias, sk):
     """L independent problems of one shape (CUTLASS's batched L mode): each
     output equals the oracle on that problem's own operands.  The activations
     come from a taller buffer, so consecutive problems are not adjacent."""
@@ -366,7 +445,8 @@ def test_gemm_batched(ora, sp24, L, M, N, K, gN, gK, with_bias):
     bias_bits = [inputs.bf16_bits(torch.from_numpy(rng.normal(0, 0.5, N).astype(np.float32)).to(torch.bfloat16))
                  for _ in range(L)]
     bias = torch.stack([dev(b) for b in bias_bits]) if with_bias else None
-    y = sp24.gemm_batched(xq, sx, values, meta, sw, 1, gN, gk, bias=bias)
+    with sp24.decomposition(sp24.DECOMP_STREAM_K if sk else sp24.DECOMP_HEURISTIC):
+        y = sp24.gemm_batched(xq, sx, values, meta, sw, 1, gN, gk, bias=bias)
     torch.cuda.synchronize()
     sp24.last_device_error()
     for l, p in enumerate(probs):

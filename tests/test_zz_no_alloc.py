@@ -22,7 +22,7 @@ from gpu_util import assert_close, bf16_to_f64, dev
 
 pytestmark = pytest.mark.gpu
 
-FIXED_SCRATCH_BYTES = 4 << 20   # the array size the header documents
+FIXED_SCRATCH_BYTES = 8 << 20   # the array size the header documents
 SP24_ERR_WORKSPACE = 6
 
 
@@ -60,13 +60,21 @@ def _gemm_fixed_scratch(lib, d, M, N, K):
     return st, y
 
 
-def test_fixed_scratch_matches_workspace_entry_point(ora, sp24):
+@pytest.fixture
+def streamk(sp24):
+    """Stream-K forced, so that the small shapes below need scratch."""
+    sp24.set_decomposition(sp24.DECOMP_STREAM_K)
+    yield
+    sp24.set_decomposition(sp24.DECOMP_HEURISTIC)
+
+
+def test_fixed_scratch_matches_workspace_entry_point(ora, sp24, streamk):
     lib = sp24.load()
     M, N, K = 16, 5120, 4096          # few tiles: the GEMM splits K and needs scratch
     need = lib.sp24_fp8_gemm_workspace_size(M, N, K, 0)
     assert 0 < need <= FIXED_SCRATCH_BYTES
     d, host = _operands(ora, inputs.Workload("na", M, N, K, seed=31))
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     st, y_ref = _gemm_with_workspace(lib, d, M, N, K, ws)
     assert st == 0
     ref = bf16_to_f64(y_ref)
@@ -80,9 +88,9 @@ def test_fixed_scratch_matches_workspace_entry_point(ora, sp24):
     assert_close(ref, ora.gemm(*host), "workspace entry point vs oracle")
 
 
-def test_fixed_scratch_refuses_oversized_shapes(ora, sp24):
+def test_fixed_scratch_refuses_oversized_shapes(ora, sp24, streamk):
     lib = sp24.load()
-    M, N, K = 64, 4096, 4096          # splits K four ways on a 152-SM part: > 4 MiB of partials
+    M, N, K = 64, 4096, 4096          # the largest stream-K partials (64-token tiles)
     need = lib.sp24_fp8_gemm_workspace_size(M, N, K, 0)
     d, _ = _operands(ora, inputs.Workload("na2", M, N, K, seed=32))
     st, y = _gemm_fixed_scratch(lib, d, M, N, K)
@@ -90,7 +98,7 @@ def test_fixed_scratch_refuses_oversized_shapes(ora, sp24):
         assert st == SP24_ERR_WORKSPACE
     else:                              # another SM count may split less: then it must just work
         assert st == 0
-        ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
         st2, y_ref = _gemm_with_workspace(lib, d, M, N, K, ws)
         assert st2 == 0
         torch.cuda.synchronize()
