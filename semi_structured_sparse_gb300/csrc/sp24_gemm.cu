@@ -819,7 +819,7 @@ extern "C" size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, 
   const int sms = current_sm_count();
   if (sms <= 0) return 0;
   // the workspace depends on the scale granularity only through promotion; size it for the
-  // per-tensor-K case, which is the one that splits
+  // per-tensor-K case, which is the one that can use stream-K
   return make_plan(M, N, K, false, r > 0, sms, 1).ws_bytes;
 }
 

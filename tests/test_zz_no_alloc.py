@@ -1,7 +1,7 @@
 """sp24_fp8_gemm_fixed_scratch: the GEMM for callers that may not allocate.
 
 Such callers (serving loops with every buffer planned at start-up, code hosted
-in a framework whose allocator this library cannot reach) get the split-K
+in a framework whose allocator this library cannot reach) get the stream-K
 scratch from a fixed array inside the library instead of a workspace they pass
 in.  This file checks, through the C ABI, that two calls in a row give the same
 result as sp24_fp8_gemm with a caller workspace (within the suite's tolerance),
