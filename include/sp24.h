@@ -258,20 +258,44 @@ SP24_API size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, in
  * the tiles' K ranges (CUTLASS's stream-K decomposition modes, [2095]'s
  * kernel schedules).  Process-wide; sp24_fp8_gemm_workspace_size answers for
  * the mode in force, so query it after setting the mode.
- *   SP24_DECOMP_HEURISTIC     (default) stream-K where the library's cost
- *                             model expects it to be faster: few weight
- *                             tiles with long K ranges;
+ *   SP24_DECOMP_HEURISTIC     (default) whichever of the three below the
+ *                             library's cost model expects to be fastest;
  *   SP24_DECOMP_DATA_PARALLEL whole tiles only (no workspace needed);
- *   SP24_DECOMP_STREAM_K      stream-K wherever it applies.
- * Stream-K applies to per-tensor-K scaling without a side GEMM and at most
+ *   SP24_DECOMP_STREAM_K      stream-K wherever it applies: all tiles' K
+ *                             stages dealt out to one CTA per SM, partials
+ *                             exchanged through the workspace;
+ *   SP24_DECOMP_CLUSTER_SPLIT each tile's K range split across the CTAs of a
+ *                             thread-block cluster (4 CTAs, or 2 when 4 do
+ *                             not fit or for 33 to 64 tokens), partials
+ *                             reduced through
+ *                             distributed shared memory (no workspace), when
+ *                             every tile's cluster fits on the SMs at once.
+ * Both splits apply to per-tensor-K scaling without a side GEMM and at most
  * 64 tokens (the one-SM kernel's small-token tiles), when a tile's K range
  * spans at least two pipeline stages (a stage holds up to four 128-wide K
- * blocks for up to 32 tokens, two above); other calls ignore the mode.  Results are the same within rounding (each mode has a
- * fixed summation order, so each is deterministic).
+ * blocks for up to 32 tokens, two above); other calls ignore the mode.
+ * Results are the same within rounding (each mode has a fixed summation
+ * order, so each is deterministic).
  * Errors: SP24_ERR_INVALID_ARG for an unknown mode.
  */
-enum { SP24_DECOMP_HEURISTIC = 0, SP24_DECOMP_DATA_PARALLEL = 1, SP24_DECOMP_STREAM_K = 2 };
+enum {
+  SP24_DECOMP_HEURISTIC = 0,
+  SP24_DECOMP_DATA_PARALLEL = 1,
+  SP24_DECOMP_STREAM_K = 2,
+  SP24_DECOMP_CLUSTER_SPLIT = 3
+};
 SP24_API sp24_status sp24_set_decomposition(int mode);
+
+/*
+ * sp24_fp8_gemm_decomposition -- the decomposition a call of this shape
+ * with per-tensor-K scaling would use under the mode in force:
+ * SP24_DECOMP_DATA_PARALLEL, SP24_DECOMP_STREAM_K or
+ * SP24_DECOMP_CLUSTER_SPLIT (and, if cluster_size is not NULL, the CTAs
+ * per tile there, else 1).  Returns -1 for an invalid shape or without a
+ * usable device.  Stream-K also needs the workspace; without it the call
+ * runs whole tiles.
+ */
+SP24_API int sp24_fp8_gemm_decomposition(int64_t M, int64_t N, int64_t K, int64_t r, int* cluster_size);
 
 /*
  * sp24_last_device_error -- synchronise `stream`, then read and clear the

@@ -38,6 +38,7 @@ SIGNATURES = {
                        _P, _SZ, _P], _I),
     "sp24_fp8_gemm_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
     "sp24_set_decomposition": ([_I], _I),
+    "sp24_fp8_gemm_decomposition": ([_I64, _I64, _I64, _I64, _P], _I),
     "sp24_fp8_gemm_batched": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _I64,
                                _I64, _I64, _I64, _I64, _I64, _I64, _I64, _P, _SZ, _P], _I),
     "sp24_fp8_gemm_fixed_scratch": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P,
@@ -106,13 +107,13 @@ def workspace_size(M: int, N: int, K: int, r: int = 0) -> int:
     return int(load().sp24_fp8_gemm_workspace_size(M, N, K, r))
 
 
-DECOMP_HEURISTIC, DECOMP_DATA_PARALLEL, DECOMP_STREAM_K = 0, 1, 2
+DECOMP_HEURISTIC, DECOMP_DATA_PARALLEL, DECOMP_STREAM_K, DECOMP_CLUSTER_SPLIT = 0, 1, 2, 3
 
 
 def set_decomposition(mode: int) -> None:
     """How later GEMM calls deal out the tiles' K ranges: DECOMP_HEURISTIC
-    (default), DECOMP_DATA_PARALLEL (whole tiles) or DECOMP_STREAM_K
-    (process-wide; workspace_size() follows the mode)."""
+    (default), DECOMP_DATA_PARALLEL (whole tiles), DECOMP_STREAM_K or
+    DECOMP_CLUSTER_SPLIT (process-wide; workspace_size() follows the mode)."""
     _check(load().sp24_set_decomposition(int(mode)), "sp24_set_decomposition")
 
 
@@ -125,6 +126,15 @@ def decomposition(mode: int):
         yield
     finally:
         set_decomposition(DECOMP_HEURISTIC)
+
+
+def decomposition_of(M: int, N: int, K: int, r: int = 0):
+    """(mode, CTAs per tile) a per-tensor-K call of this shape would use now."""
+    cs = ctypes.c_int(1)
+    mode = int(load().sp24_fp8_gemm_decomposition(M, N, K, r, ctypes.addressof(cs)))
+    if mode < 0:
+        raise ValueError("invalid shape or no usable device")
+    return mode, cs.value
 
 
 def meta_bytes(N: int, K: int) -> int:

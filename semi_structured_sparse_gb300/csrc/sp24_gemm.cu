@@ -43,7 +43,7 @@ namespace {
 // of all KS (one contiguous copy), their metadata (one copy), then KS
 // activation boxes.  Small token tiles use KS > 1 so that each barrier
 // round trip and metadata copy is amortised over more MMAs.
-template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS>
+template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS, bool CSPLIT = false>
 struct Cfg {
   static constexpr int B_SUB = BN * BK;               // e4m3 activations of one sub-tile, 128 B per token row
   static constexpr int A_OFF = 0;
@@ -59,7 +59,10 @@ struct Cfg {
   static constexpr int OUT_BYTES = OUT_TOKENS * BM * 2;
   static constexpr int NACC = BN > 128 ? 1 : ((PROMOTE && !SIDE && 3 * BN <= META_COL0) ? 3 : 2);
   static constexpr int SCALE_BYTES = 4 * BN;
-  static constexpr int FIXED = 1024 + SIDE_BYTES + OUT_BYTES + SCALE_BYTES + BAR_BYTES;
+  // cluster split: the leader CTA receives its peers' fp32 partials [peer][col][row]
+  static constexpr int CS_PEERS = CSPLIT ? (BN <= 32 ? 3 : 1) : 0;
+  static constexpr int PART_BYTES = CS_PEERS * BN * BM * 4;
+  static constexpr int FIXED = 1024 + SIDE_BYTES + OUT_BYTES + SCALE_BYTES + PART_BYTES + BAR_BYTES;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE;
   static constexpr int STAGES_CAP = META_SLOTS / KS;  // metadata ring covers every sub-tile in flight
   static constexpr int STAGES = STAGES_FIT < STAGES_CAP ? STAGES_FIT : STAGES_CAP;
@@ -72,6 +75,7 @@ struct Cfg {
   static_assert(BN <= 128 || (!PROMOTE && !SIDE), "256-token tiles: plain per-tensor-K scaling only");
   static_assert(!PROMOTE || (BN <= 128 && KS <= 2), "a scale slot holds BN + 128 floats per K block");
   static_assert(!SPLIT || (!PROMOTE && !SIDE && BN <= 128), "stream-K: plain per-tensor-K scaling only");
+  static_assert(!CSPLIT || (!PROMOTE && !SIDE && !SPLIT && BN <= 64), "cluster split: plain small-token tiles only");
 };
 
 // Work schedule.  A tile is (problem of the batch, token tile, weight tile),
@@ -83,18 +87,26 @@ struct Cfg {
 // completes that tile (adding the partials of the CTAs that hold its later
 // stages, which start their ranges with them); any other piece is published
 // as this CTA's partial.  The host keeps S (and the tile count) below 2^31,
-// so all of this is 32-bit arithmetic.
+// so all of this is 32-bit arithmetic.  With a cluster split (MODE 2) each
+// cluster of C CTAs takes one tile and CTA rank r its stages
+// [r kst / C, (r + 1) kst / C); rank 0 completes the tile with the other
+// ranks' partials, which arrive in its shared memory.
 struct Unit {
   int b, m_tile, n_tile, kt0, kt1;
   uint32_t tile;
-  int role;  // 0: a whole tile; 1: a tile's first stages, completes it; 2: later stages, published
+  int role;  // 0: a whole tile; 1: a tile's first stages, completes it; 2: later stages, published;
+             // cluster split: 3 the leader's stages, completes the tile; 4 a peer's stages, sent to the leader
 };
 struct WorkIter {
   uint32_t pos, end;
 };
-template <bool STREAMK>
+template <int MODE>  // 0: whole tiles, 1: stream-K, 2: cluster split
 __device__ __forceinline__ WorkIter work_begin(const GemmArgs& p) {
-  if (STREAMK) {
+  if (MODE == 2) {
+    const uint32_t c = cluster_id_x();
+    return {c, c + 1};
+  }
+  if (MODE == 1) {
     const uint32_t units = static_cast<uint32_t>(p.sk_units), q = units / gridDim.x, r = units % gridDim.x;
     const uint32_t c = blockIdx.x;
     const uint32_t begin = c * q + (c < r ? c : r);
@@ -102,10 +114,17 @@ __device__ __forceinline__ WorkIter work_begin(const GemmArgs& p) {
   }
   return {blockIdx.x, static_cast<uint32_t>(p.L) * static_cast<uint32_t>(p.m_tiles) * static_cast<uint32_t>(p.n_tiles)};
 }
-template <bool STREAMK, int KS>
+template <int MODE, int KS>
 __device__ __forceinline__ bool work_next(const GemmArgs& p, WorkIter& w, Unit& t) {
   if (w.pos >= w.end) return false;
-  if (STREAMK) {
+  if (MODE == 2) {
+    const uint32_t kst = static_cast<uint32_t>(p.kst), r = cluster_rank(), cs = cluster_nrank();
+    t.tile = w.pos;
+    w.pos = w.end;
+    t.kt0 = static_cast<int>(r * kst / cs) * KS;
+    t.kt1 = min(static_cast<int>((r + 1) * kst / cs) * KS, p.k_tiles);
+    t.role = r == 0 ? 3 : 4;
+  } else if (MODE == 1) {
     const uint32_t kst = static_cast<uint32_t>(p.kst);
     t.tile = w.pos / kst;
     const uint32_t s0 = w.pos - t.tile * kst;
@@ -136,12 +155,13 @@ __device__ __forceinline__ int sk_owner(const GemmArgs& p, uint32_t s) {
   return static_cast<int>(s < big ? s / (q + 1) : r + (s - big) / q);
 }
 
-template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS>
+template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS, bool CSPLIT = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sp24_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w2,
                      const __grid_constant__ CUtensorMap tm_x2, const __grid_constant__ CUtensorMap tm_y,
                      const GemmArgs p) {
-  using C = Cfg<BN, PROMOTE, SIDE, SPLIT, KS>;
+  using C = Cfg<BN, PROMOTE, SIDE, SPLIT, KS, CSPLIT>;
+  constexpr int SCHED = SPLIT ? 1 : (CSPLIT ? 2 : 0);
   constexpr int STAGES = C::STAGES;
   constexpr int NACC = C::NACC;
   constexpr int COLS = C::COLS;
@@ -156,7 +176,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* side_x2 = side_w2 + BM * 128;
   uint8_t* out_tile = sm + STAGES * C::STAGE + C::SIDE_BYTES;      // [2 halves][tokens][64 channels] bf16
   float* scl = reinterpret_cast<float*>(out_tile + C::OUT_BYTES);  // per-tile token scales [BN]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(out_tile + C::OUT_BYTES + C::SCALE_BYTES);
+  float* part = reinterpret_cast<float*>(out_tile + C::OUT_BYTES + C::SCALE_BYTES);  // cluster split, leader
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_tile + C::OUT_BYTES + C::SCALE_BYTES + C::PART_BYTES);
   uint64_t* full = bars;                   // [STAGES] loads -> MMA
   uint64_t* empty = bars + MAX_STAGES;     // [STAGES] MMA (and promotion epilogue) -> loads, cluster-wide
   uint64_t* accf = bars + 2 * MAX_STAGES;  // [NACC]  MMA -> epilogue
@@ -166,7 +187,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* saccf = sidee + 1;             // side accumulator ready
   uint64_t* sacce = saccf + 1;             // side accumulator drained
   uint64_t* drain = sacce + 1;             // MMA drain on abort
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* pfull = drain + 1;             // cluster split, leader: every peer partial landed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(pfull + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -183,7 +205,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(saccf, 1);
     mbar_init(sacce, EPI_WARPS);
     mbar_init(drain, 1);
+    if (CSPLIT) mbar_init(pfull, 1);
     fence_mbar_init();
+    // the leader expects every peer's partial (st.async bytes) on pfull
+    if (CSPLIT && cluster_rank() == 0) mbar_arrive_expect_tx(pfull, (cluster_nrank() - 1) * (BN * BM * 4));
   }
   if (warp == MMA_WARP + 1 && lane == 0) {
     tma_prefetch_desc(&tm_x);
@@ -198,7 +223,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CSPLIT)
+    cluster_sync();  // the leader's pfull exists before any peer stores to it
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
   pdl_wait();  // the previous kernel's writes are visible from here on
@@ -214,9 +242,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int64_t flat = 0;  // stage index over this CTA's whole tile sequence
     uint32_t side_phase = 0;
     bool ok = true;
-    WorkIter work = work_begin<SPLIT>(p);
+    WorkIter work = work_begin<SCHED>(p);
     Unit t;
-    while (ok && work_next<SPLIT, KS>(p, work, t)) {
+    while (ok && work_next<SCHED, KS>(p, work, t)) {
       const int n_tile = t.n_tile;
       const int n0 = n_tile * BM;
       const int m0 = t.m_tile * BN;
@@ -294,9 +322,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0, side_cnt = 0, meta_ctr = 0;
       uint32_t acc_cnt = 0;
       bool ok = true;
-      WorkIter work = work_begin<SPLIT>(p);
+      WorkIter work = work_begin<SCHED>(p);
       Unit t;
-      while (ok && work_next<SPLIT, KS>(p, work, t)) {
+      while (ok && work_next<SCHED, KS>(p, work, t)) {
         uint32_t d = 0;
         if (!PROMOTE) {
           const uint32_t b = acc_cnt % NACC;
@@ -373,9 +401,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // stream-K: this launch's epoch (the counter changes only after every CTA
     // of the launch has finished; the previous launch is complete here)
     const unsigned long long epoch = SPLIT ? (*reinterpret_cast<volatile unsigned long long*>(p.sk_word) >> 20) + 1 : 0;
-    WorkIter work = work_begin<SPLIT>(p);
+    WorkIter work = work_begin<SCHED>(p);
     Unit t;
-    while (ok && work_next<SPLIT, KS>(p, work, t)) {
+    while (ok && work_next<SCHED, KS>(p, work, t)) {
       const int n0 = t.n_tile * BM;
       const int m0 = t.m_tile * BN;
       const int n = n0 + row;
@@ -453,7 +481,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           continue;
         }
-        if constexpr (SPLIT) {
+        if constexpr (SPLIT || CSPLIT) {
+          if (CSPLIT && t.role == 4) {
+            // a peer's stages of the cluster's tile: the unscaled fp32 partial
+            // goes straight into the leader CTA's shared memory, [peer][col][row],
+            // each word counted on the leader's pfull barrier
+            const uint32_t peer = cluster_rank() - 1;
+            const uint32_t dst = cluster_addr(part, 0) + 4u * (peer * (BN * BM) + c0 * BM + row);
+            const uint32_t pbar = cluster_addr(pfull, 0);
+#pragma unroll
+            for (int c = 0; c < COLS; c += CH) {
+              uint32_t v[CH];
+              tmem_load_cols<CH / 8>(lane_base + b * BN + c0 + c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < CH; ++j) st_async_b32(dst + 4u * ((c + j) * BM), v[j], pbar);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
+            ++acc_cnt;
+            continue;
+          }
           if (t.role == 2) {
             // later stages of a tile: publish the unscaled fp32 partial in this
             // CTA's slot, [col][row], for the CTA that holds the tile's start
@@ -476,7 +525,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (et == 0) st_release_u64(&p.flags[blockIdx.x], epoch);
             continue;
           }
-          if (t.role == 1) {
+          if (t.role == 1 || t.role == 3) {
             // a tile's first stages complete it: this accumulator, then the
             // partials of the CTAs that hold its later stages, in stage order
             // (a fixed summation order, whatever the arrival order).  Those
@@ -495,16 +544,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[b]);  // one arrival per warp
             ++acc_cnt;
-            // add the partials in CTA order: the gathered group, then the rest
+            if constexpr (CSPLIT) {
+              // the peers' partials, in rank order, from this CTA's shared memory
+              if (!mbar_wait(pfull, 0)) ok = false;
+              if (epilogue_bar_any(!ok)) { ok = false; break; }
+              const int peers = static_cast<int>(cluster_nrank()) - 1;
+              for (int i = 0; i < peers; ++i) {
+                const float* src = part + i * (BN * BM) + c0 * BM + row;
 #pragma unroll
-            for (int g = 0; g < SK_GRP; ++g)
-              if (g < nparts) {
-#pragma unroll
-                for (int c = 0; c < COLS; ++c) acc[c] += pre[g][c];
+                for (int c = 0; c < COLS; ++c) acc[c] += src[c * BM];
               }
-            for (int i = SK_GRP; i < nparts; ++i) {
+            } else {
+              // add the partials in CTA order: the gathered group, then the rest
 #pragma unroll
-              for (int c = 0; c < COLS; ++c) acc[c] += __ldcg(wsp + static_cast<int64_t>(i) * (BN * BM) + c * BM);
+              for (int g = 0; g < SK_GRP; ++g)
+                if (g < nparts) {
+#pragma unroll
+                  for (int c = 0; c < COLS; ++c) acc[c] += pre[g][c];
+                }
+              for (int i = SK_GRP; i < nparts; ++i) {
+#pragma unroll
+                for (int c = 0; c < COLS; ++c) acc[c] += __ldcg(wsp + static_cast<int64_t>(i) * (BN * BM) + c * BM);
+              }
             }
             if (!ok) break;
 #pragma unroll
@@ -632,7 +693,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   pdl_trigger();  // only teardown is left: the next kernel may begin launching
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CSPLIT)
+    cluster_sync();  // no CTA leaves while a peer may still store into its shared memory
+  else
+    __syncthreads();
   if (SPLIT && threadIdx.x == 0) {
     // count this CTA out (low 20 bits); the launch's last CTA starts the next
     // epoch with a zero count.  Every CTA read the epoch before any CTA got
@@ -648,17 +712,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS>
+template <int BN, bool PROMOTE, bool SIDE, bool SPLIT, int KS, bool CSPLIT = false>
 sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2, const CUtensorMap& x2,
                    const CUtensorMap& y, const GemmArgs& args, cudaStream_t stream) {
-  using C = Cfg<BN, PROMOTE, SIDE, SPLIT, KS>;
-  auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE, SPLIT, KS>;
+  using C = Cfg<BN, PROMOTE, SIDE, SPLIT, KS, CSPLIT>;
+  auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE, SPLIT, KS, CSPLIT>;
   static bool attr_done[64] = {};
   if (!attr_done[dev->ordinal]) {
     if (static_cast<size_t>(C::SMEM) > dev->smem_optin) return SP24_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return SP24_ERR_CUDA;
     attr_done[dev->ordinal] = true;
+  }
+  if constexpr (CSPLIT) {
+    // one cluster of args.cs CTAs per tile (every tile's K range split cs ways)
+    const int64_t tiles = static_cast<int64_t>(args.L) * args.m_tiles * args.n_tiles;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(args.cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * args.cs), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, x, w2, x2, y, args) != cudaSuccess) return SP24_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
   }
   // stream-K: one CTA per range of stages (at most one per SM); otherwise
   // persistent CTAs over whole tiles
@@ -678,12 +762,14 @@ template <bool PROMOTE, bool SIDE>
 sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMap& w2,
                       const CUtensorMap& x2, const CUtensorMap& y, const GemmArgs& args, cudaStream_t s) {
   const bool split = args.sk_units > 0;
+  const bool csplit = args.cs > 1;
   constexpr bool PLAIN = !PROMOTE && !SIDE;
   switch (bn) {
     case 16:
       if constexpr (!PROMOTE) {
         if (ks == 4) {
           if constexpr (PLAIN) if (split) return launch<16, false, false, true, 4>(dev, x, w2, x2, y, args, s);
+          if constexpr (PLAIN) if (csplit) return launch<16, false, false, false, 4, true>(dev, x, w2, x2, y, args, s);
           return launch<16, false, SIDE, false, 4>(dev, x, w2, x2, y, args, s);
         }
       }
@@ -695,6 +781,7 @@ sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& 
       if constexpr (!PROMOTE) {
         if (ks == 4) {
           if constexpr (PLAIN) if (split) return launch<32, false, false, true, 4>(dev, x, w2, x2, y, args, s);
+          if constexpr (PLAIN) if (csplit) return launch<32, false, false, false, 4, true>(dev, x, w2, x2, y, args, s);
           return launch<32, false, SIDE, false, 4>(dev, x, w2, x2, y, args, s);
         }
       }
@@ -706,6 +793,7 @@ sp24_status launch_bn(int bn, int ks, const DeviceInfo* dev, const CUtensorMap& 
       if constexpr (!PROMOTE) {
         if (ks == 2) {
           if constexpr (PLAIN) if (split) return launch<64, false, false, true, 2>(dev, x, w2, x2, y, args, s);
+          if constexpr (PLAIN) if (csplit) return launch<64, false, false, false, 2, true>(dev, x, w2, x2, y, args, s);
           return launch<64, false, SIDE, false, 2>(dev, x, w2, x2, y, args, s);
         }
       }
@@ -740,6 +828,7 @@ int pick_bn(int64_t M, bool plain) {
 struct Plan {
   int bn, ks, m_tiles, n_tiles, k_tiles;
   bool streamk;
+  int cs;                        // cluster split: CTAs per tile (1 = none)
   int grid;                      // stream-K: CTAs (one range each)
   size_t ws_ctrl, ws_bytes;  // stream-K: control bytes (counter, flags); total with the partials
 };
@@ -755,14 +844,20 @@ size_t streamk_ctrl_bytes(int sm_count) {
 // heuristic below, whole tiles only, or stream-K wherever it applies.
 std::atomic<int> g_decomposition{SP24_DECOMP_HEURISTIC};
 
-// Stream-K applies to the HBM-bound small-token tiles (plain scaling, BN <= 64,
-// at least two stages per tile).  The heuristic takes it when balancing the
-// weight stream saves more than it costs.  With whole tiles the busiest CTA
-// streams `rounds` tiles' weights at the rate one SM sustains alone (about
-// 80 GB/s measured on the 152-SM part); with stream-K all SMs stream the
-// weights at the HBM rate (about 6.5 TB/s), but publishing and gathering the
-// partials lengthens the launch by about 3.5 us.  (The activations are read
-// from L2 by every tile and count in neither.)
+// Stream-K and the cluster split apply to the HBM-bound small-token tiles
+// (plain scaling, BN <= 64).  The heuristic models each schedule's time in
+// microseconds from the weight bytes (the activations are read from L2 by
+// every tile and count in none of them) and constants measured on the
+// 152-SM part, and leaves whole tiles only for a gain above 0.1 us:
+//  - whole tiles: the busiest CTA streams `rounds` tiles at the rate one SM
+//    sustains alone (about 87 GB/s), at best the HBM rate (about 6.5 TB/s);
+//  - cluster split, cs = 2 or 4 CTAs per tile, all clusters in one wave: a
+//    cs-th of a tile per SM, at best the HBM rate, plus about 1.2 us for the
+//    exchange through distributed shared memory (clusters of 3 measured
+//    slower than whole tiles: they do not pack the SMs);
+//  - stream-K: the HBM rate, plus about 3.5 us for publishing and gathering
+//    the partials through L2, plus the completing CTA's read of the partials
+//    of a tile's other CTAs (about 150 GB/s).
 Plan make_plan(int64_t M, int64_t N, int64_t K, bool promote, bool side, int sm_count, int64_t L) {
   Plan pl;
   pl.bn = pick_bn(M, !promote && !side);
@@ -774,18 +869,42 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bool promote, bool side, int sm_
   const int64_t tiles = L * pl.m_tiles * pl.n_tiles;
   const int64_t kst = pl.k_tiles / pl.ks;
   pl.streamk = false;
+  pl.cs = 1;
   pl.grid = 0;
   pl.ws_ctrl = pl.ws_bytes = 0;
   const int mode = g_decomposition.load(std::memory_order_relaxed);
   if (!promote && !side && pl.bn <= 64 && kst >= 2 && sm_count > 0 && mode != SP24_DECOMP_DATA_PARALLEL) {
+    const int cs_max = pl.bn <= 32 ? 4 : 2;  // the leader's shared memory holds 3 (1) peer partials
+    auto cs_fits = [&](int cs) { return tiles * cs <= sm_count && kst >= cs; };
     if (mode == SP24_DECOMP_STREAM_K) {
       pl.streamk = true;
-    } else if (kst >= 4) {
+    } else if (mode == SP24_DECOMP_CLUSTER_SPLIT) {
+      for (int cs = cs_max; cs >= 2 && pl.cs == 1; cs /= 2)
+        if (cs_fits(cs)) pl.cs = cs;
+    } else {
       const double rounds = static_cast<double>((tiles + sm_count - 1) / sm_count);
       const double tile_bytes = static_cast<double>(pl.k_tiles) * (BM * BK / 2 + BM * BK / 8);
-      const double t_whole_us = rounds * tile_bytes / 80e3;
-      const double t_streamk_us = static_cast<double>(tiles) * tile_bytes / 6.5e6;
-      pl.streamk = t_whole_us - t_streamk_us > 3.5;
+      const double t_hbm = static_cast<double>(tiles) * tile_bytes / 6.5e6;
+      const double t_whole = std::max(rounds * tile_bytes / 87e3, t_hbm);
+      double best = t_whole - 0.1;
+      if (kst >= 4) {
+        const double ctas_per_tile = std::min<double>(static_cast<double>(sm_count), static_cast<double>(tiles * kst)) /
+                                     static_cast<double>(tiles);
+        const double t = t_hbm + 3.5 + (ctas_per_tile - 1.0) * pl.bn * BM * 4 / 150e3;
+        if (t < best) {
+          best = t;
+          pl.streamk = true;
+        }
+      }
+      for (int cs = 2; cs <= cs_max; cs *= 2) {
+        if (!cs_fits(cs) || kst < 2 * cs) continue;
+        const double t = std::max(tile_bytes / cs / 87e3, t_hbm) + 1.2;
+        if (t <= best) {  // on a tie the larger split: more SMs streaming
+          best = t;
+          pl.cs = cs;
+          pl.streamk = false;
+        }
+      }
     }
   }
   if (pl.streamk) {
@@ -807,10 +926,24 @@ int current_sm_count() {
 }  // namespace sp24
 
 extern "C" sp24_status sp24_set_decomposition(int mode) {
-  if (mode != SP24_DECOMP_HEURISTIC && mode != SP24_DECOMP_DATA_PARALLEL && mode != SP24_DECOMP_STREAM_K)
+  if (mode != SP24_DECOMP_HEURISTIC && mode != SP24_DECOMP_DATA_PARALLEL && mode != SP24_DECOMP_STREAM_K &&
+      mode != SP24_DECOMP_CLUSTER_SPLIT)
     return SP24_ERR_INVALID_ARG;
   sp24::g_decomposition.store(mode, std::memory_order_relaxed);
   return SP24_OK;
+}
+
+extern "C" int sp24_fp8_gemm_decomposition(int64_t M, int64_t N, int64_t K, int64_t r, int* cluster_size) {
+  using namespace sp24;
+  if (cluster_size) *cluster_size = 1;
+  if (M < 1 || N < BM || N % BM != 0 || K < BK || K % BK != 0 || r < 0) return -1;
+  const int sms = current_sm_count();
+  if (sms <= 0) return -1;
+  if (pair_gemm_applies(M, N, K, true, r)) return SP24_DECOMP_DATA_PARALLEL;
+  const Plan pl = make_plan(M, N, K, false, r > 0, sms, 1);
+  if (cluster_size) *cluster_size = pl.cs;
+  if (pl.streamk) return SP24_DECOMP_STREAM_K;
+  return pl.cs > 1 ? SP24_DECOMP_CLUSTER_SPLIT : SP24_DECOMP_DATA_PARALLEL;
 }
 
 extern "C" size_t sp24_fp8_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int64_t r) {
@@ -899,6 +1032,7 @@ sp24_status gemm_impl(const void* Xq, const float* sx, int64_t M, int64_t K, int
   a.k_tiles = pl.k_tiles;
   a.side_ksteps = static_cast<int>(r / 16);
   a.kst = pl.k_tiles / pl.ks;
+  a.cs = pl.cs;
   a.sk_units = 0;
   a.ws = nullptr;
   a.flags = nullptr;

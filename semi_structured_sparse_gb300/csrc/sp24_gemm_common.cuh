@@ -29,6 +29,7 @@ struct GemmArgs {
   // stream-K (one-CTA kernel, SPLIT instances): the stage sequence of all
   // tiles, tile-major, cut into one contiguous range per CTA
   int kst;          // stages per tile
+  int cs;           // cluster split: CTAs of a cluster sharing one tile's K range (1 = none)
   int64_t sk_units; // stages in all (tiles x kst)
   float* ws;        // per CTA: one unscaled fp32 partial [BN][128]
   unsigned long long* flags;  // per CTA: the epoch at which its partial was published

@@ -151,9 +151,9 @@ def test_set_decomposition_modes(lib):
     """The three modes are accepted, anything else refused; the heuristic is
     left in force."""
     try:
-        for mode in (1, 2, 0):
+        for mode in (1, 2, 3, 0):
             assert lib.sp24_set_decomposition(mode) == 0
-        for bad in (-1, 3, 100):
+        for bad in (-1, 4, 100):
             assert lib.sp24_set_decomposition(bad) == 1  # SP24_ERR_INVALID_ARG
     finally:
         lib.sp24_set_decomposition(0)

@@ -333,23 +333,75 @@ def test_split_k(ora, sp24, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,expect", [
-    (16, 4096, 14336, True),    # few weight tiles, long K: the weight stream is balanced
-    (64, 4096, 14336, True),
-    (16, 4096, 4096, False),    # short K: the partials' exchange costs more than it saves
-    (16, 28672, 4096, False),   # enough tiles for whole rounds
-    (128, 4096, 14336, False),  # 128-token tiles: whole tiles only
+    (16, 4096, 14336, (3, 4)),   # few weight tiles, long K: a cluster of 4 CTAs per tile
+    (64, 4096, 14336, (3, 2)),   # 64-token tiles: clusters of 2
+    (16, 4096, 4096, (3, 4)),
+    (16, 6144, 4096, (3, 2)),    # 48 tiles: clusters of 2 (4 would not fit in one wave)
+    (16, 14336, 4096, (1, 1)),   # 112 tiles: no room to split, whole tiles already stream at the HBM rate
+    (16, 28672, 4096, (1, 1)),   # enough tiles for whole rounds
+    (128, 4096, 14336, (1, 1)),  # 128-token tiles: whole tiles only
 ])
 def test_heuristic_decomposition(sp24, M, N, K, expect):
-    """The default mode takes stream-K only where its cost model expects a gain."""
-    assert (sp24.workspace_size(M, N, K) > 0) == expect
+    """The default mode's choice (cost model on a 152-SM part)."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected choices are those of a 152-SM part")
+    assert sp24.decomposition_of(M, N, K) == expect
+    assert sp24.workspace_size(M, N, K) == 0
 
 
-def test_heuristic_streamk_shape(ora, sp24):
+def test_heuristic_split_shape(ora, sp24):
     """A shape the heuristic itself splits, through the default path."""
     M, N, K = 5, 1024, 16384
-    assert sp24.workspace_size(M, N, K) > 0
+    assert sp24.decomposition_of(M, N, K)[0] != sp24.DECOMP_DATA_PARALLEL
     w = inputs.Workload("skh", M, N, K, seed=77)
-    _check_full(ora, sp24, w, "heuristic stream-K")
+    _check_full(ora, sp24, w, "heuristic split")
+
+
+@pytest.mark.parametrize("M,N,K,cs", [(16, 5120, 4096, 2), (1, 5120, 4096, 2), (64, 4096, 4096, 2),
+                                      (33, 6144, 2048, 2), (16, 256, 2048, 4), (7, 2560, 4096, 4),
+                                      (16, 512, 1024, 2)])
+def test_cluster_split(ora, sp24, M, N, K, cs):
+    """Cluster split forced: each tile's K range is cut across the cs CTAs of a
+    cluster, whose partials reach the leader CTA's shared memory (st.async)
+    and are added in rank order; deterministic, and equal to whole tiles
+    within rounding."""
+    w = inputs.Workload("cl", M, N, K, seed=3 * M + N)
+    with sp24.decomposition(sp24.DECOMP_CLUSTER_SPLIT):
+        assert sp24.decomposition_of(M, N, K) == (sp24.DECOMP_CLUSTER_SPLIT, cs)
+        assert sp24.workspace_size(M, N, K) == 0
+        y, ref = _check_full(ora, sp24, w, "cluster split M=%d N=%d K=%d" % (M, N, K))
+        xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+        y2 = _run_gpu(sp24, w, xq, sx, values, meta, sw, None, None)
+    assert np.array_equal(y, y2)
+
+
+def test_cluster_split_graph_replay(ora, sp24):
+    """Cluster-split launches captured in a CUDA graph replay bit-identically."""
+    shapes = [(16, 2560, 4096), (64, 1024, 2048)]
+    with sp24.decomposition(sp24.DECOMP_CLUSTER_SPLIT):
+        cases = []
+        for i, (M, N, K) in enumerate(shapes):
+            w = inputs.Workload("clg", M, N, K, seed=60 + i)
+            xq, sx, values, meta, sw, _, _ = _prep(ora, w)
+            tv, tm = _abi(ora, values, meta)
+            ops = [dev(t) for t in (xq, sx, tv, tm, sw)]
+            y = sp24.gemm(*ops)
+            torch.cuda.synchronize()
+            sp24.last_device_error()
+            assert_close(bf16_to_f64(y), ora.gemm(xq, sx, values, meta, sw), "cluster split shape %d" % i)
+            cases.append((ops, y.clone(), torch.empty_like(y)))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for ops, _, out in cases:
+                sp24.gemm(*ops, out=out)
+    for _ in range(3):
+        for _, _, out in cases:
+            out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        sp24.last_device_error()
+        for i, (_, ref, out) in enumerate(cases):
+            assert torch.equal(out, ref), "graph replay of shape %d" % i
 
 
 def test_streamk_workspace_reuse_and_graph_replay(ora, sp24):
@@ -414,15 +466,16 @@ def test_split_k_without_workspace_runs_unsplit(ora, sp24):
     assert_close(bf16_to_f64(y), ora.gemm(xq, sx, values, meta, sw), "unsplit fallback")
 
 
-@pytest.mark.parametrize("L,M,N,K,gN,gK,with_bias,sk", [
-    (3, 16, 512, 512, 1, None, False, False),     # decode-size problems: one launch over all of them
-    (4, 40, 384, 512, 128, 128, True, False),     # group-wise promotion, ragged token tails
-    (2, 40, 1024, 2048, 1, None, True, True),     # few tiles: stream-K, each tile cut between 8 CTAs
-    (3, 16, 2560, 4096, 1, None, False, True),    # stream-K ranges that cross tiles and problems
-    (3, 300, 512, 512, 1, None, True, False),     # SM-pair problems: one launch each
-    (2, 200, 512, 768, 128, 128, False, False),   # SM-pair group-wise problems
+@pytest.mark.parametrize("L,M,N,K,gN,gK,with_bias,mode", [
+    (3, 16, 512, 512, 1, None, False, 0),     # decode-size problems: one launch over all of them
+    (4, 40, 384, 512, 128, 128, True, 0),     # group-wise promotion, ragged token tails
+    (2, 40, 1024, 2048, 1, None, True, 2),    # few tiles: stream-K, each tile cut between 8 CTAs
+    (3, 16, 2560, 4096, 1, None, False, 2),   # stream-K ranges that cross tiles and problems
+    (3, 16, 2560, 4096, 1, None, True, 3),    # cluster split, one cluster per (problem, tile)
+    (3, 300, 512, 512, 1, None, True, 0),     # SM-pair problems: one launch each
+    (2, 200, 512, 768, 128, 128, False, 0),   # SM-pair group-wise problems
 ])
-def test_gemm_batched(ora, sp24, L, M, N, K, gN, gK, with_bias, sk):
+def test_gemm_batched(ora, sp24, L, M, N, K, gN, gK, with_bias, mode):
     """L independent problems of one shape (CUTLASS's batched L mode): each
     output equals the oracle on that problem's own operands.  The activations
     come from a taller buffer, so consecutive problems are not adjacent."""
@@ -445,7 +498,7 @@ def test_gemm_batched(ora, sp24, L, M, N, K, gN, gK, with_bias, sk):
     bias_bits = [inputs.bf16_bits(torch.from_numpy(rng.normal(0, 0.5, N).astype(np.float32)).to(torch.bfloat16))
                  for _ in range(L)]
     bias = torch.stack([dev(b) for b in bias_bits]) if with_bias else None
-    with sp24.decomposition(sp24.DECOMP_STREAM_K if sk else sp24.DECOMP_HEURISTIC):
+    with sp24.decomposition(mode):
         y = sp24.gemm_batched(xq, sx, values, meta, sw, 1, gN, gk, bias=bias)
     torch.cuda.synchronize()
     sp24.last_device_error()
