@@ -39,7 +39,7 @@ DESCR = {
              "W[4096,4096] bf16 N(0,0.02) -> 2:4 e4m3 per-channel, Y bf16",
     "groupwise": "group-wise scaling: X[3000,4096] 1x128 scales, W[14336,4096] 128x128 block scales",
     "fused": "fused: llama shapes + bf16 side GEMM X2[2048,64] W2[4096,64]",
-    "decode": "decode: X[M,4096] per-token, W[28672,4096] per-channel",
+    "decode": "decode: X[M,{K}] per-token, W[{N},{K}] per-channel",
     "tiny": "tiny: X[128,512], W[256,512]",
 }
 
@@ -49,22 +49,22 @@ DESCR = {
 # An entry is removed when its kernel changes; absent entries report null.
 CAPTURED_TRAFFIC = {
     # sp24_gemm_pair_kernel<256,0,0> on the Llama-style linear (M 2048, N 4096, K 4096)
-    ("llama", 2048, "gemm"): 18941184 + 0,
+    ("llama", 2048, 4096, 4096, "gemm"): 18938880 + 0,
     # compress_rows_kernel<0> on W[4096, 4096] (Llama-style linear), two rows per CTA
-    ("llama", 2048, "compress"): 33597696 + 9728,
+    ("llama", 2048, 4096, 4096, "compress"): 33597696 + 9728,
     # compress_rows_kernel<0> on W[28672, 4096] (decode workload), two rows per CTA
-    ("decode", 16, "compress"): 234962688 + 19037184,
-    # sp24_gemm_kernel<16,0,0,0,4>, decode M 16, N 28672, K 4096
-    ("decode", 16, "gemm"): 73601792 + 572928,
+    ("decode", 16, 28672, 4096, "compress"): 234962688 + 19037184,
+    # sp24_gemm_kernel<16,0,0,0,4,0> (whole tiles), decode M 16, N 28672, K 4096
+    ("decode", 16, 28672, 4096, "gemm"): 73602816 + 467968,
     # sp24_gemm_pair_kernel<128,0,1>, group-wise M 3000, N 14336, K 4096
-    ("groupwise", 3000, "gemm"): 50562304 + 57765632,
+    ("groupwise", 3000, 14336, 4096, "gemm"): 52530944 + 57308672,
     # sp24_gemm_pair_kernel<240,1,0>, fused side GEMM M 2048, N 4096, K 4096, r 64
-    ("fused", 2048, "gemm"): 19724288 + 0,
+    ("fused", 2048, 4096, 4096, "gemm"): 19725056 + 0,
 }
 
 
-def captured_traffic(workload, M, kernel):
-    return CAPTURED_TRAFFIC.get((workload, M, kernel))
+def captured_traffic(workload, w, kernel):
+    return CAPTURED_TRAFFIC.get((workload, w.M, w.N, w.K, kernel))
 
 
 # ---------------------------------------------------------------- utilities
@@ -229,7 +229,7 @@ def run_ours(args):
     sp24.load(build_if_missing=(world == 1))
     w = inputs.WORKLOADS[args.workload]
     if args.workload == "decode":
-        w = inputs.with_shape(w, M=args.decode_m)
+        w = inputs.with_shape(w, M=args.decode_m, N=args.decode_n, K=args.decode_k)
     w = inputs.with_shape(w, seed=w.seed + 1000 * rank)  # each replica its own batch
     gk = w.gk
     X, W, X2, W2 = inputs.generate(w)
@@ -424,7 +424,7 @@ def run_ours(args):
         roofline = {"kernel": gemm_kernel, "bound": "tensor", "achieved": round(gemm_tflops_alg, 1),
                     "peak": round(fp8_dense_peak, 1), "unit": "TFLOP/s",
                     "frac": round(gemm_tflops_alg / fp8_dense_peak, 4),
-                    "traffic": captured_traffic(args.workload, w.M, "gemm"),
+                    "traffic": captured_traffic(args.workload, w, "gemm"),
                     "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16), of %s" % (
                         pk["source"], FP8_OVER_BF16, pk["source"]),
                     "achieved_counts": "algorithmic 2*M*N*K/2 flops (kept weights only) per launch"}
@@ -432,7 +432,7 @@ def run_ours(args):
         comp_kernel = "compress_blocks_kernel" if w.gN == 128 else "compress_rows_kernel"
         roofline = {"kernel": comp_kernel, "bound": "hbm", "achieved": round(comp_gbs, 1),
                     "peak": round(pk["hbm_gbs"], 1), "unit": "GB/s", "frac": round(comp_gbs / pk["hbm_gbs"], 4),
-                    "traffic": captured_traffic(args.workload, w.M, "compress"),
+                    "traffic": captured_traffic(args.workload, w, "compress"),
                     "peak_source": "%s copy bandwidth, of %s" % (pk["source"], pk["source"]),
                     "achieved_counts": "algorithmic bytes per launch: W read + values, metadata, scales written"}
     out = {
@@ -448,7 +448,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "e4m3",
         "data": "synthetic",
-        "config": {"workload": DESCR[args.workload], "M": w.M, "N": w.N, "K": w.K,
+        "config": {"workload": DESCR[args.workload].format(N=w.N, K=w.K), "M": w.M, "N": w.N, "K": w.K,
                    "scales": {"gM": w.gM, "gN": w.gN, "gK": gk}, "side_r": w.r,
                    "step": "compress(W) + sparse GEMM", "flops_per_step": "2*M*N*K dense-equivalent",
                    "l2": "rotating %d input sets of %.1f MB (> L2 %.0f MB)" % (nsets, set_bytes / 1e6, l2 / 1e6),
@@ -525,7 +525,7 @@ def run_reference(args):
         return  # the CPU reference arm runs on rank 0 only
     w = inputs.WORKLOADS[args.workload]
     if args.workload == "decode":
-        w = inputs.with_shape(w, M=args.decode_m)
+        w = inputs.with_shape(w, M=args.decode_m, N=args.decode_n, K=args.decode_k)
     budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
     secs = []
     descr, threads = "", 1
@@ -539,7 +539,7 @@ def run_reference(args):
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "impl": "reference",
-        "config": {"workload": DESCR[args.workload], "M": w.M, "N": w.N, "K": w.K,
+        "config": {"workload": DESCR[args.workload].format(N=w.N, K=w.K), "M": w.M, "N": w.N, "K": w.K,
                    "scales": {"gM": w.gM, "gN": w.gN, "gK": w.gk}, "side_r": w.r,
                    "step": "compress(W) + sparse GEMM", "parallelism": "single"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -557,6 +557,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(inputs.WORKLOADS), default="llama")
     ap.add_argument("--decode-m", type=int, default=16)
+    ap.add_argument("--decode-n", type=int, default=None,
+                    help="decode workload: another weight height (default 28672)")
+    ap.add_argument("--decode-k", type=int, default=None,
+                    help="decode workload: another K (default 4096)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
