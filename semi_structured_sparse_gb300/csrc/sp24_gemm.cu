@@ -9,16 +9,24 @@
 // klevzoff's swap+transpose answer); a weight row is a TMEM lane and a token
 // is a TMEM column.  Row-major Y is column-major Y^T, so nothing is moved.
 //
-// Structure (one persistent CTA per SM, 6 warps):
-//   warp 0      TMA producer: per 128-wide K step, the kept-value tile
-//               (128 rows x 64 B, 64-byte swizzle), the metadata tile
-//               (128 rows x 16 B) and the activation tile (BN rows x 128 B,
-//               128-byte swizzle) into one stage of a shared-memory ring.
-//   warp 1      TMEM allocation and the single-thread MMA issuer: copies the
-//               stage's metadata into TMEM (tcgen05.cp, lane = weight row)
-//               and issues two sparse tcgen05.mma (K = 64 each) per stage.
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator, scale, add the
-//               side accumulator, round to bf16, predicated stores.
+// Structure (one CTA per SM, 11 warps):
+//   warps 0-1   producers, taking pipeline stages in turn: per stage, KS
+//               128-wide K steps of kept values (128 rows x 64 B each,
+//               64-byte swizzle) and metadata (128 rows x 16 B) in two bulk
+//               copies, and KS activation boxes (BN rows x 128 B, 128-byte
+//               swizzle) by TMA, into one stage of a shared-memory ring.
+//   warp 2      TMEM allocation and the single-thread MMA issuer: copies each
+//               K step's metadata into TMEM (tcgen05.cp, lane = weight row)
+//               and issues two sparse tcgen05.mma (K = 64 each) per K step.
+//   warps 3-10  epilogue: tcgen05.ld of the fp32 accumulator, scale, add the
+//               side accumulator and the bias, round to bf16, TMA store
+//               (rows past M clipped by the tensor map).
+// Schedules (the host picks one per call): whole tiles dealt round-robin to
+// persistent CTAs; stream-K over all tiles' stages with partials exchanged
+// through a workspace; or a cluster split, each tile's K range cut across a
+// 2- or 4-CTA cluster whose peers send their partials into the leader CTA's
+// shared memory.  Large token counts use the SM-pair kernel instead
+// (sp24_gemm_pair.cu).
 // Scale promotion (gK = 128, CUTLASS PR #2095's per-K-tile promotion): every
 // 128-wide K step is its own scale block, so each stage's partial product
 // lands in its own TMEM buffer (ring of NACC) and the epilogue folds it into
@@ -717,12 +725,12 @@ sp24_status launch(const DeviceInfo* dev, const CUtensorMap& x, const CUtensorMa
                    const CUtensorMap& y, const GemmArgs& args, cudaStream_t stream) {
   using C = Cfg<BN, PROMOTE, SIDE, SPLIT, KS, CSPLIT>;
   auto kern = sp24_gemm_kernel<BN, PROMOTE, SIDE, SPLIT, KS, CSPLIT>;
-  static bool attr_done[64] = {};
-  if (!attr_done[dev->ordinal]) {
+  static std::atomic<bool> attr_done[64];  // per device ordinal; host threads may race to set it (idempotent)
+  if (!attr_done[dev->ordinal].load(std::memory_order_acquire)) {
     if (static_cast<size_t>(C::SMEM) > dev->smem_optin) return SP24_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return SP24_ERR_CUDA;
-    attr_done[dev->ordinal] = true;
+    attr_done[dev->ordinal].store(true, std::memory_order_release);
   }
   if constexpr (CSPLIT) {
     // one cluster of args.cs CTAs per tile (every tile's K range split cs ways)

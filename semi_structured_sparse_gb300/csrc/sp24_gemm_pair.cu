@@ -48,6 +48,7 @@
 // prologue (barriers, TMEM, descriptor prefetch) overlaps the previous
 // kernel's tail, and pdl_wait() precedes every global-memory access.
 #include <cuda_bf16.h>
+#include <atomic>
 #include "sp24_gemm_common.cuh"
 
 namespace sp24 {
@@ -608,7 +609,7 @@ sp24_status launch_pair(const DeviceInfo* dev, const void* Xq, int64_t ldx, cons
   if (st != SP24_OK) return st;
 
   auto kern = sp24_gemm_pair_kernel<PN, SIDE, PROMOTE>;
-  static int max_pairs[64] = {};  // per device: co-resident pairs (0 = not yet known)
+  static std::atomic<int> max_pairs[64];  // per device: co-resident pairs (0 = not yet known; races are idempotent)
   const int d = dev->ordinal;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -623,17 +624,19 @@ sp24_status launch_pair(const DeviceInfo* dev, const void* Xq, int64_t ldx, cons
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_pairs[d] == 0) {
+  int known = max_pairs[d].load(std::memory_order_acquire);
+  if (known == 0) {
     if (static_cast<size_t>(C::SMEM) > dev->smem_optin) return SP24_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return SP24_ERR_CUDA;
     cfg.gridDim = dim3(2 * (dev->sm_count / 2), 1, 1);
     int active = 0;
     if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) return SP24_ERR_CUDA;
-    max_pairs[d] = active;
+    max_pairs[d].store(active, std::memory_order_release);
+    known = active;
   }
   const int units = a.m_tiles * a.n_tiles;
-  const int pairs = units < max_pairs[d] ? units : max_pairs[d];
+  const int pairs = units < known ? units : known;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, kern, tm_x, tm_v, tm_m, tm_y, tm_w2, tm_x2, a) != cudaSuccess) return SP24_ERR_CUDA;
