@@ -420,6 +420,12 @@ def run_ours(args):
     pair = (w.gk == w.K and w.r <= 64 and w.M > 192 and w.N % 256 == 0) or \
         (w.gk == 128 and w.K > 128 and w.r == 0 and w.M > 64 and w.N % 256 == 0 and (w.K // 128) % 2 == 0)
     gemm_kernel = "sp24_gemm_pair_kernel" if pair else "sp24_gemm_kernel"
+    if pair or w.gk != w.K:
+        gemm_schedule = "whole tiles"
+    else:
+        mode, cs = sp24.decomposition_of(w.M, w.N, w.K, w.r)
+        gemm_schedule = {sp24.DECOMP_STREAM_K: "stream-K" if ws_bytes else "whole tiles",
+                         sp24.DECOMP_CLUSTER_SPLIT: "cluster split-K, %d CTAs per tile" % cs}.get(mode, "whole tiles")
     if t_gemm >= t_comp:
         roofline = {"kernel": gemm_kernel, "bound": "tensor", "achieved": round(gemm_tflops_alg, 1),
                     "peak": round(fp8_dense_peak, 1), "unit": "TFLOP/s",
@@ -458,7 +464,8 @@ def run_ours(args):
                              "sets between one event pair; e2e: eager calls through the public API"},
         "kernels": {
             "gemm": {"ms": round(t_gemm, 5), "tflops_dense_equiv": round(gemm_tflops_dense, 1),
-                     "frac_fp8_sparse_peak": round(gemm_tflops_alg / fp8_dense_peak, 4)},
+                     "frac_fp8_sparse_peak": round(gemm_tflops_alg / fp8_dense_peak, 4),
+                     "kernel": gemm_kernel, "schedule": gemm_schedule},
             "compress": {"ms": round(t_comp, 5), "gbs": round(comp_gbs, 1),
                          "frac_hbm": round(comp_gbs / pk["hbm_gbs"], 4)},
         },
