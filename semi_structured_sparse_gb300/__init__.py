@@ -92,14 +92,40 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _dev_tensor(t, dtype, name):
+def _dev_tensor(t, dtype, name, device=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
     if t.dtype != dtype:
         raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if t.stride(-1) != 1:
         raise ValueError("%s must have unit stride in its last dimension" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the operands on %s" % (name, t.device, device))
     return t
+
+
+def _cdiv(a, b):
+    return (a + b - 1) // b
+
+
+def _scale_count(K, gK, rows, g):
+    """Scales of a [rows, K] operand at granularity g x gK (0 if gK is invalid:
+    the library then refuses the call itself)."""
+    if not gK or K % gK != 0 or g <= 0:
+        return 0
+    return (K // gK) * _cdiv(rows, g)
+
+
+def _at_least(t, n, name):
+    """The kernels read or write n elements of t; the C ABI cannot see sizes."""
+    if not t.is_contiguous() or t.numel() < n:
+        raise ValueError("%s must be contiguous with at least %d elements (has %d)" % (name, n, t.numel()))
+
+
+def _matrix(t, rows, cols, name):
+    """A [rows, cols] matrix with unit column stride and row stride >= cols."""
+    if t.dim() != 2 or tuple(t.shape) != (rows, cols) or t.stride(0) < cols:
+        raise ValueError("%s must be [%d, %d], got %s" % (name, rows, cols, tuple(t.shape)))
 
 
 def workspace_size(M: int, N: int, K: int, r: int = 0) -> int:
@@ -150,6 +176,8 @@ def compress(w: torch.Tensor, gN: int = 1, gK: int = None, out=None, stream=None
     ``out`` may supply those three tensors (no allocation then)."""
     lib = load()
     _dev_tensor(w, torch.bfloat16, "w")
+    if w.dim() != 2:
+        raise ValueError("w must be [N, K]")
     N, K = w.shape
     gK = K if gK is None else gK
     if out is None:
@@ -158,6 +186,12 @@ def compress(w: torch.Tensor, gN: int = 1, gK: int = None, out=None, stream=None
         scales = torch.empty((K // gK, (N + gN - 1) // gN), dtype=torch.float32, device=w.device)
     else:
         values, meta, scales = out
+        _dev_tensor(values, torch.uint8, "values", w.device)
+        _dev_tensor(meta, torch.uint8, "meta", w.device)
+        _dev_tensor(scales, torch.float32, "scales", w.device)
+        _at_least(values, N * (K // 2), "values")
+        _at_least(meta, N * (K // 8), "meta")
+        _at_least(scales, _scale_count(K, gK, N, gN), "scales")
     _check(lib.sp24_fp8_compress(_ptr(w), N, K, w.stride(0), gN, gK, _ptr(values), _ptr(meta), _ptr(scales),
                                  _stream(stream)), "sp24_fp8_compress")
     return values, meta, scales
@@ -168,11 +202,20 @@ def decompress(values, meta, scales, gN: int = 1, gK: int = None, out=None, stre
     kept positions bf16(scale * e4m3 value), 0 elsewhere."""
     lib = load()
     _dev_tensor(values, torch.uint8, "values")
-    _dev_tensor(meta, torch.uint8, "meta")
-    _dev_tensor(scales, torch.float32, "scales")
+    if values.dim() != 2:
+        raise ValueError("values must be [N, K/2]")
     N, K = values.shape[0], values.shape[1] * 2
     gK = K if gK is None else gK
-    W = torch.empty((N, K), dtype=torch.bfloat16, device=values.device) if out is None else out
+    _dev_tensor(meta, torch.uint8, "meta", values.device)
+    _dev_tensor(scales, torch.float32, "scales", values.device)
+    _at_least(values, N * (K // 2), "values")
+    _at_least(meta, N * (K // 8), "meta")
+    _at_least(scales, _scale_count(K, gK, N, gN), "scales")
+    if out is None:
+        W = torch.empty((N, K), dtype=torch.bfloat16, device=values.device)
+    else:
+        W = _dev_tensor(out, torch.bfloat16, "out", values.device)
+        _matrix(W, N, K, "out")
     _check(lib.sp24_fp8_decompress(_ptr(values), _ptr(meta), _ptr(scales), N, K, gN, gK, _ptr(W), W.stride(0),
                                    _stream(stream)), "sp24_fp8_decompress")
     return W
@@ -184,6 +227,8 @@ def quantize_act(x: torch.Tensor, gK: int = None, out=None, stream=None):
     lib = load()
     bf16 = isinstance(x, torch.Tensor) and x.dtype == torch.bfloat16
     _dev_tensor(x, torch.bfloat16 if bf16 else torch.float32, "x")
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
     M, K = x.shape
     gK = K if gK is None else gK
     if out is None:
@@ -191,6 +236,10 @@ def quantize_act(x: torch.Tensor, gK: int = None, out=None, stream=None):
         sx = torch.empty((K // gK, M), dtype=torch.float32, device=x.device)
     else:
         xq, sx = out
+        _dev_tensor(xq, torch.uint8, "xq", x.device)
+        _dev_tensor(sx, torch.float32, "sx", x.device)
+        _at_least(xq, M * K, "xq")  # written densely, row stride K
+        _at_least(sx, _scale_count(K, gK, M, 1), "sx")
     f, name = ((lib.sp24_fp8_quantize_act_bf16, "sp24_fp8_quantize_act_bf16") if bf16
                else (lib.sp24_fp8_quantize_act, "sp24_fp8_quantize_act"))
     _check(f(_ptr(x), M, K, x.stride(0), gK, _ptr(xq), _ptr(sx), _stream(stream)), name)
@@ -206,30 +255,47 @@ def gemm(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = None, x2=
     the same stream; without one, each call that needs scratch allocates a zeroed one."""
     lib = load()
     _dev_tensor(xq, torch.uint8, "xq")
-    _dev_tensor(values, torch.uint8, "values")
-    _dev_tensor(meta, torch.uint8, "meta")
-    _dev_tensor(sx, torch.float32, "sx")
-    _dev_tensor(sw, torch.float32, "sw")
+    dev_ = xq.device
+    _dev_tensor(values, torch.uint8, "values", dev_)
+    if xq.dim() != 2 or values.dim() != 2:
+        raise ValueError("xq must be [M, K] and values [N, K/2]")
+    _dev_tensor(meta, torch.uint8, "meta", dev_)
+    _dev_tensor(sx, torch.float32, "sx", dev_)
+    _dev_tensor(sw, torch.float32, "sw", dev_)
     M, K = xq.shape
     N = values.shape[0]
     gK = K if gK is None else gK
     r = 0
     if x2 is not None:
-        _dev_tensor(x2, torch.bfloat16, "x2")
-        _dev_tensor(w2, torch.bfloat16, "w2")
+        _dev_tensor(x2, torch.bfloat16, "x2", dev_)
+        _dev_tensor(w2, torch.bfloat16, "w2", dev_)
         r = x2.shape[1]
         if not (x2.is_contiguous() and w2.is_contiguous()):
             raise ValueError("x2 and w2 must be contiguous")
+        _matrix(x2, M, r, "x2")
+        _matrix(w2, N, r, "w2")
     if not (sx.is_contiguous() and sw.is_contiguous() and values.is_contiguous() and meta.is_contiguous()):
         raise ValueError("scales, values and meta must be contiguous")
+    _at_least(values, N * (K // 2), "values")
+    _at_least(meta, N * (K // 8), "meta")
+    _at_least(sx, _scale_count(K, gK, M, gM), "sx")
+    _at_least(sw, _scale_count(K, gK, N, gN), "sw")
     if bias is not None:
-        _dev_tensor(bias, torch.bfloat16, "bias")
+        _dev_tensor(bias, torch.bfloat16, "bias", dev_)
         if not bias.is_contiguous() or bias.numel() != N:
             raise ValueError("bias must be a contiguous bf16 vector of N values")
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if out is None else out
+    if out is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev_)
+    else:
+        y = _dev_tensor(out, torch.bfloat16, "out", dev_)
+        _matrix(y, M, N, "out")
     ws_bytes = int(lib.sp24_fp8_gemm_workspace_size(M, N, K, r))
     if ws_bytes and workspace is None:
-        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=xq.device)
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev_)
+    elif workspace is not None:
+        _dev_tensor(workspace, torch.uint8, "workspace", dev_)
+        if not workspace.is_contiguous():
+            raise ValueError("workspace must be contiguous")
     _check(lib.sp24_fp8_gemm(_ptr(xq), _ptr(sx), M, K, xq.stride(0), gM, _ptr(values), _ptr(meta), _ptr(sw), N,
                              gN, gK, _ptr(x2), _ptr(w2), r, _ptr(bias), _ptr(y), y.stride(0), _ptr(workspace),
                              0 if workspace is None else workspace.numel() * workspace.element_size(),
@@ -251,14 +317,31 @@ def gemm_batched(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = N
     L, M, K = xq.shape
     N = values.shape[1]
     gK = K if gK is None else gK
+    dev_ = xq.device
+    for t, nm in ((values, "values"), (meta, "meta"), (sx, "sx"), (sw, "sw")):
+        if t.device != dev_ or t.shape[0] != L:
+            raise ValueError("%s must hold the same L problems on %s" % (nm, dev_))
+    _at_least(values[0], N * (K // 2), "values[l]")
+    _at_least(meta[0], N * (K // 8), "meta[l]")
+    _at_least(sx[0], _scale_count(K, gK, M, gM), "sx[l]")
+    _at_least(sw[0], _scale_count(K, gK, N, gN), "sw[l]")
     if bias is not None:
-        _dev_tensor(bias, torch.bfloat16, "bias")
+        _dev_tensor(bias, torch.bfloat16, "bias", dev_)
         if bias.shape != (L, N):
             raise ValueError("bias must be [L, N]")
-    y = torch.empty((L, M, N), dtype=torch.bfloat16, device=xq.device) if out is None else out
+    if out is None:
+        y = torch.empty((L, M, N), dtype=torch.bfloat16, device=dev_)
+    else:
+        y = _dev_tensor(out, torch.bfloat16, "out", dev_)
+        if y.dim() != 3 or tuple(y.shape) != (L, M, N) or y.stride(1) < N:
+            raise ValueError("out must be [L, M, N]")
     ws_bytes = L * int(lib.sp24_fp8_gemm_workspace_size(M, N, K, 0))
     if ws_bytes and workspace is None:
-        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=xq.device)
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev_)
+    elif workspace is not None:
+        _dev_tensor(workspace, torch.uint8, "workspace", dev_)
+        if not workspace.is_contiguous():
+            raise ValueError("workspace must be contiguous")
     _check(lib.sp24_fp8_gemm_batched(
         _ptr(xq), _ptr(sx), M, K, xq.stride(1), gM, _ptr(values), _ptr(meta), _ptr(sw), N, gN, gK, _ptr(bias),
         _ptr(y), y.stride(1), L, xq.stride(0), sx.stride(0), values.stride(0), meta.stride(0), sw.stride(0),

@@ -165,3 +165,26 @@ def test_product_path_has_no_cpu_fallback():
     txt = open(pkg).read()
     assert "import oracle" not in txt and "from oracle" not in txt
     assert "import numpy" not in txt
+
+
+def test_binding_size_checks():
+    """The binding checks what the C ABI cannot see: buffer sizes, shapes and
+    strides of the tensors the kernels read and write."""
+    import torch
+    import semi_structured_sparse_gb300 as s
+    assert s._scale_count(4096, 4096, 2048, 1) == 2048          # per token
+    assert s._scale_count(4096, 128, 3000, 1) == 32 * 3000      # 1 x 128
+    assert s._scale_count(4096, 128, 300, 128) == 32 * 3        # 128 x 128, ragged
+    assert s._scale_count(4096, 100, 16, 1) == 0                # invalid gK: the library refuses it
+    s._at_least(torch.zeros(10), 10, "t")
+    with pytest.raises(ValueError):
+        s._at_least(torch.zeros(9), 10, "t")
+    with pytest.raises(ValueError):
+        s._at_least(torch.zeros(4, 6)[:, :3], 12, "t")             # not contiguous
+    s._matrix(torch.zeros(4, 8)[:, :6], 4, 6, "m")                # a row stride above the width is fine
+    with pytest.raises(ValueError):
+        s._matrix(torch.zeros(4, 6), 4, 8, "m")
+    with pytest.raises(ValueError):
+        s._matrix(torch.zeros(24), 4, 6, "m")
+    with pytest.raises(ValueError):
+        s._dev_tensor(torch.zeros(4), torch.float32, "t")          # host tensors are refused
