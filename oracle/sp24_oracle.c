@@ -29,7 +29,7 @@
  *     #2058 "How to implement a fused mixed precision matrix multiplication
  *     such as w4a4 + w16a16?", hyx1999's statement of Y = X1 W1^T + X2 W2^T).
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - ties in the pruning argsort: the lower index wins;
  *   - amax == 0 (all-zero group, which must be accepted): scale = 1;
  *   - quantization divides by the scale (IEEE fp32, correctly rounded),
