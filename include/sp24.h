@@ -174,13 +174,14 @@ SP24_API sp24_status sp24_fp8_quantize_act_bf16(const void* X, int64_t M, int64_
  *           16-byte aligned.
  *   workspace, workspace_bytes: device scratch of at least
  *           sp24_fp8_gemm_workspace_size(M, N, K, r) bytes, 16-byte aligned
- *           (may be NULL when that size is 0).  Used when the small-token
- *           tiles alone would leave SMs idle in the last wave: the launch
- *           then deals the (tile, K block) work out to one CTA per SM in
- *           equal contiguous ranges (stream-K), and a tile cut between CTAs
- *           is finished by the CTA holding its first K blocks, which adds the
- *           others' fp32 partials in a fixed order (the result does not
- *           depend on timing).  The workspace holds a launch counter, one
+ *           (may be NULL when that size is 0).  Only the stream-K
+ *           decomposition of small-token calls uses it (see
+ *           sp24_set_decomposition; the size is 0 for the others): the launch
+ *           deals the (tile, K block) work out to one CTA per SM in equal
+ *           contiguous ranges, and a tile cut between CTAs is finished by the
+ *           CTA holding its first K blocks, which adds the others' fp32
+ *           partials in a fixed order (the result does not depend on
+ *           timing).  The workspace holds a launch counter, one
  *           flag per CTA and one partial tile per CTA.  Zero it once before
  *           its first use; each launch leaves it consistent for the next,
  *           whatever the shape, CUDA graph replays included (after a
