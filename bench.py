@@ -5,14 +5,24 @@ weight (magnitude 2:4 prune + e4m3 + pack) and run the group-wise scaled
 sparse GEMM on e4m3 activations.  Activation quantization is input
 preparation and runs before the timed region.
 
-Prints ONE JSON line (rank 0).  ``value`` is dense-equivalent TFLOPS (2*M*N*K
-per step, the convention sparse tensor peaks are quoted in) over the whole
-step, summed over ranks; per-kernel figures and the roofline of the dominant
-kernel ride along.  ``--impl reference`` times the CPU oracle instead, on a
-bounded sample of the same workload.
+The headline workload is the group-wise one (X[3000,4096] with 1x128
+activation scales, W[14336,4096] with 128x128 block scales), the largest
+configuration that fits one GPU.  Prints ONE JSON line (rank 0).  ``value`` is
+dense-equivalent TFLOPS (2*M*N*K per step, the convention sparse tensor peaks
+are quoted in) over the whole step, summed over ranks; ``roofline`` describes
+the step's dominant kernel.  ``kernels`` carries every configuration's kernels
+timed alone (the Llama-style linear, the group-wise GEMM, the decode sweep
+and its weight's compression, the fused side GEMM), each against its own
+roofline.  ``--impl reference`` times the CPU oracle instead, on a bounded
+sample of the same workload.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama]
-       torchrun --nproc-per-node N bench.py --gpus N ...
+Timing: CUDA events on the launching stream around CUDA-graph replays (the
+kernels run back to back with their programmatic-launch edges, no host gaps),
+over rotating input sets larger than L2.  Each figure is the median over
+several replays, with the minimum and maximum beside it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload groupwise]
+       torchrun --nproc-per-node N bench.py --gpus N [--multi split|replicas] ...
 """
 import argparse
 import json
@@ -33,20 +43,22 @@ import inputs  # noqa: E402
 METRIC = "sparse FP8 GEMM TFLOPS & % of FP8 sparse peak; compress GB/s & % HBM peak"
 UNIT = "TFLOPS"
 FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+REPLAYS = 5          # timed graph replays per figure (median, min, max)
 
 DESCR = {
     "llama": "Llama-style FP8 linear: X[2048,4096] e4m3 per-token (N(0,1), 0.1% outliers x20), "
              "W[4096,4096] bf16 N(0,0.02) -> 2:4 e4m3 per-channel, Y bf16",
-    "groupwise": "group-wise scaling: X[3000,4096] 1x128 scales, W[14336,4096] 128x128 block scales",
+    "groupwise": "group-wise scaling: X[3000,4096] e4m3 with 1x128 activation scales (partial M tile), "
+                 "W[14336,4096] bf16 N(0,0.02) -> 2:4 e4m3 with 128x128 block scales, Y bf16",
     "fused": "fused: llama shapes + bf16 side GEMM X2[2048,64] W2[4096,64]",
     "decode": "decode: X[M,{K}] per-token, W[{N},{K}] per-channel",
     "tiny": "tiny: X[128,512], W[256,512]",
 }
 
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
-# capture of the current kernel build (summaries and commands under profiles/).
-# An entry is removed when its kernel changes; absent entries report null.
+# DRAM bytes (read + write) per launch of a kernel, from one ncu capture of
+# the current kernel build (summaries and commands under profiles/).  An entry
+# is removed when its kernel changes; absent entries report null.
 CAPTURED_TRAFFIC = {
     # sp24_gemm_pair_kernel<256,0,0> on the Llama-style linear (M 2048, N 4096, K 4096)
     ("llama", 2048, 4096, 4096, "gemm"): 18938880 + 0,
@@ -56,8 +68,6 @@ CAPTURED_TRAFFIC = {
     ("decode", 16, 28672, 4096, "compress"): 234962688 + 19037184,
     # sp24_gemm_kernel<16,0,0,0,4,0> (whole tiles), decode M 16, N 28672, K 4096
     ("decode", 16, 28672, 4096, "gemm"): 73602816 + 467968,
-    # sp24_gemm_pair_kernel<128,0,1>, group-wise M 3000, N 14336, K 4096
-    ("groupwise", 3000, 14336, 4096, "gemm"): 52530944 + 57308672,
     # sp24_gemm_pair_kernel<240,1,0>, fused side GEMM M 2048, N 4096, K 4096, r 64
     ("fused", 2048, 4096, 4096, "gemm"): 19725056 + 0,
 }
@@ -67,79 +77,56 @@ def captured_traffic(workload, w, kernel):
     return CAPTURED_TRAFFIC.get((workload, w.M, w.N, w.K, kernel))
 
 
-# ---------------------------------------------------------------- utilities
-def next_rows(sp24, w, gk, sets, stream, ws, steps, pk):
-    """The kernels beyond the timed step, each alone, K launches back to back
-    (one CUDA graph) over the rotating sets between one event pair: the GEMM
-    with a bf16 bias, a batch of 4 problems, the activation quantization from
-    bf16, and the GPU dequantize."""
-    n = max(steps, 3)
-    bias = [torch.randn(w.N, device=s["y"].device).to(torch.bfloat16) for s in sets]
-    xb = [torch.randn(w.M, w.K, device=s["y"].device).to(torch.bfloat16) for s in sets]
-    qx = [(torch.empty_like(s["xq"]), torch.empty_like(s["sx"])) for s in sets]
-    dq = [torch.empty((w.N, w.K), dtype=torch.bfloat16, device=s["y"].device) for s in sets]
+# ------------------------------------------------------ algorithmic counts
+def n_scales(K, gk, rows, g):
+    return (K // gk) * ((rows + g - 1) // g)
 
-    def timed(fn):
-        for i in range(3):
-            fn(i % len(sets))
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()  # n launches replayed back to back, as the step is
-        cs = torch.cuda.Stream(stream.device)
-        cs.wait_stream(stream)
-        with torch.cuda.stream(cs):
-            with torch.cuda.graph(g, stream=cs):
-                for i in range(n):
-                    fn(i % len(sets))
-        stream.wait_stream(cs)
-        g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / n
 
-    def gemm_bias(i):
-        s = sets[i]
-        sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"],
-                  workspace=ws, bias=bias[i])
+def compress_bytes(w):
+    """W read once + kept values, metadata and scales written (2.625 B per weight)."""
+    return w.N * w.K * 2 + w.N * w.K // 2 + w.N * w.K // 8 + 4 * n_scales(w.K, w.gk, w.N, w.gN)
 
-    t_bias = timed(gemm_bias)
-    # a batch of 4 problems of this shape (no side GEMM), stacked
-    L = 4
-    s0 = sets[0]
-    bx = s0["xq"].unsqueeze(0).repeat(L, 1, 1)
-    bsx = s0["sx"].unsqueeze(0).repeat(L, 1, 1)
-    bv = s0["v"].unsqueeze(0).repeat(L, 1, 1)
-    bm = s0["m"].unsqueeze(0).repeat(L, 1, 1)
-    bsw = s0["sw"].unsqueeze(0).repeat(L, 1, 1)
-    by = torch.empty((L, w.M, w.N), dtype=torch.bfloat16, device=bx.device)
-    bws = torch.zeros(max(16, L * sp24.workspace_size(w.M, w.N, w.K)), dtype=torch.uint8, device=bx.device)
-    t_batch = timed(lambda i: sp24.gemm_batched(bx, bsx, bv, bm, bsw, w.gM, w.gN, gk, out=by, workspace=bws))
-    one = (bx[0], bsx[0], bv[0], bm[0], bsw[0], by[0])
-    t_one = timed(lambda i: sp24.gemm(one[0], one[1], one[2], one[3], one[4], w.gM, w.gN, gk, out=one[5],
-                                      workspace=ws))
-    t_q = timed(lambda i: sp24.quantize_act(xb[i], gk, out=qx[i]))
-    t_d = timed(lambda i: sp24.decompress(sets[i]["v"], sets[i]["m"], sets[i]["sw"], w.gN, gk, out=dq[i]))
-    sp24.last_device_error()
-    q_bytes = w.M * w.K * 2 + w.M * w.K + 4 * (w.K // gk) * w.M
-    d_bytes = w.N * w.K // 2 + w.N * w.K // 8 + 4 * (w.K // gk) * ((w.N + w.gN - 1) // w.gN) + 2 * w.N * w.K
-    hbm = pk["hbm_gbs"]
-    batch_bytes = L * (w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.K + 2 * w.M * w.N)
-    return {
-        "gemm_batched": {"L": L, "ms": round(t_batch, 5), "ms_one_problem": round(t_one, 5),
-                         "tflops_dense_equiv": round(L * 2 * w.M * w.N * w.K / (t_batch * 1e-3) / 1e12, 1),
-                         "gbs_operands": round(batch_bytes / (t_batch * 1e-3) / 1e9, 1)},
-        "gemm_with_bias": {"ms": round(t_bias, 5),
-                           "tflops_dense_equiv": round(w.dense_flops() / (t_bias * 1e-3) / 1e12, 1)},
-        "quantize_act_bf16": {"ms": round(t_q, 5), "gbs": round(q_bytes / (t_q * 1e-3) / 1e9, 1),
-                              "frac_hbm": round(q_bytes / (t_q * 1e-3) / 1e9 / hbm, 4),
-                              "bytes": "M*K*2 read + M*K + scales written"},
-        "decompress": {"ms": round(t_d, 5), "gbs": round(d_bytes / (t_d * 1e-3) / 1e9, 1),
-                       "frac_hbm": round(d_bytes / (t_d * 1e-3) / 1e9 / hbm, 4),
-                       "bytes": "N*K/2 values + N*K/8 metadata + scales read, N*K*2 written"},
-    }
+
+def gemm_bytes(w):
+    """Operands read once + Y written: values, metadata, activations, scales, side operands."""
+    side = 2 * w.r * (w.M + w.N)
+    return (w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.K + 2 * w.M * w.N + side
+            + 4 * (n_scales(w.K, w.gk, w.M, w.gM) + n_scales(w.K, w.gk, w.N, w.gN)))
+
+
+def pair_kernel_applies(w):
+    """The library's SM-pair rules: plain scaling above 192 tokens (side rank
+    at most 64), group-wise above 64 tokens with whole two-block stages."""
+    if w.N % 256 != 0:
+        return False
+    if w.gk == w.K:
+        return w.r <= 64 and w.M > 192
+    return w.gk == 128 and w.K > 128 and w.r == 0 and w.M > 64 and (w.K // 128) % 2 == 0
+
+
+def spread(ms_list, per=1):
+    """Median, min and max of per-launch times (ms) from a list of replay times."""
+    v = sorted(x / per for x in ms_list)
+    return {"ms": round(statistics.median(v), 5), "ms_min": round(v[0], 5), "ms_max": round(v[-1], 5),
+            "replays": len(v)}
+
+
+def tensor_entry(w, t, peak_fp8_dense, peak_bf16):
+    """Roofline of a tensor-bound GEMM: algorithmic flops (kept weights only)
+    against the fp8 dense peak, plus the side GEMM's bf16 flops against the
+    bf16 peak (the combined roofline time of the fused kernel)."""
+    alg = w.dense_flops() / 2
+    side = 2.0 * w.M * w.N * w.r
+    t_roof = alg / (peak_fp8_dense * 1e12) + side / (peak_bf16 * 1e12)
+    return {"bound": "tensor", "achieved": round((alg + side) / (t * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "tflops_dense_equiv": round(w.dense_flops() / (t * 1e-3) / 1e12, 1),
+            "frac": round(t_roof / (t * 1e-3), 4)}
+
+
+def hbm_entry(nbytes, t, peak_hbm):
+    gbs = nbytes / (t * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak_hbm, 4),
+            "bytes": int(nbytes)}
 
 
 def peaks():
@@ -215,7 +202,296 @@ def dist_env():
     return rank, world, local
 
 
+def rank_workload(w, world, rank, multi):
+    """This rank's share of the workload.  split: the weight rows of
+    shard.shard_rows (whole 128-row tiles) with the full activations, a
+    disjoint block of Y's columns and no exchange; replicas: the whole
+    layer on a batch of its own."""
+    if world == 1:
+        return w, (0, w.N)
+    if multi == "split":
+        from semi_structured_sparse_gb300 import shard
+        a, b = shard.shard_rows(w.N, world, rank)
+        return inputs.with_shape(w, N=b - a), (a, b)
+    return inputs.with_shape(w, seed=w.seed + 1000 * rank), (0, w.N)
+
+
 # ------------------------------------------------------------- our GPU arm
+class Bench:
+    """Device-resident rotating input sets of one workload and graph timing."""
+
+    def __init__(self, sp24, w, dev, stream, X=None, W=None, X2=None, W2=None, weights_from=None):
+        self.sp24, self.w, self.dev, self.stream = sp24, w, dev, stream
+        if X is None:
+            X, W, X2, W2 = inputs.generate(w)
+        self.X, self.W, self.X2, self.W2 = X, W, X2, W2
+        gk = w.gk
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.set_bytes = (w.N * w.K * 2 + w.M * w.K + w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.N * 2)
+        gemm_operands = w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.K
+        if weights_from is not None:
+            # decode token counts share the weight sets of one workload: only the
+            # activations and outputs are per set
+            self.nsets = weights_from.nsets
+        else:
+            # enough sets that both the compress inputs and the GEMM operands
+            # of the other sets exceed 3x L2 between two uses of a set
+            self.nsets = max(2, -(-3 * l2 // self.set_bytes), -(-3 * l2 // gemm_operands))
+        self.l2 = l2
+        self.xq0, self.sx0 = sp24.quantize_act(X.to(dev), gk)
+        Wd = None if weights_from is not None else W.to(dev)
+        self.sets = []
+        for i in range(self.nsets):
+            if weights_from is not None:
+                src = weights_from.sets[i]
+                s = {k: src[k] for k in ("W", "v", "m", "sw")}
+            else:
+                s = {"W": Wd.clone(),
+                     "v": torch.empty((w.N, w.K // 2), dtype=torch.uint8, device=dev),
+                     "m": torch.empty((w.N, w.K // 8), dtype=torch.uint8, device=dev),
+                     "sw": torch.empty((w.K // gk, (w.N + w.gN - 1) // w.gN), dtype=torch.float32, device=dev)}
+            s.update({"xq": self.xq0.clone(), "sx": self.sx0.clone(),
+                      "y": torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev),
+                      "x2": None if X2 is None else X2.to(dev), "w2": None if W2 is None else W2.to(dev)})
+            self.sets.append(s)
+        self.ws_bytes = sp24.workspace_size(w.M, w.N, w.K, w.r)
+        self.ws = torch.zeros(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
+        if weights_from is None:
+            for s in self.sets:
+                self.compress(s)
+        torch.cuda.synchronize()
+
+    def compress(self, s):
+        w = self.w
+        self.sp24.compress(s["W"], w.gN, w.gk, out=(s["v"], s["m"], s["sw"]))
+
+    def gemm(self, s):
+        w = self.w
+        self.sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, w.gk, s["x2"], s["w2"],
+                       out=s["y"], workspace=self.ws)
+
+    def step(self, s):
+        self.compress(s)
+        self.gemm(s)
+
+    def capture(self, fn, n, offset=0):
+        """A CUDA graph of n calls fn(set) over the rotating sets: replayed, the
+        kernels run back to back with their programmatic-launch edges."""
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(self.dev)
+        cs.wait_stream(self.stream)
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                for i in range(n):
+                    fn(self.sets[(offset + i) % self.nsets])
+        self.stream.wait_stream(cs)
+        torch.cuda.synchronize()
+        return g
+
+    def time_replays(self, g, reps):
+        """Replay g reps times, one event pair per replay on the launching stream."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        g.replay()  # warm, untimed
+        torch.cuda.synchronize()
+        ev[0].record(self.stream)
+        for i in range(reps):
+            g.replay()
+            ev[i + 1].record(self.stream)
+        torch.cuda.synchronize()
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+
+    def time_kernel(self, fn, n, reps=REPLAYS):
+        for i in range(3):
+            fn(self.sets[i % self.nsets])
+        torch.cuda.synchronize()
+        g = self.capture(fn, n)
+        r = self.time_replays(g, reps)
+        self.sp24.last_device_error()
+        return spread(r, n)
+
+
+def gemm_schedule(sp24, w, ws_bytes):
+    if pair_kernel_applies(w):
+        return "sp24_gemm_pair_kernel", "whole tiles"
+    if w.gk != w.K or w.r:
+        return "sp24_gemm_kernel", "whole tiles"
+    mode, cs = sp24.decomposition_of(w.M, w.N, w.K, w.r)
+    sched = {sp24.DECOMP_STREAM_K: "stream-K" if ws_bytes else "whole tiles",
+             sp24.DECOMP_CLUSTER_SPLIT: "cluster split-K, %d CTAs per tile" % cs}.get(mode, "whole tiles")
+    return "sp24_gemm_kernel", sched
+
+
+def other_configs(sp24, dev, stream, headline, pk, n):
+    """Every configuration's kernels, each alone (a graph of n launches over
+    rotating sets larger than L2, replayed REPLAYS times): the Llama-style
+    linear (GEMM, compress), the fused side GEMM, the decode sweep (GEMM at
+    every token count, compress of its weight), plus the headline workload's
+    own kernels, which the caller adds."""
+    fp8 = pk["bf16_tflops"] * FP8_OVER_BF16
+    out = {}
+
+    def gemm_row(name, b, wl):
+        t = b.time_kernel(b.gemm, n)
+        kern, sched = gemm_schedule(sp24, b.w, b.ws_bytes)
+        row = dict(t, kernel=kern, schedule=sched, M=b.w.M, N=b.w.N, K=b.w.K)
+        if b.w.M > 64:
+            row.update(tensor_entry(b.w, t["ms"], fp8, pk["bf16_tflops"]))
+        else:
+            row.update(hbm_entry(gemm_bytes(b.w), t["ms"], pk["hbm_gbs"]))
+        row["traffic"] = captured_traffic(wl, b.w, "gemm")
+        out[name] = row
+
+    def compress_row(name, b, wl):
+        t = b.time_kernel(b.compress, n)
+        kern = "compress_blocks_kernel" if b.w.gN == 128 else "compress_rows_kernel"
+        out[name] = dict(t, kernel=kern, N=b.w.N, K=b.w.K, traffic=captured_traffic(wl, b.w, "compress"),
+                         **hbm_entry(compress_bytes(b.w), t["ms"], pk["hbm_gbs"]))
+
+    for wl in ("llama", "fused"):
+        if wl == headline:
+            continue
+        b = Bench(sp24, inputs.WORKLOADS[wl], dev, stream)
+        gemm_row(wl + "_gemm", b, wl)
+        if wl == "llama":
+            compress_row("llama_compress", b, wl)
+        del b
+    if headline != "groupwise":
+        b = Bench(sp24, inputs.WORKLOADS["groupwise"], dev, stream)
+        gemm_row("groupwise_gemm", b, "groupwise")
+        compress_row("groupwise_compress", b, "groupwise")
+        del b
+    base = None
+    for M in inputs.DECODE_M:
+        wd = inputs.with_shape(inputs.WORKLOADS["decode"], M=M)
+        if base is None:
+            base = Bench(sp24, wd, dev, stream)
+            compress_row("decode_compress", base, "decode")
+            b = base
+        else:
+            X, _, _, _ = inputs.generate(wd) if M != base.w.M else (base.X, None, None, None)
+            b = Bench(sp24, wd, dev, stream, X=X, W=base.W, weights_from=base)
+        gemm_row("decode_gemm_M%d" % M, b, "decode")
+    torch.cuda.synchronize()
+    return out
+
+
+def next_rows(sp24, b, pk, n):
+    """The §8(f) kernels on the headline workload, each alone: the GEMM with a
+    bf16 bias, a batch of 4 problems, activation quantization from bf16, and
+    the GPU dequantize."""
+    w, sets, gk = b.w, b.sets, b.w.gk
+    dev = sets[0]["y"].device
+    bias = [torch.randn(w.N, device=dev).to(torch.bfloat16) for _ in sets]
+    xb = [torch.randn(w.M, w.K, device=dev).to(torch.bfloat16) for _ in sets]
+    qx = [(torch.empty_like(s["xq"]), torch.empty_like(s["sx"])) for s in sets]
+    dq = [torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev) for _ in sets]
+    idx = {id(s): i for i, s in enumerate(sets)}
+
+    def gemm_bias(s):
+        sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"],
+                  workspace=b.ws, bias=bias[idx[id(s)]])
+
+    t_bias = b.time_kernel(gemm_bias, n)
+    L = 4
+    s0 = sets[0]
+    bx = s0["xq"].unsqueeze(0).repeat(L, 1, 1)
+    bsx = s0["sx"].unsqueeze(0).repeat(L, 1, 1)
+    bv = s0["v"].unsqueeze(0).repeat(L, 1, 1)
+    bm = s0["m"].unsqueeze(0).repeat(L, 1, 1)
+    bsw = s0["sw"].unsqueeze(0).repeat(L, 1, 1)
+    by = torch.empty((L, w.M, w.N), dtype=torch.bfloat16, device=dev)
+    bws = torch.zeros(max(16, L * sp24.workspace_size(w.M, w.N, w.K)), dtype=torch.uint8, device=dev)
+    t_batch = b.time_kernel(lambda s: sp24.gemm_batched(bx, bsx, bv, bm, bsw, w.gM, w.gN, gk, out=by,
+                                                        workspace=bws), max(3, n // 4))
+    t_q = b.time_kernel(lambda s: sp24.quantize_act(xb[idx[id(s)]], gk, out=qx[idx[id(s)]]), n)
+    t_d = b.time_kernel(lambda s: sp24.decompress(s["v"], s["m"], s["sw"], w.gN, gk, out=dq[idx[id(s)]]), n)
+    q_bytes = w.M * w.K * 2 + w.M * w.K + 4 * n_scales(w.K, gk, w.M, 1)
+    d_bytes = w.N * w.K // 2 + w.N * w.K // 8 + 4 * n_scales(w.K, gk, w.N, w.gN) + 2 * w.N * w.K
+    fp8 = pk["bf16_tflops"] * FP8_OVER_BF16
+    return {
+        "gemm_with_bias": dict(t_bias, **tensor_entry(w, t_bias["ms"], fp8, pk["bf16_tflops"])),
+        "gemm_batched": dict(t_batch, L=L, **tensor_entry(inputs.with_shape(w, M=L * w.M), t_batch["ms"], fp8,
+                                                             pk["bf16_tflops"])),
+        "quantize_act_bf16": dict(t_q, **hbm_entry(q_bytes, t_q["ms"], pk["hbm_gbs"]),
+                                  counts="M*K*2 read + M*K + scales written"),
+        "decompress": dict(t_d, **hbm_entry(d_bytes, t_d["ms"], pk["hbm_gbs"]),
+                           counts="N*K/2 values + N*K/8 metadata + scales read, N*K*2 written"),
+    }
+
+
+def e2e_pass(sp24, b, steps, warm, pg):
+    """End to end through the public API with host buffers: every step uploads
+    its inputs from pinned host memory and downloads its output.  Two buffer
+    sets and two copy streams let step i + 1's upload and step i - 1's
+    download overlap step i's kernels; each step still moves all its bytes."""
+    w, dev, stream = b.w, b.dev, b.stream
+    pin_W = b.W.pin_memory()
+    pin_xq = b.xq0.cpu().pin_memory()
+    pin_sx = b.sx0.cpu().pin_memory()
+    pin_x2 = None if b.X2 is None else b.X2.pin_memory()
+    pin_w2 = None if b.W2 is None else b.W2.pin_memory()
+    pin_y = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    bufs = b.sets[:2]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of set i uploaded
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # kernels on set i finished (inputs free, output ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # output of set i downloaded
+    used = [False, False]
+
+    def one(i):
+        k = i % 2
+        s = bufs[k]
+        with torch.cuda.stream(up):
+            if used[k]:
+                up.wait_event(ev_done[k])  # the previous step on this set has read its inputs
+            s["W"].copy_(pin_W, non_blocking=True)
+            s["xq"].copy_(pin_xq, non_blocking=True)
+            s["sx"].copy_(pin_sx, non_blocking=True)
+            if pin_x2 is not None:
+                s["x2"].copy_(pin_x2, non_blocking=True)
+                s["w2"].copy_(pin_w2, non_blocking=True)
+            ev_in[k].record(up)
+        stream.wait_event(ev_in[k])
+        if used[k]:
+            stream.wait_event(ev_out[k])  # this set's previous output has been downloaded
+        b.step(s)
+        ev_done[k].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[k])
+            pin_y[k].copy_(s["y"], non_blocking=True)
+            ev_out[k].record(down)
+        used[k] = True
+
+    i = 0
+    for _ in range(warm):
+        one(i)
+        i += 1
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    e0.record(stream)
+    up.wait_stream(stream)
+    for _ in range(steps):
+        one(i)
+        i += 1
+    stream.wait_stream(down)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = (pin_W.numel() * 2 + pin_xq.numel() + pin_sx.numel() * 4
+           + (0 if pin_x2 is None else pin_x2.numel() * 2 + pin_w2.numel() * 2))
+    return ms, int(h2d), int(pin_y[0].numel() * 2)
+
+
+def replay_split(steps):
+    """Steps per timed replay: REPLAYS replays (fewer if K is smaller) whose
+    step counts add up to exactly K."""
+    r = max(1, min(REPLAYS, steps))
+    q, extra = divmod(steps, r)
+    return [q + (1 if i < extra else 0) for i in range(r)]
+
+
 def run_ours(args):
     import semi_structured_sparse_gb300 as sp24
 
@@ -227,262 +503,171 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
         pg = dist
     sp24.load(build_if_missing=(world == 1))
-    w = inputs.WORKLOADS[args.workload]
+    w0 = inputs.WORKLOADS[args.workload]
     if args.workload == "decode":
-        w = inputs.with_shape(w, M=args.decode_m, N=args.decode_n, K=args.decode_k)
-    w = inputs.with_shape(w, seed=w.seed + 1000 * rank)  # each replica its own batch
-    gk = w.gk
-    X, W, X2, W2 = inputs.generate(w)
+        w0 = inputs.with_shape(w0, M=args.decode_m, N=args.decode_n, K=args.decode_k)
+    w, rows = rank_workload(w0, world, rank, args.multi)
     dev = torch.device("cuda", local)
-
-    # rotating input sets so that the working set exceeds L2 between reuses
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    set_bytes = (w.N * w.K * 2 + w.M * w.K + w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.N * 2)
-    nsets = max(2, -(-3 * l2 // set_bytes))
-    Wd = W.to(dev)
-    xq0, sx0 = sp24.quantize_act(X.to(dev), gk)
-    sets = []
-    for i in range(nsets):
-        s = {
-            "W": Wd.clone(), "xq": xq0.clone(), "sx": sx0.clone(),
-            "v": torch.empty((w.N, w.K // 2), dtype=torch.uint8, device=dev),
-            "m": torch.empty((w.N, w.K // 8), dtype=torch.uint8, device=dev),
-            "sw": torch.empty((w.K // gk, (w.N + w.gN - 1) // w.gN), dtype=torch.float32, device=dev),
-            "y": torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev),
-            "x2": None if X2 is None else X2.to(dev), "w2": None if W2 is None else W2.to(dev),
-        }
-        sets.append(s)
     stream = torch.cuda.current_stream()
-    ws_bytes = sp24.workspace_size(w.M, w.N, w.K, w.r)
-    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-
-    def step(s):
-        sp24.compress(s["W"], w.gN, gk, out=(s["v"], s["m"], s["sw"]))
-        sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"],
-                  workspace=ws)
+    if world > 1 and args.multi == "split":
+        # this rank's rows of the one layer's weight, with the full activations
+        X, W, X2, W2 = inputs.generate(w0)
+        a, e = rows
+        b = Bench(sp24, w, dev, stream, X=X, W=W[a:e].contiguous(), X2=X2,
+                  W2=None if W2 is None else W2[a:e].contiguous())
+    else:
+        b = Bench(sp24, w, dev, stream)
 
     for i in range(args.warmup):
-        step(sets[i % nsets])
+        b.step(b.sets[i % b.nsets])
     torch.cuda.synchronize()
     sp24.last_device_error()
 
-    def capture(fn):
-        """A CUDA graph of fn()'s launches: replayed, the kernels run back to back
-        with their programmatic-launch edges, without the host in between."""
-        g = torch.cuda.CUDAGraph()
-        cs = torch.cuda.Stream(dev)
-        cs.wait_stream(stream)
-        with torch.cuda.stream(cs):
-            with torch.cuda.graph(g, stream=cs):
-                fn()
-        stream.wait_stream(cs)
-        torch.cuda.synchronize()
-        return g
-
-    def compress_only(s):
-        sp24.compress(s["W"], w.gN, gk, out=(s["v"], s["m"], s["sw"]))
-
-    def gemm_only(s):
-        sp24.gemm(s["xq"], s["sx"], s["v"], s["m"], s["sw"], w.gM, w.gN, gk, s["x2"], s["w2"], out=s["y"],
-                  workspace=ws)
-
-    g_steps = capture(lambda: [step(sets[i % nsets]) for i in range(args.steps)])
-    g_comp = capture(lambda: [compress_only(sets[i % nsets]) for i in range(args.steps)])
-    g_gemm = capture(lambda: [gemm_only(sets[i % nsets]) for i in range(args.steps)])
-    for g in (g_steps, g_comp, g_gemm):  # warm replays, untimed
+    # the timed steps: exactly K whole steps, cut into replays of graphs whose
+    # step counts add up to K (one event pair per replay)
+    split = replay_split(args.steps)
+    graphs, off = [], 0
+    for k in split:
+        graphs.append(b.capture(b.step, k, offset=off))
+        off += k
+    n_k = max(args.steps, 3)
+    g_comp = b.capture(b.compress, n_k)
+    g_gemm = b.capture(b.gemm, n_k)
+    for g in graphs + [g_comp, g_gemm]:  # warm replays, untimed
         g.replay()
     torch.cuda.synchronize()
     sp24.last_device_error()
 
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
     with ClockSampler(local) as clk:
         # keep the GPU busy ~1 s so the clock samples see it under load, untimed
         t_end = time.time() + (0.0 if args.quick else 1.0)
         i = 0
         while time.time() < t_end:
-            g_steps.replay()
+            graphs[0].replay()
             i += 1
-            if i % 8 == 0:
+            if i % 4 == 0:
                 torch.cuda.synchronize()
         if pg:
             pg.barrier()
         torch.cuda.synchronize()
-        # the timed region: K whole steps back to back, replayed from a CUDA
-        # graph, nothing between the kernels (an event between two launches
-        # would stop the next kernel's prologue from overlapping the previous
-        # kernel's tail)
-        start.record(stream)
-        g_steps.replay()
-        stop.record(stream)
+        ev[0].record(stream)
+        for j, g in enumerate(graphs):
+            g.replay()
+            ev[j + 1].record(stream)
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
-        # per-kernel durations for the roofline: each kernel on its own, K
-        # launches back to back over the same rotating input sets, one event
-        # pair per kernel pass on the launching stream (an event pair around
-        # every launch would also time the launch gap it creates)
-        kev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        kev[0].record(stream)
-        g_comp.replay()
-        kev[1].record(stream)
-        g_gemm.replay()
-        kev[2].record(stream)
-        torch.cuda.synchronize()
+        # each kernel alone for the roofline: a graph of launches over the
+        # same rotating sets, replayed REPLAYS times between event pairs
+        t_comp = spread(b.time_replays(g_comp, REPLAYS), n_k)
+        t_gemm = spread(b.time_replays(g_gemm, REPLAYS), n_k)
     sp24.last_device_error()
-    ms = start.elapsed_time(stop)
-    t_comp = kev[0].elapsed_time(kev[1]) / args.steps
-    t_gemm = kev[1].elapsed_time(kev[2]) / args.steps
+    per_step = sorted(ev[j].elapsed_time(ev[j + 1]) / k for j, k in enumerate(split))
+    total_ms = sum(ev[j].elapsed_time(ev[j + 1]) for j in range(len(split)))
+    ms_step = statistics.median(per_step)
     if pg:
-        t = torch.tensor([ms], device=dev)
+        t = torch.tensor([ms_step, total_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_step = ms / args.steps
+        ms_step, total_ms = float(t[0].item()), float(t[1].item())
 
-    # end to end through the public API with host buffers: every step uploads
-    # its inputs from pinned host memory and downloads its output.  Two buffer
-    # sets and two copy streams let step i + 1's upload and step i - 1's
-    # download overlap step i's kernels; each step still moves all its bytes.
-    pin_W = W.pin_memory()
-    pin_xq = xq0.cpu().pin_memory()
-    pin_sx = sx0.cpu().pin_memory()
-    pin_x2 = None if X2 is None else X2.pin_memory()
-    pin_w2 = None if W2 is None else W2.pin_memory()
-    pin_y = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    bufs = sets[:2]
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of set b uploaded
-    ev_done = [torch.cuda.Event() for _ in range(2)]  # kernels on set b finished (inputs free, output ready)
-    ev_out = [torch.cuda.Event() for _ in range(2)]   # output of set b downloaded
-    used = [False, False]
+    e2e_ms, h2d, d2h = (None, 0, 0)
+    if not args.quick:
+        e2e_ms, h2d, d2h = e2e_pass(sp24, b, max(3, min(args.steps, 20)), max(3, args.warmup), pg)
+        if pg:
+            t = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
 
-    def e2e_step(i):
-        b = i % 2
-        s = bufs[b]
-        with torch.cuda.stream(up):
-            if used[b]:
-                up.wait_event(ev_done[b])  # the previous step on this set has read its inputs
-            s["W"].copy_(pin_W, non_blocking=True)
-            s["xq"].copy_(pin_xq, non_blocking=True)
-            s["sx"].copy_(pin_sx, non_blocking=True)
-            if pin_x2 is not None:
-                s["x2"].copy_(pin_x2, non_blocking=True)
-                s["w2"].copy_(pin_w2, non_blocking=True)
-            ev_in[b].record(up)
-        stream.wait_event(ev_in[b])
-        if used[b]:
-            stream.wait_event(ev_out[b])  # this set's previous output has been downloaded
-        step(s)
-        ev_done[b].record(stream)
-        with torch.cuda.stream(down):
-            down.wait_event(ev_done[b])
-            pin_y[b].copy_(s["y"], non_blocking=True)
-            ev_out[b].record(down)
-        used[b] = True
-
-    n_e2e = 0
-    for _ in range(0 if args.quick else max(3, args.warmup)):
-        e2e_step(n_e2e)
-        n_e2e += 1
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = 1 if args.quick else max(3, min(args.steps, 50))
-    if pg:
-        pg.barrier()
-    e0.record(stream)
-    up.wait_stream(stream)
-    for _ in range(e2e_steps):
-        e2e_step(n_e2e)
-        n_e2e += 1
-    stream.wait_stream(down)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    h2d = (pin_W.numel() * 2 + pin_xq.numel() + pin_sx.numel() * 4
-           + (0 if pin_x2 is None else pin_x2.numel() * 2 + pin_w2.numel() * 2))
-    d2h = pin_y[0].numel() * 2
-
-    flops = w.dense_flops()
-    alg_flops = flops / 2  # only kept weights are multiplied
     pk = peaks()
-    extra = None if args.quick else next_rows(sp24, w, gk, sets, stream, ws, args.steps, pk)
-    fp8_dense_peak = pk["bf16_tflops"] * FP8_OVER_BF16
-    comp_bytes = w.N * w.K * 2 + w.N * w.K // 2 + w.N * w.K // 8 + 4 * (w.K // gk) * ((w.N + w.gN - 1) // w.gN)
-    gemm_bytes = (w.N * w.K // 2 + w.N * w.K // 8 + w.M * w.K + 2 * w.M * w.N
-                  + 4 * (w.K // gk) * (w.M + (w.N + w.gN - 1) // w.gN))
-    gemm_tflops_alg = alg_flops / (t_gemm * 1e-3) / 1e12
-    comp_gbs = comp_bytes / (t_comp * 1e-3) / 1e9
-    gemm_tflops_dense = 2 * gemm_tflops_alg
-    # the library's SM-pair rules: plain scaling above 192 tokens, group-wise above 64 with whole stages
-    pair = (w.gk == w.K and w.r <= 64 and w.M > 192 and w.N % 256 == 0) or \
-        (w.gk == 128 and w.K > 128 and w.r == 0 and w.M > 64 and w.N % 256 == 0 and (w.K // 128) % 2 == 0)
-    gemm_kernel = "sp24_gemm_pair_kernel" if pair else "sp24_gemm_kernel"
-    if pair or w.gk != w.K:
-        gemm_schedule = "whole tiles"
+    fp8 = pk["bf16_tflops"] * FP8_OVER_BF16
+    # units of work: the whole layer's flops when the ranks split it, each
+    # replica's own batch otherwise
+    job_flops = w0.dense_flops() if (world > 1 and args.multi == "split") else world * w.dense_flops()
+    kern, sched = gemm_schedule(sp24, w, b.ws_bytes)
+    gemm_row = dict(t_gemm, kernel=kern, schedule=sched, M=w.M, N=w.N, K=w.K,
+                    traffic=captured_traffic(args.workload, w, "gemm"),
+                    **(tensor_entry(w, t_gemm["ms"], fp8, pk["bf16_tflops"]) if w.M > 64
+                       else hbm_entry(gemm_bytes(w), t_gemm["ms"], pk["hbm_gbs"])))
+    comp_kernel = "compress_blocks_kernel" if w.gN == 128 else "compress_rows_kernel"
+    comp_row = dict(t_comp, kernel=comp_kernel, N=w.N, K=w.K, traffic=captured_traffic(args.workload, w, "compress"),
+                    **hbm_entry(compress_bytes(w), t_comp["ms"], pk["hbm_gbs"]))
+    kernels = {args.workload + "_gemm": gemm_row, args.workload + "_compress": comp_row}
+    extra = None
+    if world == 1 and not args.quick:
+        kernels.update(other_configs(sp24, dev, stream, args.workload, pk, n_k))
+        extra = next_rows(sp24, b, pk, n_k)
+    # the dominant kernel of the step
+    if t_gemm["ms"] >= t_comp["ms"]:
+        g = gemm_row
+        if g["bound"] == "tensor":
+            roofline = {"kernel": g["kernel"], "bound": "tensor", "achieved": g["achieved"], "peak": round(fp8, 1),
+                        "unit": "TFLOP/s", "frac": g["frac"], "traffic": g["traffic"],
+                        "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16), of %s" % (
+                            pk["source"], FP8_OVER_BF16, pk["source"]),
+                        "achieved_counts": "algorithmic 2*M*N*K/2 flops (kept weights only) per launch",
+                        "ms": g["ms"]}
+        else:
+            roofline = {"kernel": g["kernel"], "bound": "hbm", "achieved": g["achieved"],
+                        "peak": round(pk["hbm_gbs"], 1), "unit": "GB/s", "frac": g["frac"], "traffic": g["traffic"],
+                        "peak_source": "%s copy bandwidth, of %s" % (pk["source"], pk["source"]),
+                        "achieved_counts": "algorithmic bytes per launch: operands read once, Y written",
+                        "ms": g["ms"]}
     else:
-        mode, cs = sp24.decomposition_of(w.M, w.N, w.K, w.r)
-        gemm_schedule = {sp24.DECOMP_STREAM_K: "stream-K" if ws_bytes else "whole tiles",
-                         sp24.DECOMP_CLUSTER_SPLIT: "cluster split-K, %d CTAs per tile" % cs}.get(mode, "whole tiles")
-    if t_gemm >= t_comp:
-        roofline = {"kernel": gemm_kernel, "bound": "tensor", "achieved": round(gemm_tflops_alg, 1),
-                    "peak": round(fp8_dense_peak, 1), "unit": "TFLOP/s",
-                    "frac": round(gemm_tflops_alg / fp8_dense_peak, 4),
-                    "traffic": captured_traffic(args.workload, w, "gemm"),
-                    "peak_source": "%s bf16 burst x %.0f (nominal fp8/bf16), of %s" % (
-                        pk["source"], FP8_OVER_BF16, pk["source"]),
-                    "achieved_counts": "algorithmic 2*M*N*K/2 flops (kept weights only) per launch"}
-    else:
-        comp_kernel = "compress_blocks_kernel" if w.gN == 128 else "compress_rows_kernel"
-        roofline = {"kernel": comp_kernel, "bound": "hbm", "achieved": round(comp_gbs, 1),
-                    "peak": round(pk["hbm_gbs"], 1), "unit": "GB/s", "frac": round(comp_gbs / pk["hbm_gbs"], 4),
-                    "traffic": captured_traffic(args.workload, w, "compress"),
+        roofline = {"kernel": comp_kernel, "bound": "hbm", "achieved": comp_row["achieved"],
+                    "peak": round(pk["hbm_gbs"], 1), "unit": "GB/s", "frac": comp_row["frac"],
+                    "traffic": comp_row["traffic"],
                     "peak_source": "%s copy bandwidth, of %s" % (pk["source"], pk["source"]),
-                    "achieved_counts": "algorithmic bytes per launch: W read + values, metadata, scales written"}
+                    "achieved_counts": "algorithmic bytes per launch: W read + values, metadata, scales written",
+                    "ms": comp_row["ms"]}
+    mode = "single" if world == 1 else ("split along N, %d rows on rank 0" % (rows[1] - rows[0])
+                                        if args.multi == "split" else "replicas")
     out = {
         "metric": METRIC,
-        "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2),
+        "value": round(job_flops / (ms_step * 1e-3) / 1e12, 2),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
+        "ms_per_step_spread": {"min": round(per_step[0], 5), "max": round(per_step[-1], 5),
+                               "mean": round(total_ms / args.steps, 5), "replays": len(split)},
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if (world > 1 and args.multi == "split") else "weak",
         "vs_baseline": None,
         "dtype": "e4m3",
         "data": "synthetic",
-        "config": {"workload": DESCR[args.workload].format(N=w.N, K=w.K), "M": w.M, "N": w.N, "K": w.K,
-                   "scales": {"gM": w.gM, "gN": w.gN, "gK": gk}, "side_r": w.r,
-                   "step": "compress(W) + sparse GEMM", "flops_per_step": "2*M*N*K dense-equivalent",
-                   "l2": "rotating %d input sets of %.1f MB (> L2 %.0f MB)" % (nsets, set_bytes / 1e6, l2 / 1e6),
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "timing": "value: K back-to-back steps replayed from one CUDA graph between one event pair; "
-                             "kernels/roofline: each kernel alone, a graph of K launches over the same rotating "
-                             "sets between one event pair; e2e: eager calls through the public API"},
-        "kernels": {
-            "gemm": {"ms": round(t_gemm, 5), "tflops_dense_equiv": round(gemm_tflops_dense, 1),
-                     "frac_fp8_sparse_peak": round(gemm_tflops_alg / fp8_dense_peak, 4),
-                     "kernel": gemm_kernel, "schedule": gemm_schedule},
-            "compress": {"ms": round(t_comp, 5), "gbs": round(comp_gbs, 1),
-                         "frac_hbm": round(comp_gbs / pk["hbm_gbs"], 4)},
-        },
+        "config": config_dict(args.workload, w0, mode),
+        "input_sets": {"sets": b.nsets, "mb_per_set": round(b.set_bytes / 1e6, 1), "l2_mb": round(b.l2 / 1e6, 1)},
+        "kernels": kernels,
         "roofline": roofline,
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
-                "pipelining": "two buffer sets; step i+1's upload and step i-1's download overlap step i"},
+        "e2e": None if e2e_ms is None else {
+            "value": round(job_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "pipelining": "two buffer sets; step i+1's upload and step i-1's download overlap step i"},
         "next_rows": extra,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.quick):
-        out["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = cpu_baseline(w0, budget_s=args.cpu_budget)
     if pg:
         pg.destroy_process_group()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def config_dict(workload, w, parallelism):
+    """The workload and timing description, the same in both arms."""
+    l2_text = ("inputs larger than L2: rotating input sets, the GEMM operands and the compress inputs "
+               "of the other sets each exceed 3x L2 between two uses of a set")
+    return {"workload": DESCR[workload].format(N=w.N, K=w.K), "M": w.M, "N": w.N, "K": w.K,
+            "scales": {"gM": w.gM, "gN": w.gN, "gK": w.gk}, "side_r": w.r,
+            "step": "compress(W) + sparse GEMM", "flops_per_step": "2*M*N*K dense-equivalent",
+            "l2": l2_text, "parallelism": parallelism,
+            "timing": "value: exactly K steps, as %d CUDA-graph replays between event pairs, median per-step "
+                      "time; kernels/roofline: each kernel alone, a graph of launches over the same rotating "
+                      "sets, median of %d replays; e2e: eager calls through the public API" % (REPLAYS, REPLAYS)}
 
 
 # ------------------------------------------------------------ oracle (CPU)
@@ -490,8 +675,6 @@ def cpu_step_estimate(w: inputs.Workload, budget_s: float):
     """Time the oracle on a bounded sample of the workload and scale it to one
     whole step (compress all of W + GEMM of all M tokens).
     Returns (seconds per step, description, threads)."""
-    import numpy as np
-
     import oracle
     X, W, X2, W2 = inputs.generate(w)
     gk = w.gk
@@ -540,15 +723,15 @@ def run_reference(args):
         s, descr, threads = cpu_step_estimate(w, budget)
         if i >= args.warmup:
             secs.append(s)
-    sec = sum(secs) / len(secs)
+    sec = statistics.median(secs)
     value = w.dense_flops() / sec / 1e12
     out = {
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
+        "scaling": "strong" if (world > 1 and args.multi == "split") else "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "impl": "reference",
-        "config": {"workload": DESCR[args.workload].format(N=w.N, K=w.K), "M": w.M, "N": w.N, "K": w.K,
-                   "scales": {"gM": w.gM, "gN": w.gN, "gK": w.gk}, "side_r": w.r,
-                   "step": "compress(W) + sparse GEMM", "parallelism": "single"},
+        "config": config_dict(args.workload, w, "single" if world == 1 else (
+            "split along N" if args.multi == "split" else "replicas")),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": descr},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -556,13 +739,15 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(inputs.WORKLOADS), default="llama")
+    ap.add_argument("--workload", choices=sorted(inputs.WORKLOADS), default="groupwise")
+    ap.add_argument("--multi", choices=["split", "replicas"], default="split",
+                    help="N > 1: split the weight rows across ranks (no exchange), or run replicas")
     ap.add_argument("--decode-m", type=int, default=16)
     ap.add_argument("--decode-n", type=int, default=None,
                     help="decode workload: another weight height (default 28672)")
@@ -571,10 +756,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
-                    help="profiling runs: no clock soak, no e2e pass, no CPU baseline")
-    args = ap.parse_args()
+                    help="profiling runs: no clock soak, no e2e pass, no other configs, no CPU baseline")
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    return args
+
+
+def main():
+    args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -184,8 +184,9 @@ SP24_API sp24_status sp24_fp8_quantize_act_bf16(const void* X, int64_t M, int64_
  *           timing).  The workspace holds a launch counter, one
  *           flag per CTA and one partial tile per CTA.  Zero it once before
  *           its first use; each launch leaves it consistent for the next,
- *           whatever the shape, CUDA graph replays included (after a
- *           device error reported by sp24_last_device_error, zero it again).
+ *           whatever the shape, CUDA graph replays included, and a launch
+ *           that gave up on a wait (SP24_ERR_DEVICE_TIMEOUT) as well: every
+ *           CTA counts itself out of the launch counter before it exits.
  *           Calls that overlap on the GPU must not share it.  With less than the
  *           queried size the call runs with whole tiles per CTA.
  * Preconditions: M >= 1; N a positive multiple of 128; K a positive multiple
@@ -237,14 +238,18 @@ SP24_API sp24_status sp24_fp8_gemm_batched(const void* Xq, const float* sx, int6
  *     exits, and all calls on a device share it: calls that overlap on the
  *     GPU (other streams, other host threads) race on it and corrupt each
  *     other's results.  Serialise them.
- *   - The first call on a device looks up the array's device address (a
- *     one-time set-up with that device current); make that first call before
- *     any stream capture.
+ *   - Every call looks up the array's device address in the current
+ *     device's context (so a context that was reset and created again gets
+ *     the new address).  The first call on a device may load the library's
+ *     device image there; make that first call before any stream capture.
  *   - A shape whose scratch need (sp24_fp8_gemm_workspace_size) exceeds
- *     8 MiB is refused with SP24_ERR_WORKSPACE (none does on a 152-SM part);
- *     shapes that need no scratch always run.
+ *     8 MiB is refused with SP24_ERR_WORKSPACE.  No shape needs that much
+ *     on parts with up to 240 SMs (the 152-SM GB300 among them): the refusal
+ *     guards larger parts.  Shapes that need no scratch always run.
  * The array starts zeroed, and the stream-K counter and flags keep it
- * consistent from call to call.
+ * consistent from call to call.  That holds after SP24_ERR_DEVICE_TIMEOUT
+ * too: a launch that gave up on a wait still counts every CTA out of the
+ * counter, so nothing is left for the caller to reset.
  */
 SP24_API sp24_status sp24_fp8_gemm_fixed_scratch(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
                                                  int gM, const void* values, const void* meta, const float* sw,

@@ -844,7 +844,7 @@ struct Plan {
 // Bytes of the stream-K control region: the launch counter, then one flag per
 // possible CTA (at most one per SM), rounded up to 1 KiB.  It depends on the
 // device only, so every shape finds its counter and flags at the same place.
-size_t streamk_ctrl_bytes(int sm_count) {
+constexpr size_t streamk_ctrl_bytes(int sm_count) {
   return (64 + 8 * static_cast<size_t>(sm_count) + 1023) & ~size_t(1023);
 }
 
@@ -1154,22 +1154,26 @@ namespace {
 constexpr size_t kFixedScratchBytes = size_t(8) << 20;  // 8 MiB per device
 static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
 
-std::mutex g_fixed_scratch_mutex;
-void* g_fixed_scratch_addr[64] = {};  // device address of g_fixed_scratch, per device ordinal
+// The largest stream-K scratch is the control region plus one 64-token
+// partial tile per CTA, with at most one CTA per SM (make_plan).  Every part
+// with up to kFixedScratchMaxSMs SMs (the 152-SM GB300 among them) fits the
+// array at every shape, so the refusal in the entry point is a guard for
+// larger parts; a change of tile sizes that breaks this bound fails here.
+constexpr int kFixedScratchMaxSMs = 240;
+static_assert(streamk_ctrl_bytes(kFixedScratchMaxSMs) +
+                      static_cast<size_t>(kFixedScratchMaxSMs) * 64 * BM * sizeof(float) <=
+                  kFixedScratchBytes,
+              "the fixed scratch holds every stream-K plan of a part with up to kFixedScratchMaxSMs SMs");
 
-// Device address of the scratch array on the current device.  In host code the
-// array's name is only a host-side handle; the real device address is looked up
-// once per device (with that device current) and cached.
+// Device address of the scratch array in the current device's context.  In
+// host code the array's name is only a host-side handle; the runtime maps it
+// to the device copy.  The lookup runs on every call (cheap once the
+// library's device image is loaded), so a context that was reset and created
+// again never receives a stale address.
 sp24_status fixed_scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SP24_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_fixed_scratch_mutex);
-  if (g_fixed_scratch_addr[dev] == nullptr) {
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_fixed_scratch) != cudaSuccess || addr == nullptr) return SP24_ERR_CUDA;
-    g_fixed_scratch_addr[dev] = addr;
-  }
-  *out = g_fixed_scratch_addr[dev];
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_fixed_scratch) != cudaSuccess || addr == nullptr) return SP24_ERR_CUDA;
+  *out = addr;
   return SP24_OK;
 }
 

@@ -81,3 +81,40 @@ def test_peaks_fallback_is_labelled(tmp_path, monkeypatch):
     p = bench.peaks()
     assert p["source"] == "measured" and p["hbm_gbs"] == 6780.7
     assert p["bf16_tflops_sustained"] == 1901.0
+
+
+@pytest.mark.parametrize("steps", [1, 3, 5, 7, 50, 51])
+def test_replay_split_times_exactly_k_steps(steps):
+    split = bench.replay_split(steps)
+    assert sum(split) == steps and all(k >= 1 for k in split)
+    assert len(split) == min(bench.REPLAYS, steps)
+    assert max(split) - min(split) <= 1
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    args = bench.parse_args([])
+    assert args.workload == "groupwise" and args.multi == "split"
+    big = max(inputs.WORKLOADS.values(), key=lambda w: w.dense_flops())
+    assert big.name == args.workload
+
+
+def test_both_arms_describe_the_same_config():
+    """The reference arm and the GPU arm print the same config dict: it holds
+    only the workload's description, no figure measured at run time."""
+    w = inputs.WORKLOADS["groupwise"]
+    a = bench.config_dict("groupwise", w, "single")
+    assert a == bench.config_dict("groupwise", w, "single")
+    assert a["M"] == 3000 and a["N"] == 14336 and a["scales"] == {"gM": 1, "gN": 128, "gK": 128}
+
+
+def test_algorithmic_counts():
+    w = inputs.WORKLOADS["groupwise"]
+    assert bench.compress_bytes(w) == w.N * w.K * 21 // 8 + 4 * 32 * 112
+    d = inputs.with_shape(inputs.WORKLOADS["decode"], M=16)
+    assert bench.gemm_bytes(d) == d.N * d.K * 5 // 8 + 16 * d.K + 2 * 16 * d.N + 4 * (16 + d.N)
+    fused = inputs.WORKLOADS["fused"]
+    e = bench.tensor_entry(fused, 1.0, 1000.0, 500.0)
+    alg, side = fused.dense_flops() / 2, 2.0 * fused.M * fused.N * fused.r
+    assert e["frac"] == pytest.approx(round((alg / 1e15 + side / 5e14) / 1e-3, 4))
+    assert bench.pair_kernel_applies(w) and bench.pair_kernel_applies(inputs.WORKLOADS["llama"])
+    assert not bench.pair_kernel_applies(d)

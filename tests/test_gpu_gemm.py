@@ -5,10 +5,9 @@ Inputs are the seeded synthetic workloads; both sides consume the same bytes
 element: |Y - ref| <= 1e-2 |ref| + 1e-3 with ref the oracle's fp32-accumulated
 result (the bf16 output rounding alone is <= 2^-9 |ref|).
 
-Small cases cover every output element (several tiles, ragged token tails,
-every granularity); the full-size workloads, run in the same launch
-configuration the benchmark times, are checked on sampled token rows that the
-oracle computes one by one (first, last, tile edges).
+Every test compares every output element: the small cases (several tiles,
+ragged token tails, every granularity) and the full-size workloads, run in
+the same launch configuration the benchmark times.
 """
 import numpy as np
 import pytest
@@ -191,35 +190,21 @@ def test_repeat_is_deterministic(ora, sp24):
 
 
 # ------------------------------------------------------------- full-size runs
-def _sample_rows(M, BN=128):
-    rows = {0, 1, M // 2, M - 1}
-    for t in (BN - 1, BN, 2 * BN - 1, (M // BN) * BN, (M // BN) * BN - 1):
-        if 0 <= t < M:
-            rows.add(t)
-    return sorted(rows)
-
-
 @pytest.mark.parametrize("name", ["llama", "groupwise", "fused"])
-def test_full_size_sampled(ora, sp24, name):
+def test_full_size(ora, sp24, name):
+    """The full-size workloads, in the launch configuration the benchmark
+    times, compared with the oracle on every output element."""
     w = inputs.WORKLOADS[name]
-    xq, sx, values, meta, sw, x2, w2 = _prep(ora, w)
-    y = _run_gpu(sp24, w, xq, sx, values, meta, sw, x2, w2)
-    rows = _sample_rows(w.M)
-    assert w.gM == 1
-    ref = ora.gemm(xq[rows], sx[:, rows], values, meta, sw, 1, w.gN, w.gk,
-                   None if x2 is None else x2[rows], w2)
-    assert_close(y[rows], ref, name + " sampled rows %s" % rows)
-    assert np.isfinite(y).all()
+    y, ref = _check_full(ora, sp24, w, name + " (every element)")
+    assert y.shape == (w.M, w.N) and np.isfinite(y).all()
 
 
 @pytest.mark.parametrize("M", inputs.DECODE_M)
 def test_decode_full_size(ora, sp24, M):
+    """The decode sweep's full-size weight (N 28672, K 4096) at every token
+    count of the sweep, every output element."""
     w = inputs.with_shape(inputs.WORKLOADS["decode"], M=M)
-    xq, sx, values, meta, sw, _, _ = _prep(ora, w)
-    y = _run_gpu(sp24, w, xq, sx, values, meta, sw, None, None)
-    rows = sorted({0, M - 1, M // 2})
-    ref = ora.gemm(xq[rows], sx[:, rows], values, meta, sw)
-    assert_close(y[rows], ref, "decode M=%d" % M)
+    _check_full(ora, sp24, w, "decode M=%d (every element)" % M)
 
 
 def test_compress_then_gemm_on_device(ora, sp24):

@@ -36,6 +36,39 @@ def test_shard_plan_partitions_rows():
         shard.shard_rows(200, 2, 0)
 
 
+def _bench_worker(rank, world, port, result_path):
+    """What bench.py --gpus N builds on each rank: its rows of the one layer's
+    weight (split) or the whole layer on a batch of its own (replicas)."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    import inputs
+    assert bench.dist_env()[:2] == (rank, world)
+    w0 = inputs.WORKLOADS["groupwise"]
+    w, rows = bench.rank_workload(w0, world, rank, "split")
+    r, _ = bench.rank_workload(w0, world, rank, "replicas")
+    mine = torch.tensor([rows[0], rows[1], w.M, w.N, w.K, r.N, r.seed], dtype=torch.int64)
+    got = [torch.zeros(7, dtype=torch.int64) for _ in range(world)]
+    dist.all_gather(got, mine)
+    if rank == 0:
+        np.save(result_path, torch.stack(got).numpy())
+    dist.destroy_process_group()
+
+
+def test_bench_rank_shapes_two_ranks(tmp_path):
+    world, port = 2, _free_port()
+    path = str(tmp_path / "shapes.npy")
+    mp.start_processes(_bench_worker, args=(world, port, path), nprocs=world, start_method="spawn")
+    t = np.load(path)
+    w0 = __import__("inputs").WORKLOADS["groupwise"]
+    # split: contiguous whole-tile blocks of W's rows covering N once, full M and K on every rank
+    assert t[0, 0] == 0 and t[0, 1] == t[1, 0] and t[1, 1] == w0.N
+    assert all(t[i, 3] == t[i, 1] - t[i, 0] and t[i, 3] % 256 == 0 for i in range(world))
+    assert all(t[i, 2] == w0.M and t[i, 4] == w0.K for i in range(world))
+    # replicas: the whole layer, a batch of its own per rank
+    assert all(t[i, 5] == w0.N for i in range(world)) and t[0, 6] != t[1, 6]
+
+
 def _worker(rank, world, port, result_path):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
