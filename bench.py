@@ -62,10 +62,6 @@ DESCR = {
 CAPTURED_TRAFFIC = {
     # sp24_gemm_pair_kernel<256,0,0> on the Llama-style linear (M 2048, N 4096, K 4096)
     ("llama", 2048, 4096, 4096, "gemm"): 18938880 + 0,
-    # compress_rows_kernel<0> on W[4096, 4096] (Llama-style linear), two rows per CTA
-    ("llama", 2048, 4096, 4096, "compress"): 33597696 + 9728,
-    # compress_rows_kernel<0> on W[28672, 4096] (decode workload), two rows per CTA
-    ("decode", 16, 28672, 4096, "compress"): 234962688 + 19037184,
     # sp24_gemm_kernel<16,0,0,0,4,0> (whole tiles), decode M 16, N 28672, K 4096
     ("decode", 16, 28672, 4096, "gemm"): 73602816 + 467968,
     # sp24_gemm_pair_kernel<240,1,0>, fused side GEMM M 2048, N 4096, K 4096, r 64

@@ -168,15 +168,16 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return v;
 }
 
-// Packs and stores the chunks c = h, h + 2, ... of row n (two warps per row):
-// the first kHeldChunks from registers, any further ones re-read from global.
-template <bool FAST>
+// Packs and stores the chunks c = h, h + WPR, ... of row n (WPR warps per
+// row): the first kHeldChunks from registers, any further ones re-read from
+// global.
+template <bool FAST, int WPR>
 __device__ __forceinline__ void emit_row(const uint4 (&held)[8], const uint16_t* row, int n, int K, int nchunks, int h,
                                          int lane, float s, float r, uint8_t* values, uint8_t* meta) {
   const RowStore st(n, K, lane);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int c = 2 * i + h, k = c * 256 + lane * 8;
+    const int c = WPR * i + h, k = c * 256 + lane * 8;
     if (c < nchunks && k < K) {
       uint32_t vals, mb;
       pack_chunk<FAST>(held[i], s, r, vals, mb);
@@ -184,7 +185,7 @@ __device__ __forceinline__ void emit_row(const uint4 (&held)[8], const uint16_t*
       meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
     }
   }
-  for (int c = 16 + h; c < nchunks; c += 2) {
+  for (int c = 8 * WPR + h; c < nchunks; c += WPR) {
     const int k = c * 256 + lane * 8;
     if (k < K) {
       uint32_t vals, mb;
@@ -196,14 +197,16 @@ __device__ __forceinline__ void emit_row(const uint4 (&held)[8], const uint16_t*
 }
 
 constexpr int kRowsPerCta = 8;   // gK = 128: one warp per weight row
-constexpr int kPairRowsPerCta = 2;  // gK = K: two warps per weight row (128-thread CTAs: a finer last wave)
+constexpr int kRowThreads = 128;    // gK = K: 128-thread CTAs (a finer last wave), WPR warps per weight row
 constexpr int kHeldChunks = 8;   // per warp: 8 x 16 bytes per lane stay in registers
 
-// gN = 1.  GK128 = false: one scale per row (gK = K); two warps share a row,
-// warp h of the pair owning the 256-element chunks c = h, h+2, h+4, ...; the
-// row's amax is combined through shared memory.  GK128 = true: one scale per
-// row and 128-wide K block; one warp per row, each half-warp owns a block.
-template <bool GK128>
+// gN = 1.  GK128 = false: one scale per row (gK = K); WPR warps share a row
+// (2 up to K = 4096, 4 up to 8192, 8 above, so that every chunk of rows up
+// to 16384 stays in registers), warp h owning the 256-element chunks
+// c = h, h + WPR, ...; the row's amax is combined through shared memory.
+// GK128 = true: one scale per row and 128-wide K block; one warp per row,
+// each half-warp owns a block.
+template <bool GK128, int WPR = 2>
 __global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* __restrict__ W, int N, int K, int64_t ldw,
                                                             uint8_t* __restrict__ values, uint8_t* __restrict__ meta,
                                                             float* __restrict__ scales) {
@@ -212,36 +215,38 @@ __global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* _
   pdl_wait();
 
   if (!GK128) {
-    __shared__ uint32_t pair_amax[8];
-    const int h = warp & 1;
-    const int n = blockIdx.x * kPairRowsPerCta + (warp >> 1);
+    __shared__ uint32_t warp_amax[8];
+    const int h = warp % WPR;
+    const int n = blockIdx.x * (blockDim.x / 32 / WPR) + warp / WPR;
     const bool valid = n < N;
     const uint16_t* row = W + static_cast<int64_t>(valid ? n : 0) * ldw;
     uint4 held[kHeldChunks];
     uint32_t amax2 = 0;
 #pragma unroll
     for (int i = 0; i < kHeldChunks; ++i) {
-      const int c = 2 * i + h, k = c * 256 + lane * 8;
+      const int c = WPR * i + h, k = c * 256 + lane * 8;
       if (valid && c < nchunks && k < K) {
         held[i] = ldg_stream(row + k);
         amax2 = amax2_acc(amax2, held[i]);
       }
     }
-    for (int c = 2 * kHeldChunks + h; valid && c < nchunks; c += 2) {  // rows longer than 4096: stream for amax
+    for (int c = WPR * kHeldChunks + h; valid && c < nchunks; c += WPR) {  // longer rows: stream for amax
       const int k = c * 256 + lane * 8;
       if (k < K) amax2 = amax2_acc(amax2, ldg_stream(row + k));
     }
     uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, amax2_bits(amax2));
-    if (lane == 0) pair_amax[warp] = amax;
+    if (lane == 0) warp_amax[warp] = amax;
     __syncthreads();
     if (!valid) return;
-    amax = max(pair_amax[warp & ~1], pair_amax[warp | 1]);
+    const int w0 = warp - h;  // the row's first warp
+#pragma unroll
+    for (int i = 0; i < WPR; ++i) amax = max(amax, warp_amax[w0 + i]);
     const float s = weight_scale(amax), r = __frcp_rn(s);
     if (lane == 0 && h == 0) scales[n] = s;
     if (s >= kMinFastScale)  // the same for the whole row: warp-uniform
-      emit_row<true>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+      emit_row<true, WPR>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
     else
-      emit_row<false>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+      emit_row<false, WPR>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
   } else {
     // lanes 0-15 cover K block 2c, lanes 16-31 block 2c+1 (when it exists)
     const int n = blockIdx.x * kRowsPerCta + warp;
@@ -299,16 +304,21 @@ __global__ void __launch_bounds__(256) compress_blocks_kernel(const uint16_t* __
   for (int w = 1; w < 8; ++w) amax = max(amax, warp_max[w]);
   const float s = weight_scale(amax), r = __frcp_rn(s);
   if (t == 0) scales[static_cast<int64_t>(kb) * (N / 128) + nb] = s;
+  // The block is exactly one storage tile, and rows r0 + 16 i share the
+  // swizzle of row r0 (it depends on (row / 2) mod 4): the stores of row
+  // r0 + 16 i land 16 * 64 bytes (values) and 16 * 16 bytes (metadata) after
+  // those of row r0.
+  uint8_t* vrow = values + values_offset(nb * 128 + r0, k / 2, K);
+  uint8_t* mrow = meta + meta_offset(nb * 128 + r0, k / 8, K);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int n = nb * 128 + r0 + 16 * i;
     uint32_t vals, mb;
     if (s >= kMinFastScale)  // the same for the whole block: CTA-uniform
       pack_chunk<true>(v[i], s, r, vals, mb);
     else
       pack_chunk<false>(v[i], s, r, vals, mb);
-    *reinterpret_cast<uint32_t*>(values + values_offset(n, k / 2, K)) = vals;
-    meta[meta_offset(n, k / 8, K)] = static_cast<uint8_t>(mb);
+    *reinterpret_cast<uint32_t*>(vrow + i * 1024) = vals;
+    mrow[i * 256] = static_cast<uint8_t>(mb);
   }
   pdl_trigger();
 }
@@ -386,10 +396,22 @@ extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, in
       return SP24_ERR_CUDA;
   } else {
     if (per_channel) {
-      const unsigned grid = static_cast<unsigned>((N + kPairRowsPerCta - 1) / kPairRowsPerCta);
-      if (launch_pdl(compress_rows_kernel<false>, dim3(grid), dim3(32 * 2 * kPairRowsPerCta), 0, s, w, (int)N, (int)K, ldw, v, m,
-                     scales) != cudaSuccess)
-        return SP24_ERR_CUDA;
+      // warps per row: enough to hold a row of up to 16384 in registers
+      const int wpr = K <= 4096 ? 2 : (K <= 8192 ? 4 : 8);
+      const int rows_per_cta = wpr <= 4 ? kRowThreads / 32 / wpr : 1;
+      const unsigned threads = wpr <= 4 ? kRowThreads : 256;
+      const unsigned grid = static_cast<unsigned>((N + rows_per_cta - 1) / rows_per_cta);
+      cudaError_t e;
+      if (wpr == 2)
+        e = launch_pdl(compress_rows_kernel<false, 2>, dim3(grid), dim3(threads), 0, s, w, (int)N, (int)K, ldw, v, m,
+                       scales);
+      else if (wpr == 4)
+        e = launch_pdl(compress_rows_kernel<false, 4>, dim3(grid), dim3(threads), 0, s, w, (int)N, (int)K, ldw, v, m,
+                       scales);
+      else
+        e = launch_pdl(compress_rows_kernel<false, 8>, dim3(grid), dim3(threads), 0, s, w, (int)N, (int)K, ldw, v, m,
+                       scales);
+      if (e != cudaSuccess) return SP24_ERR_CUDA;
     } else {
       const unsigned grid = static_cast<unsigned>((N + kRowsPerCta - 1) / kRowsPerCta);
       if (launch_pdl(compress_rows_kernel<true>, dim3(grid), dim3(256), 0, s, w, (int)N, (int)K, ldw, v, m,
