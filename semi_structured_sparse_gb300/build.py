@@ -62,5 +62,42 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     return LIB
 
 
+# A fault-test copy of the library for the tests of the give-up path: bounded
+# waits give up after 1 ms, and the one-CTA GEMM kernel issues nothing for
+# each CTA's first pipeline stage (SP24_FAULT_WITHHOLD_FIRST_STAGE), so that
+# its MMA thread's wait runs out and the launch reports a device timeout.
+# Built into _build/fault/, separate from libsp24.so, whose build never
+# defines either macro.
+FAULT_DIR = os.path.join(BUILD, "fault")
+FAULT_LIB = os.path.join(FAULT_DIR, "libsp24_faulttest.so")
+FAULT_FLAGS = ["-DSP24_WAIT_TIMEOUT_NS=1000000ull", "-DSP24_FAULT_WITHHOLD_FIRST_STAGE"]
+
+
+def build_fault_test() -> str:
+    """Compile (if sources changed) the fault-test library; return its path."""
+    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(ROOT, "include", "sp24.h"),
+                                                                  os.path.abspath(__file__)]
+    if os.path.exists(FAULT_LIB) and all(os.path.getmtime(d) <= os.path.getmtime(FAULT_LIB) for d in deps):
+        return FAULT_LIB
+    os.makedirs(FAULT_DIR, exist_ok=True)
+
+    def comp(src):
+        obj = os.path.join(FAULT_DIR, src.replace(".cu", ".o"))
+        cmd = [_nvcc()] + ARCH + FLAGS + FAULT_FLAGS + ["-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed for %s:\n%s" % (src, r.stderr))
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(comp, SOURCES))
+    tmp = FAULT_LIB + ".tmp%d" % os.getpid()
+    r = subprocess.run([_nvcc()] + ARCH + ["-shared", "-o", tmp] + objs, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n" + r.stderr)
+    os.replace(tmp, FAULT_LIB)
+    return FAULT_LIB
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))

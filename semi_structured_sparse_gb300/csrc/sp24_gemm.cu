@@ -265,7 +265,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool got = mbar_wait(&empty[stage], phase ^ 1);
         if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
         uint8_t* sA = ring + stage * C::STAGE;
-        if (lane == 0) {
+        // A fault-test build (SP24_FAULT_WITHHOLD_FIRST_STAGE, which the
+        // library itself never defines) issues nothing for the CTA's first
+        // stage: no copies are in flight for it, and the MMA thread's bounded
+        // wait for it runs out.  The tests use it to check the give-up path.
+#ifdef SP24_FAULT_WITHHOLD_FIRST_STAGE
+        const bool issue = flat != 0;
+#else
+        constexpr bool issue = true;
+#endif
+        if (lane == 0 && issue) {
           mbar_arrive_expect_tx(&full[stage], C::LOAD_BYTES);
           bulk_load(sA + C::A_OFF, vsrc + static_cast<int64_t>(kt) * A_STAGE, KS * A_STAGE, &full[stage]);
           bulk_load(sA + C::META_OFF, msrc + static_cast<int64_t>(kt) * META_STAGE, KS * META_STAGE, &full[stage]);

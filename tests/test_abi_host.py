@@ -188,3 +188,12 @@ def test_binding_size_checks():
         s._matrix(torch.zeros(24), 4, 6, "m")
     with pytest.raises(ValueError):
         s._dev_tensor(torch.zeros(4), torch.float32, "t")          # host tensors are refused
+
+
+def test_fault_switches_stay_out_of_the_library():
+    """The give-up-path test library is built apart, with its own switches;
+    the library proper is compiled without them."""
+    from semi_structured_sparse_gb300 import build as b
+    assert b.FAULT_LIB != b.LIB and os.path.dirname(b.FAULT_LIB) != os.path.dirname(b.LIB)
+    assert not any("SP24_FAULT" in f or "SP24_WAIT_TIMEOUT_NS" in f for f in b.FLAGS)
+    assert any("SP24_FAULT_WITHHOLD_FIRST_STAGE" in f for f in b.FAULT_FLAGS)
