@@ -66,11 +66,20 @@ CAPTURED_TRAFFIC = {
     ("decode", 16, 28672, 4096, "gemm"): 73602816 + 467968,
     # sp24_gemm_pair_kernel<240,1,0>, fused side GEMM M 2048, N 4096, K 4096, r 64
     ("fused", 2048, 4096, 4096, "gemm"): 19725056 + 0,
+    # sp24_gemm_pair_kernel<128,0,1>, group-wise M 3000, N 14336, K 4096
+    ("groupwise", 3000, 14336, 4096, "gemm"): 52530000 + 57310000,
+    # compress (no token count): compress_rows_kernel<0,2>, W 4096 x 4096 (the
+    # output stays in L2)
+    ("llama", None, 4096, 4096, "compress"): 33599232 + 256,
+    # compress_rows_kernel<0,2>, W 28672 x 4096
+    ("decode", None, 28672, 4096, "compress"): 234928640 + 18278400,
+    # compress_blocks_kernel, W 14336 x 4096, 128 x 128 block scales
+    ("groupwise", None, 14336, 4096, "compress"): 117486848 + 6374400,
 }
 
 
 def captured_traffic(workload, w, kernel):
-    return CAPTURED_TRAFFIC.get((workload, w.M, w.N, w.K, kernel))
+    return CAPTURED_TRAFFIC.get((workload, None if kernel == "compress" else w.M, w.N, w.K, kernel))
 
 
 # ------------------------------------------------------ algorithmic counts

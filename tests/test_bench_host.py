@@ -60,17 +60,26 @@ def test_decode_description_follows_the_shape():
 
 
 def test_captured_traffic_is_keyed_by_the_full_shape():
+    """GEMM figures are keyed by (M, N, K), compress figures by (N, K) alone:
+    compress reads the weight whatever the token count."""
     for (workload, M, N, K, kernel), traffic in bench.CAPTURED_TRAFFIC.items():
         assert kernel in ("gemm", "compress")
+        assert (M is None) == (kernel == "compress")
         w = inputs.WORKLOADS[workload]
-        if workload == "decode":
+        if workload == "decode" and M is not None:
             w = inputs.with_shape(w, M=M)
-        assert (w.M, w.N, w.K) == (M, N, K), "entry for a shape the benchmark does not run"
+        assert (w.N, w.K) == (N, K) and M in (None, w.M), "entry for a shape the benchmark does not run"
         assert bench.captured_traffic(workload, w, kernel) == traffic
+        for m in inputs.DECODE_M if workload == "decode" and kernel == "compress" else ():
+            assert bench.captured_traffic(workload, inputs.with_shape(w, M=m), kernel) == traffic
         # the algorithmic bytes bound the traffic from below (weights read once)
-        assert traffic >= N * K * 5 // 8 * 0.95 or kernel == "compress"
+        if kernel == "gemm":
+            assert traffic >= N * K * 5 // 8 * 0.95
+        else:
+            assert traffic >= N * K * 2 * 0.99  # the bf16 weight read once
     other = inputs.with_shape(inputs.WORKLOADS["decode"], M=16, N=4096, K=14336)
     assert bench.captured_traffic("decode", other, "gemm") is None
+    assert bench.captured_traffic("decode", other, "compress") is None
 
 
 def test_peaks_fallback_is_labelled(tmp_path, monkeypatch):
