@@ -130,6 +130,8 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 // launch_pair_gemm builds its tensor maps and launches it (args: operands,
 // scales, sizes and the error word; tile counts are its own).
 bool pair_gemm_applies(int64_t M, int64_t N, int64_t K, bool plain, int64_t r);
+// Token tile of a plain-scaled pair launch (256 or 240) on a part with sm_count SMs.
+int pair_token_tile(int64_t M, int64_t N, int sm_count);
 sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
                              const void* X2, const void* W2, int64_t r, const GemmArgs& args, cudaStream_t stream);
 // The same kernel with group-wise promotion (gK = 128): 256 weight rows x 128

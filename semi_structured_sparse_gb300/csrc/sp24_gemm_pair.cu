@@ -76,7 +76,9 @@ struct PairCfg {
   static constexpr int SCL_OFF = LOAD_BYTES;
   static constexpr int STAGE = LOAD_BYTES + (PROMOTE ? KS * 1024 : 0);
   static constexpr int NACC = PROMOTE ? 3 : 1;      // TMEM accumulators of PN columns
-  static constexpr int CHUNK = SIDE ? 24 : 32;      // token chunk: warp half h holds chunks h, h + 2, ...
+  // token chunk (warp half h holds chunks h, h + 2, ...): 32, or 24 when a
+  // warp's PN / 2 tokens are not a multiple of 32 (240-token tiles)
+  static constexpr int CHUNK = (PN / 2) % 32 == 0 ? 32 : 24;
   // tokens per staged store pass (promotion stages the whole tile at once)
   static constexpr int OUT_TOKENS = PROMOTE ? PN : 2 * CHUNK;
   static constexpr int OUT_BYTES = OUT_TOKENS * BM * 2;
@@ -490,18 +492,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
       uint32_t v[C::COLS];  // chunk i of this warp: tokens CHUNK * (half + 2 i) + [0, CHUNK)
 #pragma unroll
-      for (int i = 0; i < C::COLS / CHUNK; ++i) {
-        const uint32_t col = lane_base + CHUNK * (half + 2 * i);
-        tmem_ld16(col, *reinterpret_cast<uint32_t(*)[16]>(v + CHUNK * i));
-        tmem_ld16(col + 16, *reinterpret_cast<uint32_t(*)[16]>(v + CHUNK * i + 16));
-      }
+      for (int i = 0; i < C::COLS / CHUNK; ++i) tmem_load_n<CHUNK>(lane_base + CHUNK * (half + 2 * i), v + CHUNK * i);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(acce_leader);  // the next tile's MMAs may overwrite TMEM
       ++acc_cnt;
       if (last) {
-        // whole tile through the idle ring: [channel half][256 tokens][64 channels] bf16
+        // whole tile through the idle ring: [channel half][PN tokens][64 channels] bf16
         uint16_t* ring_row = reinterpret_cast<uint16_t*>(ring) + (row >> 6) * (PN * 64) + (row & 63);
 #pragma unroll
         for (int i = 0; i < C::COLS / CHUNK; ++i) {
@@ -521,8 +519,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bulk_commit();
         }
       } else {
-        // four passes of 64 tokens through the staging buffer; in pass s every
-        // warp converts its chunk s (tokens 64 s + 32 half + [0, 32))
+        // NPASS passes of OUT_TOKENS = 2 CHUNK tokens through the staging buffer;
+        // in pass s every warp converts its chunk s (tokens OUT_TOKENS s + CHUNK half + [0, CHUNK))
         uint16_t* out_row = reinterpret_cast<uint16_t*>(out_tile) + (row >> 6) * (C::OUT_TOKENS * 64) + (row & 63);
 #pragma unroll
         for (int s = 0; s < C::NPASS; ++s) {
@@ -645,9 +643,20 @@ sp24_status launch_pair(const DeviceInfo* dev, const void* Xq, int64_t ldx, cons
 
 }  // namespace
 
+// Token tile of the plain kernel: 256, or 240 where that takes fewer
+// tile-widths of time, counting every round of tiles over the SM pairs as
+// a full one (M = 2048: 144 tiles of 240 in two rounds against 128 of 256).
+int pair_token_tile(int64_t M, int64_t N, int sm_count) {
+  const int64_t pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+  auto cost = [&](int64_t pn) { return ((M + pn - 1) / pn * (N / 256) + pairs - 1) / pairs * pn; };
+  return cost(240) < cost(256) ? 240 : 256;
+}
+
 sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
                              const void* X2, const void* W2, int64_t r, const GemmArgs& args, cudaStream_t stream) {
   if (r > 0) return launch_pair<240, true, false>(dev, Xq, ldx, Y, ldy, X2, W2, r, args, stream);
+  if (pair_token_tile(args.M, args.N, dev->sm_count) == 240)
+    return launch_pair<240, false, false>(dev, Xq, ldx, Y, ldy, X2, W2, 0, args, stream);
   return launch_pair<256, false, false>(dev, Xq, ldx, Y, ldy, X2, W2, 0, args, stream);
 }
 

@@ -243,6 +243,19 @@ def test_pair_tiles_more_shapes(ora, sp24, M, N, K):
     _check_full(ora, sp24, w, "pair M=%d N=%d K=%d" % (M, N, K))
 
 
+@pytest.mark.parametrize("M,N,K", [(512, 19456, 256), (520, 19456, 384), (2048, 4096, 512), (721, 2048, 768)])
+def test_pair_token_tiles(ora, sp24, M, N, K):
+    """The plain pair kernel's token tile, 256 or 240, whichever takes fewer
+    tile-widths of time over the rounds of tiles on the SM pairs.  On a
+    152-SM part: 512 x 19456 is 152 tiles of 256 in two rounds (228 of 240
+    would take three), so it runs 256-token tiles; 520 tokens need three
+    rounds either way (3 x 240 < 3 x 256); 2048 x 4096 is 144 tiles of 240
+    in two rounds against 128 of 256, also two; 721 tokens end 1 past a
+    240 boundary (a one-token tile in the first SM's half)."""
+    w = inputs.Workload("ptile", M, N, K, seed=M + N + K + 2)
+    _check_full(ora, sp24, w, "pair token tile M=%d N=%d K=%d" % (M, N, K))
+
+
 @pytest.mark.parametrize("M,N,K,r", [(193, 256, 256, 64), (240, 512, 128, 16), (241, 512, 384, 32),
                                      (481, 768, 1024, 48), (2048, 2816, 256, 64)])
 def test_pair_tiles_side_gemm(ora, sp24, M, N, K, r):
