@@ -68,14 +68,16 @@ CAPTURED_TRAFFIC = {
     ("fused", 2048, 4096, 4096, "gemm"): 19725056 + 0,
     # sp24_gemm_pair_kernel<128,0,1>, group-wise M 3000, N 14336, K 4096
     ("groupwise", 3000, 14336, 4096, "gemm"): 52530000 + 57310000,
-    # compress (no token count): compress_rows_kernel<0,2>, W 4096 x 4096 (the
-    # output stays in L2)
-    ("llama", None, 4096, 4096, "compress"): 33599232 + 256,
-    # compress_rows_kernel<0,2>, W 28672 x 4096
-    ("decode", None, 28672, 4096, "compress"): 234928640 + 18278400,
     # compress_blocks_kernel, W 14336 x 4096, 128 x 128 block scales
     ("groupwise", None, 14336, 4096, "compress"): 117486848 + 6374400,
 }
+
+
+def compress_kernel(w):
+    """The kernel sp24_fp8_compress runs for this workload's weight."""
+    if w.gN == 128:
+        return "compress_blocks_kernel"
+    return "compress_rows_pipe_kernel" if w.gk == w.K and w.K <= 4096 else "compress_rows_kernel"
 
 
 def captured_traffic(workload, w, kernel):
@@ -348,7 +350,7 @@ def other_configs(sp24, dev, stream, headline, pk, n):
 
     def compress_row(name, b, wl):
         t = b.time_kernel(b.compress, n)
-        kern = "compress_blocks_kernel" if b.w.gN == 128 else "compress_rows_kernel"
+        kern = compress_kernel(b.w)
         out[name] = dict(t, kernel=kern, N=b.w.N, K=b.w.K, traffic=captured_traffic(wl, b.w, "compress"),
                          **hbm_entry(compress_bytes(b.w), t["ms"], pk["hbm_gbs"]))
 
@@ -594,7 +596,7 @@ def run_ours(args):
                     traffic=captured_traffic(args.workload, w, "gemm"),
                     **(tensor_entry(w, t_gemm["ms"], fp8, pk["bf16_tflops"]) if w.M > 64
                        else hbm_entry(gemm_bytes(w), t_gemm["ms"], pk["hbm_gbs"])))
-    comp_kernel = "compress_blocks_kernel" if w.gN == 128 else "compress_rows_kernel"
+    comp_kernel = compress_kernel(w)
     comp_row = dict(t_comp, kernel=comp_kernel, N=w.N, K=w.K, traffic=captured_traffic(args.workload, w, "compress"),
                     **hbm_entry(compress_bytes(w), t_comp["ms"], pk["hbm_gbs"]))
     kernels = {args.workload + "_gemm": gemm_row, args.workload + "_compress": comp_row}

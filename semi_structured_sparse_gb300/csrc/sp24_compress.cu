@@ -200,10 +200,11 @@ constexpr int kRowsPerCta = 8;   // gK = 128: one warp per weight row
 constexpr int kRowThreads = 128;    // gK = K: 128-thread CTAs (a finer last wave), WPR warps per weight row
 constexpr int kHeldChunks = 8;   // per warp: 8 x 16 bytes per lane stay in registers
 
-// gN = 1.  GK128 = false: one scale per row (gK = K); WPR warps share a row
-// (2 up to K = 4096, 4 up to 8192, 8 above, so that every chunk of rows up
-// to 16384 stays in registers), warp h owning the 256-element chunks
-// c = h, h + WPR, ...; the row's amax is combined through shared memory.
+// gN = 1.  GK128 = false: one scale per row (gK = K), rows longer than 4096
+// (shorter ones take compress_rows_pipe_kernel); WPR warps share a row (4 up
+// to K = 8192, 8 above, so that every chunk of rows up to 16384 stays in
+// registers), warp h owning the 256-element chunks c = h, h + WPR, ...; the
+// row's amax is combined through shared memory.
 // GK128 = true: one scale per row and 128-wide K block; one warp per row,
 // each half-warp owns a block.
 template <bool GK128, int WPR = 2>
@@ -273,6 +274,67 @@ __global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* _
         meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
       }
     }
+  }
+  pdl_trigger();
+}
+
+// gN = 1, gK = K, K <= 4096: persistent warp pairs.  Pair p of the grid walks
+// rows p, p + P, p + 2P, ... (P pairs in all); warp h of a pair owns the
+// chunks c = h, h + 2, ... of a row, all held in registers, and loads its
+// chunks of the pair's next row before it packs the current one, so that
+// the loads of one row overlap the integer work of the previous (with every
+// row's loads issued at once, a row could only be packed once its last
+// chunk had arrived).  The pair combines its row amax through shared memory
+// (one slot per row parity) and a named barrier of its 64 threads.
+template <int PAIRS>
+__global__ void __launch_bounds__(64 * PAIRS, 1) compress_rows_pipe_kernel(const uint16_t* __restrict__ W, int N, int K,
+                                                                         int64_t ldw, uint8_t* __restrict__ values,
+                                                                         uint8_t* __restrict__ meta,
+                                                                         float* __restrict__ scales) {
+  __shared__ uint32_t pair_amax[PAIRS][2][2];  // [pair][row parity][warp of the pair]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pr = warp >> 1, h = warp & 1;
+  const int stride = gridDim.x * PAIRS;
+  const int nchunks = (K + 255) / 256;  // at most 16: 8 per warp
+  pdl_wait();
+  auto load = [&](int n, uint4 (&held)[8]) {
+    const uint16_t* row = W + static_cast<int64_t>(n) * ldw;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = 2 * i + h, k = c * 256 + lane * 8;
+      if (c < nchunks && k < K) held[i] = ldg_stream(row + k);
+    }
+  };
+  // one row: amax, scale, packing; it is the pair's parity-th row
+  auto pack = [&](int n, int parity, const uint4 (&held)[8]) {
+    uint32_t amax2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = 2 * i + h, k = c * 256 + lane * 8;
+      if (c < nchunks && k < K) amax2 = amax2_acc(amax2, held[i]);
+    }
+    const uint32_t amax_w = __reduce_max_sync(0xFFFFFFFFu, amax2_bits(amax2));
+    if (lane == 0) pair_amax[pr][parity][h] = amax_w;
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + pr) : "memory");
+    const uint32_t amax = max(pair_amax[pr][parity][0], pair_amax[pr][parity][1]);
+    const float s = weight_scale(amax), r = __frcp_rn(s);
+    if (lane == 0 && h == 0) scales[n] = s;
+    const uint16_t* row = W + static_cast<int64_t>(n) * ldw;
+    if (s >= kMinFastScale)  // the same for the whole row: pair-uniform
+      emit_row<true, 2>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+    else
+      emit_row<false, 2>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+  };
+  uint4 a[8], b[8];
+  int n = blockIdx.x * PAIRS + pr;
+  if (n < N) load(n, a);
+  // two rows per trip, so that the two row buffers keep their registers
+  for (; n < N; n += 2 * stride) {
+    if (n + stride < N) load(n + stride, b);
+    pack(n, 0, a);
+    if (n + stride >= N) break;
+    if (n + 2 * stride < N) load(n + 2 * stride, a);
+    pack(n + stride, 1, b);
   }
   pdl_trigger();
 }
@@ -395,17 +457,22 @@ extern "C" sp24_status sp24_fp8_compress(const void* W, int64_t N, int64_t K, in
         cudaSuccess)
       return SP24_ERR_CUDA;
   } else {
-    if (per_channel) {
+    if (per_channel && K <= 4096) {
+      // persistent warp pairs, one CTA of 8 pairs per SM (fewer when N is small)
+      constexpr int kPairs = 8;
+      const int64_t ctas = (N + kPairs - 1) / kPairs;
+      const unsigned grid = static_cast<unsigned>(ctas < dev->sm_count ? ctas : dev->sm_count);
+      if (launch_pdl(compress_rows_pipe_kernel<kPairs>, dim3(grid), dim3(64 * kPairs), 0, s, w, (int)N, (int)K, ldw, v,
+                     m, scales) != cudaSuccess)
+        return SP24_ERR_CUDA;
+    } else if (per_channel) {
       // warps per row: enough to hold a row of up to 16384 in registers
-      const int wpr = K <= 4096 ? 2 : (K <= 8192 ? 4 : 8);
+      const int wpr = K <= 8192 ? 4 : 8;
       const int rows_per_cta = wpr <= 4 ? kRowThreads / 32 / wpr : 1;
       const unsigned threads = wpr <= 4 ? kRowThreads : 256;
       const unsigned grid = static_cast<unsigned>((N + rows_per_cta - 1) / rows_per_cta);
       cudaError_t e;
-      if (wpr == 2)
-        e = launch_pdl(compress_rows_kernel<false, 2>, dim3(grid), dim3(threads), 0, s, w, (int)N, (int)K, ldw, v, m,
-                       scales);
-      else if (wpr == 4)
+      if (wpr == 4)
         e = launch_pdl(compress_rows_kernel<false, 4>, dim3(grid), dim3(threads), 0, s, w, (int)N, (int)K, ldw, v, m,
                        scales);
       else

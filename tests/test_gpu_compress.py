@@ -44,9 +44,10 @@ def test_compress_ragged_shapes(ora, sp24, N, K, gN, gK):
                                  (128, 16384), (128, 16512), (128, 20480)])
 def test_compress_row_lengths(ora, sp24, N, K):
     """Per-channel compression across row lengths: rows held in registers
-    whole by 2 warps (K <= 4096), 4 warps (K <= 8192) or 8 warps (K <= 16384),
-    rows longer than that whose amax pass streams past the held chunks, and
-    ragged final chunks (K % 256 == 128)."""
+    whole by a persistent warp pair that prefetches its next row (K <= 4096),
+    by 4 warps (K <= 8192) or 8 warps (K <= 16384), rows longer than that
+    whose amax pass streams past the held chunks, and ragged final chunks
+    (K % 256 == 128)."""
     _, W, _, _ = inputs.generate(inputs.Workload("rl", 1, N, K, seed=N ^ K))
     (ov, om, os_), (gv, gm, gs) = _compress_both(ora, sp24, W, 1, K)
     assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
@@ -55,7 +56,8 @@ def test_compress_row_lengths(ora, sp24, N, K):
 
 
 def test_compress_many_rows_per_cta(ora, sp24):
-    """Many short rows: thousands of CTAs, most rows' chunks partly idle."""
+    """Many short rows: each warp pair of the persistent kernel walks 13 or 14
+    of them (both row buffers, an odd count ending early), most chunks idle."""
     _, W, _, _ = inputs.generate(inputs.Workload("mr", 1, 16384, 256, seed=3))
     (ov, om, os_), (gv, gm, gs) = _compress_both(ora, sp24, W, 1, 256)
     assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
