@@ -68,6 +68,11 @@ CAPTURED_TRAFFIC = {
     ("fused", 2048, 4096, 4096, "gemm"): 19725056 + 0,
     # sp24_gemm_pair_kernel<128,0,1>, group-wise M 3000, N 14336, K 4096
     ("groupwise", 3000, 14336, 4096, "gemm"): 52530000 + 57310000,
+    # compress (no token count): compress_rows_pipe_kernel<8>, W 4096 x 4096 (the
+    # output stays in L2)
+    ("llama", None, 4096, 4096, "compress"): 33623040 + 0,
+    # compress_rows_pipe_kernel<8>, W 28672 x 4096
+    ("decode", None, 28672, 4096, "compress"): 234959360 + 18280960,
     # compress_blocks_kernel, W 14336 x 4096, 128 x 128 block scales
     ("groupwise", None, 14336, 4096, "compress"): 117486848 + 6374400,
 }
