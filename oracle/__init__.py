@@ -1,4 +1,5 @@
-"""CPU oracle for the 2:4 sparse FP8 path (numpy front end to ``sp24_oracle.c``).
+"""CPU oracle for the 2:4 sparse FP8 path and its int8 sibling (numpy front end
+to ``sp24_oracle.c``).
 
 TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
 the CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
@@ -41,6 +42,11 @@ def lib():
         for f in ("ora_tile_values", "ora_untile_values", "ora_tile_meta", "ora_untile_meta"):
             getattr(L, f).argtypes = [P, I64, I64, P]
         L.ora_num_threads.restype = ctypes.c_int
+        L.ora_int8_from_f32.argtypes = [ctypes.c_float]
+        L.ora_int8_from_f32.restype = ctypes.c_int8
+        L.ora_compress_int8.argtypes = [P, I64, I64, I64, P, P, P]
+        L.ora_quantize_act_int8.argtypes = [P, I64, I64, I64, P, P]
+        L.ora_gemm_int8.argtypes = [P, P, I64, I64, I64, P, P, P, I64, P, P, P]
         _lib = L
     return _lib
 
@@ -251,3 +257,53 @@ def dequantize(values, meta, scales, gN: int = 1, gK: int = None) -> np.ndarray:
     s = np.repeat(np.repeat(scales.astype(np.float64), gK, axis=0)[:K], gN, axis=1)[:, :N].T  # [N, K]
     prod = e4m3_decode(codes) * s          # exact: 4 x 24 significant bits
     return f32_to_bf16_bits(prod.astype(np.float32))
+
+
+# --------------------------------------------------------------- int8 sibling
+# The int8 x int8 2:4 sibling (pytorch/ao PR #3258, review: int8 x int8 and
+# fp8 x fp8 are the 2:4 kernels; Int8SemiSparseTensor).  The pages define no
+# int8 quantizer; sp24_oracle.c states the symmetric one taken here.
+def int8_encode(x) -> int:
+    """Nearest integer to x (fp32), ties to even, clamped to [-127, 127]."""
+    return int(lib().ora_int8_from_f32(float(x)))
+
+
+def compress_int8(W_bits):
+    """Prune 2:4 and quantize to int8 with one scale per output channel.
+    Returns (values int8 [N,K/2], meta uint8 [N,K/8] logical, scales fp32 [N])."""
+    W_bits = _c(W_bits, np.uint16)
+    N, K = W_bits.shape
+    values = np.empty((N, K // 2), dtype=np.int8)
+    meta = np.empty((N, K // 8), dtype=np.uint8)
+    scales = np.empty(N, dtype=np.float32)
+    lib().ora_compress_int8(_p(W_bits), N, K, K, _p(values), _p(meta), _p(scales))
+    return values, meta, scales
+
+
+def quantize_act_int8(X):
+    """Per-token int8 activation quantization: (xq int8 [M,K], sx fp32 [M])."""
+    X = _c(X, np.float32)
+    M, K = X.shape
+    xq = np.empty((M, K), dtype=np.int8)
+    sx = np.empty(M, dtype=np.float32)
+    lib().ora_quantize_act_int8(_p(X), M, K, K, _p(xq), _p(sx))
+    return xq, sx
+
+
+def gemm_int8(xq, sx, values, meta, sw, bias=None):
+    """Y[M,N] (float64 of the fp32 result) and the exact int32 sums acc[M,N]."""
+    xq = _c(xq, np.int8)
+    M, K = xq.shape
+    values = _c(values, np.int8)
+    meta = _c(meta, np.uint8)
+    N = values.shape[0]
+    sx = _c(sx, np.float32)
+    sw = _c(sw, np.float32)
+    assert sx.shape == (M,) and sw.shape == (N,) and K <= 131072
+    if bias is not None:
+        bias = _c(bias, np.uint16)
+        assert bias.shape == (N,)
+    Y = np.empty((M, N), dtype=np.float64)
+    acc = np.empty((M, N), dtype=np.int32)
+    lib().ora_gemm_int8(_p(xq), _p(sx), M, K, K, _p(values), _p(meta), _p(sw), N, _p(bias), _p(acc), _p(Y))
+    return Y, acc

@@ -27,7 +27,11 @@
  *     PR #2095, promotion of per-K-tile partial sums), plus an optional
  *     bf16 side GEMM X2.W2^T added into the same output (CUTLASS issue
  *     #2058 "How to implement a fused mixed precision matrix multiplication
- *     such as w4a4 + w16a16?", hyx1999's statement of Y = X1 W1^T + X2 W2^T).
+ *     such as w4a4 + w16a16?", hyx1999's statement of Y = X1 W1^T + X2 W2^T);
+ *   - the int8 x int8 2:4 sibling (same PR #3258, review: int8 x int8 and
+ *     fp8 x fp8 are the two 2:4 kernels): symmetric int8 quantization of the
+ *     pruned weight and the activation, exact integer sums (section at the
+ *     end of this file).
  *
  * Readings taken where the pages are silent:
  *   - ties in the pruning argsort: the lower index wins;
@@ -377,6 +381,119 @@ void ora_gemm(const uint8_t *xq, const float *sx, int64_t M, int64_t K, int64_t 
                 if (acc_fp64) accd += (double)b; else accf += b;
             }
             Y[m * N + n] = acc_fp64 ? accd : (double)accf;
+        }
+    }
+}
+
+/* ------------------------------------------------------------ int8 sibling */
+
+/* The int8 x int8 2:4 sibling of the FP8 path.  pytorch/ao PR #3258 (review:
+ * the only 2:4 kernels are int8 x int8 and fp8 x fp8; Int8SemiSparseTensor)
+ * names it but defines no int8 quantizer, so the plainest symmetric one is
+ * taken:
+ *   - scale = amax / 127 (fp32, correctly rounded) per output channel for
+ *     the weight and per token for the activation; 1 for an all-zero row;
+ *   - q = the integer nearest to the correctly rounded fp32 quotient x/scale,
+ *     ties to even, clamped to [-127, 127] (|x| <= amax keeps it inside);
+ *   - pruning, metadata and storage as for the FP8 weight, one byte (two's
+ *     complement) per kept value;
+ *   - GEMM: acc = the exact integer sum of the kept products, then
+ *     y = (sx * sw) * float(acc) in fp32, plus the bf16 bias if any. */
+#define INT8_MAX_Q 127.0f
+
+/* Nearest integer, ties to even, written out (no dependence on the host's
+ * rounding mode): x - floor(x) is exact for |x| < 2^23. */
+static float round_half_even(float x)
+{
+    float f = floorf(x), d = x - f;
+    if (d > 0.5f) return f + 1.0f;
+    if (d < 0.5f) return f;
+    return fmodf(f, 2.0f) == 0.0f ? f : f + 1.0f;
+}
+
+int8_t ora_int8_from_f32(float x)
+{
+    float r = round_half_even(x);
+    if (r > INT8_MAX_Q) r = INT8_MAX_Q;
+    if (r < -INT8_MAX_Q) r = -INT8_MAX_Q;
+    return (int8_t)r;
+}
+
+static float int8_scale(float amax)
+{
+    return amax == 0.0f ? 1.0f : amax / INT8_MAX_Q;
+}
+
+/* values[n][K/2] int8 (as bytes), meta[n][K/8] as ora_compress, scales[n]. */
+void ora_compress_int8(const uint16_t *W, int64_t N, int64_t K, int64_t ldw,
+                       uint8_t *values, uint8_t *meta, float *scales)
+{
+    int64_t n;
+#pragma omp parallel for schedule(static)
+    for (n = 0; n < N; ++n) {
+        int64_t g, k;
+        float amax = 0.0f, s;
+        for (k = 0; k < K; ++k) {
+            float a = fabsf(ora_bf16_to_f32(W[n * ldw + k]));
+            if (a > amax) amax = a;
+        }
+        s = int8_scale(amax);
+        scales[n] = s;
+        for (g = 0; g < K / 8; ++g) meta[n * (K / 8) + g] = 0;
+        for (g = 0; g < K / 4; ++g) {
+            const uint16_t *v = W + n * ldw + 4 * g;
+            int keep[2], t;
+            ora_keep2(v, keep);
+            for (t = 0; t < 2; ++t)
+                values[n * (K / 2) + 2 * g + t] = (uint8_t)ora_int8_from_f32(ora_bf16_to_f32(v[keep[t]]) / s);
+            meta[n * (K / 8) + g / 2] |= (uint8_t)((keep[0] | (keep[1] << 2)) << (4 * (g & 1)));
+        }
+    }
+}
+
+/* Per-token int8 quantization of X fp32 [M][K] (row stride ldx): xq [M][K]
+ * int8 (as bytes), sx [M]. */
+void ora_quantize_act_int8(const float *X, int64_t M, int64_t K, int64_t ldx, uint8_t *xq, float *sx)
+{
+    int64_t m;
+#pragma omp parallel for schedule(static)
+    for (m = 0; m < M; ++m) {
+        int64_t k;
+        float amax = 0.0f, s;
+        for (k = 0; k < K; ++k) {
+            float a = fabsf(X[m * ldx + k]);
+            if (a > amax) amax = a;
+        }
+        s = int8_scale(amax);
+        sx[m] = s;
+        for (k = 0; k < K; ++k) xq[m * K + k] = (uint8_t)ora_int8_from_f32(X[m * ldx + k] / s);
+    }
+}
+
+/* Y[m][n] = (sx[m] * sw[n]) * float(acc[m][n]) (+ bias[n]) with acc the exact
+ * integer sum over the kept k of wq[n][k] * xq[m][k].  acc [M][N] (int32, or
+ * NULL) receives the sums; K <= 131072 keeps them inside int32. */
+void ora_gemm_int8(const uint8_t *xq, const float *sx, int64_t M, int64_t K, int64_t ldx,
+                   const uint8_t *values, const uint8_t *meta, const float *sw, int64_t N,
+                   const uint16_t *bias, int32_t *acc, double *Y)
+{
+    int64_t m;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (m = 0; m < M; ++m) {
+        int64_t n;
+        for (n = 0; n < N; ++n) {
+            int64_t a = 0, g;
+            float y;
+            for (g = 0; g < K / 4; ++g) {
+                int nib = (meta[n * (K / 8) + g / 2] >> (4 * (g & 1))) & 0xF;
+                int i0 = nib & 3, i1 = (nib >> 2) & 3;
+                a += (int64_t)(int8_t)values[n * (K / 2) + 2 * g] * (int8_t)xq[m * ldx + 4 * g + i0];
+                a += (int64_t)(int8_t)values[n * (K / 2) + 2 * g + 1] * (int8_t)xq[m * ldx + 4 * g + i1];
+            }
+            if (acc) acc[m * N + n] = (int32_t)a;
+            y = (sx[m] * sw[n]) * (float)a;
+            if (bias) y += ora_bf16_to_f32(bias[n]);
+            Y[m * N + n] = (double)y;
         }
     }
 }

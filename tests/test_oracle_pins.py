@@ -456,3 +456,106 @@ def test_tiled_layout_known_positions(ora):
     m[129, 20] = 9     # band 1, k tile 1 -> tile 5: 1*16 + 4
     tm = ora.tile_meta(m)
     assert tm[19] == 7 and tm[5 * 2048 + 20] == 9
+
+
+# ---------------------------------------------------------------- int8 sibling
+def test_int8_rounding_golden(ora):
+    """Hand-derived: ties go to the even integer, both signs; the clamp."""
+    cases = {2.5: 2, 3.5: 4, -2.5: -2, -3.5: -4, 0.5: 0, -0.5: 0, 1.5: 2, 126.5: 126, 125.5: 126,
+             127.4: 127, 127.5: 127, 200.0: 127, -300.0: -127, 0.49999997: 0, 2.5000002: 3, -0.0: 0}
+    for x, q in cases.items():
+        assert ora.int8_encode(x) == q, x
+
+
+def test_int8_rounding_matches_numpy(ora):
+    """numpy's rint (round half to even) on fp32 grids: every half point in
+    [-128, 128], its fp32 neighbours, and random values."""
+    rng = np.random.default_rng(8)
+    half = np.arange(-256, 257, dtype=np.float32) / 2
+    grid = np.concatenate([half, np.nextafter(half, np.float32(np.inf)), np.nextafter(half, np.float32(-np.inf)),
+                           rng.uniform(-127, 127, 3000).astype(np.float32)])
+    want = np.clip(np.rint(grid.astype(np.float64)), -127, 127).astype(np.int64)
+    got = np.array([ora.int8_encode(x) for x in grid])
+    assert np.array_equal(got, want)
+
+
+def test_int8_compress_against_numpy(ora):
+    """Per-channel scale = amax/127 and q = rint(fp32(w / s)) computed with
+    numpy's fp32 division; the pruning and metadata are the FP8 weight's."""
+    w = inputs.Workload("i8c", 1, 256, 512, seed=17)
+    _, W, _, _ = inputs.generate(w)
+    bits = inputs.bf16_bits(W)
+    values, meta, scales = ora.compress_int8(bits)
+    _, meta_fp8, _ = ora.compress(bits)
+    assert np.array_equal(meta, meta_fp8)
+    Wf = ora.bf16_bits_to_f32(bits)
+    amax = np.abs(Wf).max(axis=1)
+    s_np = np.where(amax == 0, np.float32(1), (amax / np.float32(127)).astype(np.float32))
+    assert np.array_equal(scales.view(np.uint32), s_np.astype(np.float32).view(np.uint32))
+    # the kept values, read through the metadata
+    N, K = Wf.shape
+    for n in range(0, N, 37):
+        for g in range(K // 4):
+            nib = (int(meta[n, g // 2]) >> (4 * (g & 1))) & 0xF
+            i0, i1 = nib & 3, nib >> 2
+            for t, i in enumerate((i0, i1)):
+                q = np.rint(np.float64(np.float32(Wf[n, 4 * g + i]) / np.float32(scales[n])))
+                assert values[n, 2 * g + t] == int(np.clip(q, -127, 127))
+    # the row maximum maps to +-127
+    assert np.abs(values.astype(np.int64)).max(axis=1).min() == 127
+
+
+def test_int8_gemm_equals_integer_matmul(ora):
+    """The int32 sums equal numpy's exact int64 matmul of the dense int8
+    operands (the kept weights at their positions, zeros elsewhere); Y is the
+    fp32 product of the two scales and the sum, plus the bias."""
+    rng = np.random.default_rng(9)
+    w = inputs.Workload("i8g", 37, 256, 768, seed=19)
+    X, W, _, _ = inputs.generate(w)
+    values, meta, sw = ora.compress_int8(inputs.bf16_bits(W))
+    xq, sx = ora.quantize_act_int8(X.numpy())
+    bias = inputs.bf16_bits(torch.from_numpy(rng.normal(size=256).astype(np.float32)).to(torch.bfloat16))
+    Y, acc = ora.gemm_int8(xq, sx, values, meta, sw, bias=bias)
+    dense = np.zeros((256, 768), dtype=np.int64)
+    for g in range(768 // 4):
+        nib = (meta[:, g // 2].astype(np.int64) >> (4 * (g & 1))) & 0xF
+        rows = np.arange(256)
+        dense[rows, 4 * g + (nib & 3)] = values[:, 2 * g]
+        dense[rows, 4 * g + (nib >> 2)] = values[:, 2 * g + 1]
+    ref = xq.astype(np.int64) @ dense.T
+    assert np.array_equal(acc.astype(np.int64), ref)
+    y32 = (sx[:, None] * sw[None, :]).astype(np.float32) * ref.astype(np.float32)
+    y32 = (y32 + ora.bf16_bits_to_f32(bias)[None, :]).astype(np.float32)
+    assert np.array_equal(Y.astype(np.float32), y32)
+
+
+def test_int8_quantize_act_against_numpy(ora):
+    rng = np.random.default_rng(10)
+    X = rng.normal(size=(9, 384)).astype(np.float32)
+    X[3] = 0.0
+    xq, sx = ora.quantize_act_int8(X)
+    amax = np.abs(X).max(axis=1)
+    s_np = np.where(amax == 0, np.float32(1), (amax / np.float32(127)).astype(np.float32)).astype(np.float32)
+    assert np.array_equal(sx, s_np)
+    q = np.clip(np.rint((X / s_np[:, None]).astype(np.float32).astype(np.float64)), -127, 127)
+    assert np.array_equal(xq.astype(np.int64), q.astype(np.int64))
+    assert not xq[3].any()
+
+
+def test_int8_bruteforce_tiny(ora):
+    """A 1 x 8 x 8 case summed by hand in Python integers."""
+    W = np.array([[3, -1, 0, 2, 5, 5, -7, 1]] * 8, dtype=np.float32) * np.arange(1, 9, dtype=np.float32)[:, None]
+    X = np.array([[1, -2, 3, -4, 5, -6, 7, -8]], dtype=np.float32)
+    bits = _bf16_bits_from_f32(W)
+    values, meta, sw = ora.compress_int8(bits)
+    xq, sx = ora.quantize_act_int8(X)
+    _, acc = ora.gemm_int8(xq, sx, values, meta, sw)
+    for n in range(8):
+        total = 0
+        for g in range(2):
+            nib = (int(meta[n, 0]) >> (4 * g)) & 0xF
+            for t, i in enumerate((nib & 3, nib >> 2)):
+                total += int(values[n, 2 * g + t]) * int(xq[0, 4 * g + i])
+        assert acc[0, n] == total
+        # the two kept of (3, -1, 0, 2) are 3 and 2; of (5, 5, -7, 1), -7 and the first 5
+        assert (meta[n, 0] & 0xF) == (0 | 3 << 2) and (meta[n, 0] >> 4) == (0 | 2 << 2)
