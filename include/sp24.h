@@ -311,6 +311,54 @@ SP24_API int sp24_fp8_gemm_decomposition(int64_t M, int64_t N, int64_t K, int64_
  */
 SP24_API sp24_status sp24_last_device_error(void* stream);
 
+/*
+ * ---------------------------------------------------------- int8 sibling
+ * The int8 x int8 2:4 path ([3258], review: the 2:4 kernels are int8 x int8
+ * and fp8 x fp8; Int8SemiSparseTensor).  The pages name it but give no int8
+ * quantizer; the plain symmetric one is used: scale = amax / 127 (correctly
+ * rounded fp32; 1.0 for an all-zero row), code = the integer nearest to the
+ * correctly rounded quotient x / scale, ties to even, in [-127, 127].
+ *
+ * sp24_int8_compress -- magnitude 2:4 pruning along K (as sp24_fp8_compress),
+ * int8 codes with one scale per output channel.
+ *   W       (device) bf16 [N][K], row stride ldw >= K (ldw*2 a multiple of 16).
+ *   values  (device, out) [N*K/2] int8 codes, meta (device, out) [N*K/8]: the
+ *           tiled storage of sp24_fp8_compress, with int8 codes in place of
+ *           e4m3 ones.
+ *   scales  (device, out) fp32 [N].
+ * Preconditions: N a positive multiple of 128; K a positive multiple of 128;
+ * W, values, meta 16-byte aligned.
+ */
+SP24_API sp24_status sp24_int8_compress(const void* W, int64_t N, int64_t K, int64_t ldw, void* values, void* meta,
+                               float* scales, void* stream);
+
+/*
+ * sp24_int8_quantize_act -- per-token int8 activation quantization.
+ *   X   (device) fp32 [M][K], row stride ldx >= K (ldx*4 a multiple of 16).
+ *   xq  (device, out) int8 [M][K] (row stride K); sx (device, out) fp32 [M].
+ * Preconditions: M >= 1; K a positive multiple of 128; X, xq 16-byte aligned.
+ */
+SP24_API sp24_status sp24_int8_quantize_act(const float* X, int64_t M, int64_t K, int64_t ldx, void* xq, float* sx,
+                                   void* stream);
+
+/*
+ * sp24_int8_gemm -- Y[m][n] = bf16( (sx[m] * sw[n]) * float(acc[m][n]) + bias[n] ),
+ * acc[m][n] = the exact integer sum over the kept k of wq[n][k] * xq[m][k].
+ * Each step is rounded as written (fp32, then bf16 round to nearest even).
+ * sm_103a has no int8 tensor-core MMA of the tcgen05 family, so this runs on
+ * the warp-level sparse MMA (mma.sp m16n8k64 s8).
+ *   Xq  (device) int8 [M][K], row stride ldx >= K (a multiple of 16).
+ *   sx  (device) fp32 [M]; values, meta (device) from sp24_int8_compress;
+ *   sw  (device) fp32 [N]; bias (device) bf16 [N] or NULL.
+ *   Y   (device, out) bf16 [M][N], row stride ldy >= N.
+ * Preconditions: M >= 1; N a positive multiple of 128; K a positive multiple
+ * of 128 and at most 131072 (SP24_ERR_UNSUPPORTED above: the int32 sums stay
+ * exact); Xq, values, meta 16-byte aligned; sx, sw 4-byte aligned.
+ */
+SP24_API sp24_status sp24_int8_gemm(const void* Xq, const float* sx, int64_t M, int64_t K, int64_t ldx,
+                           const void* values, const void* meta, const float* sw, int64_t N, const void* bias,
+                           void* Y, int64_t ldy, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -44,6 +44,9 @@ SIGNATURES = {
     "sp24_fp8_gemm_fixed_scratch": ([_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _I, _P, _P, _I64, _P, _P,
                                      _I64, _P], _I),
     "sp24_last_device_error": ([_P], _I),
+    "sp24_int8_compress": ([_P, _I64, _I64, _I64, _P, _P, _P, _P], _I),
+    "sp24_int8_quantize_act": ([_P, _I64, _I64, _I64, _P, _P, _P], _I),
+    "sp24_int8_gemm": ([_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P, _I64, _P], _I),
 }
 
 
@@ -348,6 +351,90 @@ def gemm_batched(xq, sx, values, meta, sw, gM: int = 1, gN: int = 1, gK: int = N
         0 if bias is None else bias.stride(0), y.stride(0), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream)),
         "sp24_fp8_gemm_batched")
+    return y
+
+
+# --------------------------------------------------------------- int8 sibling
+def compress_int8(w: torch.Tensor, out=None, stream=None):
+    """Magnitude 2:4 prune + int8 (one scale per output channel) + pack of a bf16
+    weight [N, K]: (values int8 [N, K/2], meta uint8 [N, K/8], scales fp32 [N]),
+    values and meta in the tiled storage gemm_int8() reads."""
+    lib = load()
+    _dev_tensor(w, torch.bfloat16, "w")
+    if w.dim() != 2:
+        raise ValueError("w must be [N, K]")
+    N, K = w.shape
+    if out is None:
+        values = torch.empty((N, K // 2), dtype=torch.int8, device=w.device)
+        meta = torch.empty((N, K // 8), dtype=torch.uint8, device=w.device)
+        scales = torch.empty(N, dtype=torch.float32, device=w.device)
+    else:
+        values, meta, scales = out
+        _dev_tensor(values, torch.int8, "values", w.device)
+        _dev_tensor(meta, torch.uint8, "meta", w.device)
+        _dev_tensor(scales, torch.float32, "scales", w.device)
+        _at_least(values, N * (K // 2), "values")
+        _at_least(meta, N * (K // 8), "meta")
+        _at_least(scales, N, "scales")
+    _check(lib.sp24_int8_compress(_ptr(w), N, K, w.stride(0), _ptr(values), _ptr(meta), _ptr(scales),
+                                  _stream(stream)), "sp24_int8_compress")
+    return values, meta, scales
+
+
+def quantize_act_int8(x: torch.Tensor, out=None, stream=None):
+    """Per-token int8 quantization of fp32 activations [M, K]: (xq int8 [M, K], sx fp32 [M])."""
+    lib = load()
+    _dev_tensor(x, torch.float32, "x")
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
+    M, K = x.shape
+    if out is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+        sx = torch.empty(M, dtype=torch.float32, device=x.device)
+    else:
+        xq, sx = out
+        _dev_tensor(xq, torch.int8, "xq", x.device)
+        _dev_tensor(sx, torch.float32, "sx", x.device)
+        _matrix(xq, M, K, "xq")
+        if not xq.is_contiguous():
+            raise ValueError("xq must be contiguous")
+        _at_least(sx, M, "sx")
+    _check(lib.sp24_int8_quantize_act(_ptr(x), M, K, x.stride(0), _ptr(xq), _ptr(sx), _stream(stream)),
+           "sp24_int8_quantize_act")
+    return xq, sx
+
+
+def gemm_int8(xq, sx, values, meta, sw, bias=None, out=None, stream=None):
+    """Y[M, N] bf16 = bf16((sx[m] sw[n]) * float(sum of the kept xq[m, k] wq[n, k]) + bias[n])
+    for int8 activations xq [M, K] and compress_int8()'s packed weight."""
+    lib = load()
+    _dev_tensor(xq, torch.int8, "xq")
+    dev_ = xq.device
+    _dev_tensor(values, torch.int8, "values", dev_)
+    if xq.dim() != 2 or values.dim() != 2:
+        raise ValueError("xq must be [M, K] and values [N, K/2]")
+    _dev_tensor(meta, torch.uint8, "meta", dev_)
+    _dev_tensor(sx, torch.float32, "sx", dev_)
+    _dev_tensor(sw, torch.float32, "sw", dev_)
+    M, K = xq.shape
+    N = values.shape[0]
+    if not (sx.is_contiguous() and sw.is_contiguous() and values.is_contiguous() and meta.is_contiguous()):
+        raise ValueError("scales, values and meta must be contiguous")
+    _at_least(values, N * (K // 2), "values")
+    _at_least(meta, N * (K // 8), "meta")
+    _at_least(sx, M, "sx")
+    _at_least(sw, N, "sw")
+    if bias is not None:
+        _dev_tensor(bias, torch.bfloat16, "bias", dev_)
+        if not bias.is_contiguous() or bias.numel() != N:
+            raise ValueError("bias must be a contiguous bf16 vector of N values")
+    if out is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev_)
+    else:
+        y = _dev_tensor(out, torch.bfloat16, "out", dev_)
+        _matrix(y, M, N, "out")
+    _check(lib.sp24_int8_gemm(_ptr(xq), _ptr(sx), M, K, xq.stride(0), _ptr(values), _ptr(meta), _ptr(sw), N,
+                              _ptr(bias), _ptr(y), y.stride(0), _stream(stream)), "sp24_int8_gemm")
     return y
 
 

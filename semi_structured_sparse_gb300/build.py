@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsp24.so")
-SOURCES = ["sp24_abi.cu", "sp24_compress.cu", "sp24_gemm.cu", "sp24_gemm_pair.cu"]
+SOURCES = ["sp24_abi.cu", "sp24_compress.cu", "sp24_gemm.cu", "sp24_gemm_pair.cu", "sp24_int8.cu"]
 HEADERS = ["sp24_internal.cuh", "sp24_ptx.cuh", "sp24_gemm_common.cuh"]
 ROOT = os.path.dirname(HERE)
 

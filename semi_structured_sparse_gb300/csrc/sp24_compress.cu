@@ -22,10 +22,16 @@ constexpr float kE4M3Max = 448.0f;
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+// int8 sibling: symmetric codes in [-127, 127] (pytorch/ao PR #3258 names
+// the int8 x int8 2:4 kernels; the quantizer is the plain symmetric one).
+constexpr float kInt8Max = 127.0f;
+
 // Scale for a block whose largest |w| has bf16 magnitude bits `amax_bits`:
-// amax / 448 (correctly rounded), or 1 when the block is all zeros.
+// amax / 448 (amax / 127 for int8 codes), correctly rounded, or 1 when the
+// block is all zeros.
+template <bool I8 = false>
 __device__ __forceinline__ float weight_scale(uint32_t amax_bits) {
-  return amax_bits == 0 ? 1.0f : __fdiv_rn(bf16_bits_to_float(amax_bits), kE4M3Max);
+  return amax_bits == 0 ? 1.0f : __fdiv_rn(bf16_bits_to_float(amax_bits), I8 ? kInt8Max : kE4M3Max);
 }
 
 // Running max of |w| over 16-byte chunks, kept as a packed bf16 pair: for
@@ -74,6 +80,14 @@ __device__ __forceinline__ float div_scale(float x, float s, float r) {
   return __fmaf_rn(-nrem, r, q0);
 }
 
+// Two fp32 -> int8 codes: nearest integer, ties to even, clamped to
+// [-127, 127]; `lo` in bits [7:0], `hi` in bits [15:8].
+__device__ __forceinline__ uint32_t to_s8x2(float lo, float hi) {
+  const int a = max(-127, min(127, __float2int_rn(lo)));
+  const int b = max(-127, min(127, __float2int_rn(hi)));
+  return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8);
+}
+
 // Two fp32 -> e4m3 conversions in one instruction (round to nearest even,
 // saturate to +-448); `lo` lands in bits [7:0], `hi` in bits [15:8].
 __device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi) {
@@ -95,7 +109,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
-template <bool FAST, int NIB_SHIFT = 16>
+template <bool FAST, int NIB_SHIFT = 16, bool I8 = false>
 __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s, float r) {
   // Keys from the raw words: the shifts move each 15-bit magnitude to bits
   // [16:2] and the mask drops the sign bit and the neighbouring element, so
@@ -116,17 +130,18 @@ __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s
   const uint32_t sel = i0 * 0x22u + i1 * 0x2200u + 0x1010u;
   const uint32_t pair = prmt(lo, hi, sel);
   const float x0 = __uint_as_float(pair * 65536u), x1 = __uint_as_float(pair & 0xFFFF0000u);
-  const uint32_t q = FAST ? to_e4m3x2(div_scale(x0, s, r), div_scale(x1, s, r))
-                          : to_e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  const float q0 = FAST ? div_scale(x0, s, r) : __fdiv_rn(x0, s);
+  const float q1 = FAST ? div_scale(x1, s, r) : __fdiv_rn(x1, s);
+  const uint32_t q = I8 ? to_s8x2(q0, q1) : to_e4m3x2(q0, q1);
   // q < 2^16: the nibble i0 | i1 << 2 goes to bits [NIB_SHIFT + 3 : NIB_SHIFT]
   return q + i0 * (1u << NIB_SHIFT) + i1 * (4u << NIB_SHIFT);
 }
 
 // Two groups (8 bf16 in a 16-byte chunk) -> 4 value bytes and 1 meta byte.
-template <bool FAST>
+template <bool FAST, bool I8 = false>
 __device__ __forceinline__ void pack_chunk(const uint4& v, float s, float r, uint32_t& vals, uint32_t& metab) {
-  const uint32_t g0 = pack_group<FAST, 16>(v.x, v.y, s, r);  // nibble in bits [19:16]
-  const uint32_t g1 = pack_group<FAST, 20>(v.z, v.w, s, r);  // nibble in bits [23:20]
+  const uint32_t g0 = pack_group<FAST, 16, I8>(v.x, v.y, s, r);  // nibble in bits [19:16]
+  const uint32_t g1 = pack_group<FAST, 20, I8>(v.z, v.w, s, r);  // nibble in bits [23:20]
   vals = prmt(g0, g1, 0x5410u);           // codes of group 0 in bytes 0-1, group 1 in bytes 2-3
   metab = prmt(g0 | g1, 0u, 0x4442u);     // byte 2 of (g0 | g1): the two nibbles
 }
@@ -171,7 +186,7 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 // Packs and stores the chunks c = h, h + WPR, ... of row n (WPR warps per
 // row): the first kHeldChunks from registers, any further ones re-read from
 // global.
-template <bool FAST, int WPR>
+template <bool FAST, int WPR, bool I8 = false>
 __device__ __forceinline__ void emit_row(const uint4 (&held)[8], const uint16_t* row, int n, int K, int nchunks, int h,
                                          int lane, float s, float r, uint8_t* values, uint8_t* meta) {
   const RowStore st(n, K, lane);
@@ -180,7 +195,7 @@ __device__ __forceinline__ void emit_row(const uint4 (&held)[8], const uint16_t*
     const int c = WPR * i + h, k = c * 256 + lane * 8;
     if (c < nchunks && k < K) {
       uint32_t vals, mb;
-      pack_chunk<FAST>(held[i], s, r, vals, mb);
+      pack_chunk<FAST, I8>(held[i], s, r, vals, mb);
       *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
       meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
     }
@@ -189,7 +204,7 @@ __device__ __forceinline__ void emit_row(const uint4 (&held)[8], const uint16_t*
     const int k = c * 256 + lane * 8;
     if (k < K) {
       uint32_t vals, mb;
-      pack_chunk<FAST>(*reinterpret_cast<const uint4*>(row + k), s, r, vals, mb);
+      pack_chunk<FAST, I8>(*reinterpret_cast<const uint4*>(row + k), s, r, vals, mb);
       *reinterpret_cast<uint32_t*>(values + st.values_at(c)) = vals;
       meta[st.meta_at(c)] = static_cast<uint8_t>(mb);
     }
@@ -207,7 +222,7 @@ constexpr int kHeldChunks = 8;   // per warp: 8 x 16 bytes per lane stay in regi
 // row's amax is combined through shared memory.
 // GK128 = true: one scale per row and 128-wide K block; one warp per row,
 // each half-warp owns a block.
-template <bool GK128, int WPR = 2>
+template <bool GK128, int WPR = 2, bool I8 = false>
 __global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* __restrict__ W, int N, int K, int64_t ldw,
                                                             uint8_t* __restrict__ values, uint8_t* __restrict__ meta,
                                                             float* __restrict__ scales) {
@@ -242,12 +257,12 @@ __global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* _
     const int w0 = warp - h;  // the row's first warp
 #pragma unroll
     for (int i = 0; i < WPR; ++i) amax = max(amax, warp_amax[w0 + i]);
-    const float s = weight_scale(amax), r = __frcp_rn(s);
+    const float s = weight_scale<I8>(amax), r = __frcp_rn(s);
     if (lane == 0 && h == 0) scales[n] = s;
     if (s >= kMinFastScale)  // the same for the whole row: warp-uniform
-      emit_row<true, WPR>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+      emit_row<true, WPR, I8>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
     else
-      emit_row<false, WPR>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+      emit_row<false, WPR, I8>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
   } else {
     // lanes 0-15 cover K block 2c, lanes 16-31 block 2c+1 (when it exists)
     const int n = blockIdx.x * kRowsPerCta + warp;
@@ -286,7 +301,7 @@ __global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* _
 // row's loads issued at once, a row could only be packed once its last
 // chunk had arrived).  The pair combines its row amax through shared memory
 // (one slot per row parity) and a named barrier of its 64 threads.
-template <int PAIRS>
+template <int PAIRS, bool I8 = false>
 __global__ void __launch_bounds__(64 * PAIRS, 1) compress_rows_pipe_kernel(const uint16_t* __restrict__ W, int N, int K,
                                                                          int64_t ldw, uint8_t* __restrict__ values,
                                                                          uint8_t* __restrict__ meta,
@@ -317,13 +332,13 @@ __global__ void __launch_bounds__(64 * PAIRS, 1) compress_rows_pipe_kernel(const
     if (lane == 0) pair_amax[pr][parity][h] = amax_w;
     asm volatile("bar.sync %0, 64;" ::"r"(1 + pr) : "memory");
     const uint32_t amax = max(pair_amax[pr][parity][0], pair_amax[pr][parity][1]);
-    const float s = weight_scale(amax), r = __frcp_rn(s);
+    const float s = weight_scale<I8>(amax), r = __frcp_rn(s);
     if (lane == 0 && h == 0) scales[n] = s;
     const uint16_t* row = W + static_cast<int64_t>(n) * ldw;
     if (s >= kMinFastScale)  // the same for the whole row: pair-uniform
-      emit_row<true, 2>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+      emit_row<true, 2, I8>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
     else
-      emit_row<false, 2>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
+      emit_row<false, 2, I8>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
   };
   uint4 a[8], b[8];
   int n = blockIdx.x * PAIRS + pr;
@@ -389,7 +404,7 @@ __device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_ca
 
 // Activation quantization (fp32 input): one warp per token row; 128
 // elements per warp step (4 per lane).  GK128: each step is one scale block.
-template <bool GK128>
+template <bool GK128, bool I8 = false>
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ X, int M, int K, int64_t ldx,
                                                            uint8_t* __restrict__ xq, float* __restrict__ sx) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -400,8 +415,11 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
   uint8_t* qrow = xq + static_cast<int64_t>(m) * K;
   const int nsteps = K / 128;
   auto quant4 = [&](const float4& f, float s) -> uint32_t {
+    if (I8)
+      return to_s8x2(__fdiv_rn(f.x, s), __fdiv_rn(f.y, s)) | (to_s8x2(__fdiv_rn(f.z, s), __fdiv_rn(f.w, s)) << 16);
     return to_e4m3x2(__fdiv_rn(f.x, s), __fdiv_rn(f.y, s)) | (to_e4m3x2(__fdiv_rn(f.z, s), __fdiv_rn(f.w, s)) << 16);
   };
+  constexpr float kQMax = I8 ? kInt8Max : kE4M3Max;
   auto amax4 = [](const float4& f) { return fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))); };
   if (GK128) {
     for (int c = 0; c < nsteps; ++c) {
@@ -409,7 +427,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
       float a = amax4(f);
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-      const float s = a == 0.0f ? 1.0f : __fdiv_rn(a, kE4M3Max);
+      const float s = a == 0.0f ? 1.0f : __fdiv_rn(a, kQMax);
       if (lane == 0) sx[static_cast<int64_t>(c) * M + m] = s;
       *reinterpret_cast<uint32_t*>(qrow + c * 128 + lane * 4) = quant4(f, s);
     }
@@ -418,7 +436,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
     for (int c = 0; c < nsteps; ++c) a = fmaxf(a, amax4(load4(row + c * 128 + lane * 4)));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-    const float s = a == 0.0f ? 1.0f : __fdiv_rn(a, kE4M3Max);
+    const float s = a == 0.0f ? 1.0f : __fdiv_rn(a, kQMax);
     if (lane == 0) sx[m] = s;
     for (int c = 0; c < nsteps; ++c) {
       const float4 f = load4(row + c * 128 + lane * 4);
@@ -664,6 +682,59 @@ extern "C" sp24_status sp24_fp8_quantize_act(const float* X, int64_t M, int64_t 
 extern "C" sp24_status sp24_fp8_quantize_act_bf16(const void* X, int64_t M, int64_t K, int64_t ldx, int gK, void* xq,
                                                   float* sx, void* stream) {
   return sp24::quantize_act(static_cast<const uint16_t*>(X), M, K, ldx, gK, xq, sx, stream);
+}
+
+extern "C" sp24_status sp24_int8_compress(const void* W, int64_t N, int64_t K, int64_t ldw, void* values, void* meta,
+                                          float* scales, void* stream) {
+  using namespace sp24;
+  if (!W || !values || !meta || !scales) return SP24_ERR_INVALID_ARG;
+  if (N < 1 || K < 128 || K % 128 != 0 || ldw < K || N > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
+  if (N % 128 != 0) return SP24_ERR_INVALID_ARG;  // tiled storage: whole 128-row bands
+  if (!aligned16(W) || !aligned16(values) || !aligned16(meta) || (ldw * 2) % 16 != 0) return SP24_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(scales) % 4 != 0) return SP24_ERR_ALIGNMENT;
+  const DeviceInfo* dev = nullptr;
+  sp24_status st = current_device(&dev);
+  if (st != SP24_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t* w = static_cast<const uint16_t*>(W);
+  uint8_t* v = static_cast<uint8_t*>(values);
+  uint8_t* m = static_cast<uint8_t*>(meta);
+  cudaError_t e;
+  if (K <= 4096) {  // the FP8 path's kernels with int8 codes
+    constexpr int kPairs = 8;
+    const int64_t ctas = (N + kPairs - 1) / kPairs;
+    const unsigned grid = static_cast<unsigned>(ctas < dev->sm_count ? ctas : dev->sm_count);
+    e = launch_pdl(compress_rows_pipe_kernel<kPairs, true>, dim3(grid), dim3(64 * kPairs), 0, s, w, (int)N, (int)K,
+                   ldw, v, m, scales);
+  } else {
+    const int wpr = K <= 8192 ? 4 : 8;
+    const int rows_per_cta = wpr <= 4 ? kRowThreads / 32 / wpr : 1;
+    const unsigned threads = wpr <= 4 ? kRowThreads : 256;
+    const unsigned grid = static_cast<unsigned>((N + rows_per_cta - 1) / rows_per_cta);
+    e = wpr == 4 ? launch_pdl(compress_rows_kernel<false, 4, true>, dim3(grid), dim3(threads), 0, s, w, (int)N, (int)K,
+                              ldw, v, m, scales)
+                 : launch_pdl(compress_rows_kernel<false, 8, true>, dim3(grid), dim3(threads), 0, s, w, (int)N, (int)K,
+                              ldw, v, m, scales);
+  }
+  if (e != cudaSuccess) return SP24_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+}
+
+extern "C" sp24_status sp24_int8_quantize_act(const float* X, int64_t M, int64_t K, int64_t ldx, void* xq, float* sx,
+                                              void* stream) {
+  using namespace sp24;
+  if (!X || !xq || !sx) return SP24_ERR_INVALID_ARG;
+  if (M < 1 || K < 128 || K % 128 != 0 || ldx < K || M > (1 << 30) || K > (1 << 30)) return SP24_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(xq) || (ldx * 4) % 16 != 0) return SP24_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(sx) % 4 != 0) return SP24_ERR_ALIGNMENT;
+  const DeviceInfo* dev = nullptr;
+  const sp24_status st = current_device(&dev);
+  if (st != SP24_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_pdl(quantize_act_kernel<false, true>, dim3(static_cast<unsigned>((M + 7) / 8)), dim3(256), 0, s, X, (int)M,
+                 (int)K, ldx, static_cast<uint8_t*>(xq), sx) != cudaSuccess)
+    return SP24_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
 }
 
 extern "C" sp24_status sp24_fp8_decompress(const void* values, const void* meta, const float* scales, int64_t N,

@@ -197,3 +197,21 @@ def test_fault_switches_stay_out_of_the_library():
     assert b.FAULT_LIB != b.LIB and os.path.dirname(b.FAULT_LIB) != os.path.dirname(b.LIB)
     assert not any("SP24_FAULT" in f or "SP24_WAIT_TIMEOUT_NS" in f for f in b.FLAGS)
     assert any("SP24_FAULT_WITHHOLD_FIRST_STAGE" in f for f in b.FAULT_FLAGS)
+
+
+def test_int8_argument_errors(lib):
+    """The int8 sibling's entry points refuse bad arguments before any launch."""
+    P = ctypes.c_void_p
+    one = P(16)
+    INVALID, UNSUPPORTED = 1, 2  # SP24_ERR_INVALID_ARG, SP24_ERR_UNSUPPORTED
+    # compress: N not a multiple of 128, K not a multiple of 128, null pointers
+    assert lib.sp24_int8_compress(one, 100, 256, 256, one, one, one, None) == INVALID
+    assert lib.sp24_int8_compress(one, 128, 200, 200, one, one, one, None) == INVALID
+    assert lib.sp24_int8_compress(None, 128, 256, 256, one, one, one, None) == INVALID
+    # quantize: K not a multiple of 128, ldx < K
+    assert lib.sp24_int8_quantize_act(one, 4, 100, 100, one, one, None) == INVALID
+    assert lib.sp24_int8_quantize_act(one, 4, 256, 128, one, one, None) == INVALID
+    # gemm: K above the exact-int32 bound, N not a multiple of 128, ldy < N
+    assert lib.sp24_int8_gemm(one, one, 4, 131200, 131200, one, one, one, 128, None, one, 128, None) == UNSUPPORTED
+    assert lib.sp24_int8_gemm(one, one, 4, 256, 256, one, one, one, 100, None, one, 128, None) == INVALID
+    assert lib.sp24_int8_gemm(one, one, 4, 256, 256, one, one, one, 128, None, one, 64, None) == INVALID
