@@ -366,6 +366,7 @@ def other_configs(sp24, dev, stream, headline, pk, n):
         gemm_row(wl + "_gemm", b, wl)
         if wl == "llama":
             compress_row("llama_compress", b, wl)
+            out.update(int8_rows(sp24, b, pk, n))
         del b
     if headline != "groupwise":
         b = Bench(sp24, inputs.WORKLOADS["groupwise"], dev, stream)
@@ -385,6 +386,35 @@ def other_configs(sp24, dev, stream, headline, pk, n):
         gemm_row("decode_gemm_M%d" % M, b, "decode")
     torch.cuda.synchronize()
     return out
+
+
+def int8_rows(sp24, b, pk, n):
+    """The int8 x int8 2:4 sibling on the Llama-style linear's shape and
+    rotating sets (per-token x per-channel int8): its compress (HBM-bound) and
+    its GEMM, which runs on the warp-level sparse MMA (sm_103a has no int8
+    tcgen05 MMA), reported against the fp8 tensor peak for context."""
+    w = b.w
+    for s in b.sets:
+        s["v8"], s["m8"], s["sw8"] = sp24.compress_int8(s["W"])
+        s["xq8"], s["sx8"] = sp24.quantize_act_int8(b.X.to(b.dev))
+    torch.cuda.synchronize()
+    t_g = b.time_kernel(lambda s: sp24.gemm_int8(s["xq8"], s["sx8"], s["v8"], s["m8"], s["sw8"], out=s["y"]), n)
+    t_c = b.time_kernel(lambda s: sp24.compress_int8(s["W"], out=(s["v8"], s["m8"], s["sw8"])), n)
+    ops = w.M * w.N * w.K  # 2 M N K / 2: kept weights only
+    fp8 = pk["bf16_tflops"] * FP8_OVER_BF16
+    achieved = ops / (t_g["ms"] * 1e-3) / 1e12
+    c_bytes = w.N * w.K * 2 + w.N * w.K // 2 + w.N * w.K // 8 + 4 * w.N
+    for s in b.sets:
+        for k in ("v8", "m8", "sw8", "xq8", "sx8"):
+            del s[k]
+    return {
+        "llama_int8_gemm": dict(t_g, kernel="sp24_int8_gemm_kernel", M=w.M, N=w.N, K=w.K, bound="tensor",
+                                achieved=round(achieved, 1), unit="TOPS", peak=None,
+                                frac_of_fp8_peak=round(achieved / fp8, 4),
+                                counts="2*M*N*K/2 int8 operations (kept weights only)"),
+        "llama_int8_compress": dict(t_c, kernel=compress_kernel(w) + " (int8 codes)",
+                                    N=w.N, K=w.K, **hbm_entry(c_bytes, t_c["ms"], pk["hbm_gbs"])),
+    }
 
 
 def next_rows(sp24, b, pk, n):
@@ -609,6 +639,8 @@ def run_ours(args):
     if world == 1 and not args.quick:
         kernels.update(other_configs(sp24, dev, stream, args.workload, pk, n_k))
         extra = next_rows(sp24, b, pk, n_k)
+        for k in [k for k in kernels if "_int8_" in k]:  # the int8 sibling is a next row, not a configuration
+            extra[k] = kernels.pop(k)
     # the dominant kernel of the step
     if t_gemm["ms"] >= t_comp["ms"]:
         g = gemm_row
