@@ -44,6 +44,9 @@ METRIC = "sparse FP8 GEMM TFLOPS & % of FP8 sparse peak; compress GB/s & % HBM p
 UNIT = "TFLOPS"
 FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 REPLAYS = 5          # timed graph replays per figure (median, min, max)
+# The warp-level int8 sparse MMA's rate on this part (kept-weight TOPS), the
+# int8 GEMM's roofline: mma.sp m16n8k64 s8 in a register-only loop.
+INT8_MMA_SP_TOPS = 150.6
 
 DESCR = {
     "llama": "Llama-style FP8 linear: X[2048,4096] e4m3 per-token (N(0,1), 0.1% outliers x20), "
@@ -392,7 +395,9 @@ def int8_rows(sp24, b, pk, n):
     """The int8 x int8 2:4 sibling on the Llama-style linear's shape and
     rotating sets (per-token x per-channel int8): its compress (HBM-bound) and
     its GEMM, which runs on the warp-level sparse MMA (sm_103a has no int8
-    tcgen05 MMA), reported against the fp8 tensor peak for context."""
+    tcgen05 MMA).  The GEMM's peak is that instruction's own rate on this part,
+    measured with a register-only loop of it: 150.6 TOPS of kept-weight work
+    (0.062 MMA per clock per SM at 4 to 16 warps per SM)."""
     w = b.w
     for s in b.sets:
         s["v8"], s["m8"], s["sw8"] = sp24.compress_int8(s["W"])
@@ -409,7 +414,9 @@ def int8_rows(sp24, b, pk, n):
             del s[k]
     return {
         "llama_int8_gemm": dict(t_g, kernel="sp24_int8_gemm_kernel", M=w.M, N=w.N, K=w.K, bound="tensor",
-                                achieved=round(achieved, 1), unit="TOPS", peak=None,
+                                achieved=round(achieved, 1), unit="TOPS", peak=INT8_MMA_SP_TOPS,
+                                frac=round(achieved / INT8_MMA_SP_TOPS, 4),
+                                peak_source="mma.sp m16n8k64 s8 in a register-only loop on this part",
                                 frac_of_fp8_peak=round(achieved / fp8, 4),
                                 counts="2*M*N*K/2 int8 operations (kept weights only)"),
         "llama_int8_compress": dict(t_c, kernel=compress_kernel(w) + " (int8 codes)",
