@@ -111,15 +111,16 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 template <bool FAST, int NIB_SHIFT = 16, bool I8 = false>
 __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s, float r) {
-  // Keys from the raw words: the shifts move each 15-bit magnitude to bits
-  // [16:2] and the mask drops the sign bit and the neighbouring element, so
-  // no separate |w| step is needed.  Left shifts are written as multiplies
-  // and right shifts as high multiplies, which run on the FMA pipe beside the
-  // integer min/max work.
-  const uint32_t k0 = ((lo * 4u) & 0x1FFFCu) | 3u;               // element 0
-  const uint32_t k1 = (__umulhi(lo, 1u << 18) & 0x1FFFCu) | 2u;  // element 1: lo >> 14
-  const uint32_t k2 = ((hi * 4u) & 0x1FFFCu) | 1u;               // element 2
-  const uint32_t k3 = __umulhi(hi, 1u << 18) & 0x1FFFCu;         // element 3
+  // Keys from the raw words, with multiplies only (the FMA pipe, beside the
+  // integer min/max work): a multiply by 2^17 moves an element's 15
+  // magnitude bits to [31:17] and pushes its sign bit and the neighbouring
+  // element out of the word, so no |w| or mask step is needed; the added
+  // 3 - i fills bits [1:0].  The high half is brought down first with a
+  // high multiply (x >> 16).
+  const uint32_t k0 = lo * (1u << 17) + 3u;                    // element 0
+  const uint32_t k1 = __umulhi(lo, 1u << 16) * (1u << 17) + 2u;  // element 1
+  const uint32_t k2 = hi * (1u << 17) + 1u;                    // element 2
+  const uint32_t k3 = __umulhi(hi, 1u << 16) * (1u << 17);       // element 3
   const uint32_t hi01 = max(k0, k1), lo01 = min(k0, k1);
   const uint32_t hi23 = max(k2, k3), lo23 = min(k2, k3);
   const uint32_t first = max(hi01, hi23);
@@ -129,7 +130,7 @@ __device__ __forceinline__ uint32_t pack_group(uint32_t lo, uint32_t hi, float s
   // byte selector: element i is bytes 2i, 2i+1 of {hi:lo}; kept pair -> {v_i1 : v_i0}
   const uint32_t sel = i0 * 0x22u + i1 * 0x2200u + 0x1010u;
   const uint32_t pair = prmt(lo, hi, sel);
-  const float x0 = __uint_as_float(pair * 65536u), x1 = __uint_as_float(pair & 0xFFFF0000u);
+  const float x0 = __uint_as_float(pair * 65536u), x1 = __uint_as_float(__umulhi(pair, 65536u) * 65536u);
   const float q0 = FAST ? div_scale(x0, s, r) : __fdiv_rn(x0, s);
   const float q1 = FAST ? div_scale(x1, s, r) : __fdiv_rn(x1, s);
   const uint32_t q = I8 ? to_s8x2(q0, q1) : to_e4m3x2(q0, q1);
