@@ -112,11 +112,14 @@ def test_quantize_act_bit_exact(ora, sp24, name, gK):
 
 
 @pytest.mark.parametrize("gK", [None, 128])
-@pytest.mark.parametrize("M,K", [(1, 128), (7, 512), (300, 4096), (2048, 4096)])
+@pytest.mark.parametrize("M,K", [(1, 128), (7, 512), (300, 4096), (513, 384), (2048, 4096), (3000, 4096),
+                                 (8192, 4096)])
 def test_quantize_act_bf16_bit_exact(ora, sp24, M, K, gK):
     """bf16 activations (the inference dtype of the pages' models): quantized
     exactly as their fp32 widening, which the oracle quantizes.  Rows of
-    zeros, bf16 subnormals and values near the bf16 maximum included."""
+    zeros, bf16 subnormals and values near the bf16 maximum included.  K =
+    384 ends each row with a half step of 128 elements; 3000 and 8192 rows of
+    4096 take more than one wave of row CTAs."""
     g = torch.Generator().manual_seed(M + K)
     X = (torch.randn(M, K, generator=g) * 3.0).to(torch.bfloat16)
     X[0, :64] = 0.0
