@@ -99,6 +99,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// L2 prefetches.  A prefetch is a cache hint with no effect on what any load
+// returns (a line that another kernel writes afterwards is updated in L2, where
+// every later load reads it), so a kernel may issue them before pdl_wait() for
+// operands it will read once the previous kernel is done.
+// [src, src + bytes): src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // 3D tiled load / store (a batch index as the third coordinate).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
   asm volatile(
