@@ -63,14 +63,14 @@ DESCR = {
 # the current kernel build (summaries and commands under profiles/).  An entry
 # is removed when its kernel changes; absent entries report null.
 CAPTURED_TRAFFIC = {
-    # sp24_gemm_pair_kernel<256,0,0> on the Llama-style linear (M 2048, N 4096, K 4096)
-    ("llama", 2048, 4096, 4096, "gemm"): 18938880 + 0,
+    # sp24_gemm_pair_kernel<240,0,0> on the Llama-style linear (M 2048, N 4096, K 4096)
+    ("llama", 2048, 4096, 4096, "gemm"): 18939648 + 0,
     # sp24_gemm_kernel<16,0,0,0,4,0> (whole tiles), decode M 16, N 28672, K 4096
-    ("decode", 16, 28672, 4096, "gemm"): 73602816 + 467968,
+    ("decode", 16, 28672, 4096, "gemm"): 73608192 + 411392,
     # sp24_gemm_pair_kernel<240,1,0>, fused side GEMM M 2048, N 4096, K 4096, r 64
-    ("fused", 2048, 4096, 4096, "gemm"): 19725056 + 0,
+    ("fused", 2048, 4096, 4096, "gemm"): 19725312 + 0,
     # sp24_gemm_pair_kernel<128,0,1>, group-wise M 3000, N 14336, K 4096
-    ("groupwise", 3000, 14336, 4096, "gemm"): 52530000 + 57310000,
+    ("groupwise", 3000, 14336, 4096, "gemm"): 51097088 + 55554048,
     # compress (no token count): compress_rows_pipe_kernel<8>, W 4096 x 4096 (the
     # output stays in L2)
     ("llama", None, 4096, 4096, "compress"): 33622784 + 0,
