@@ -135,9 +135,11 @@ int pair_token_tile(int64_t M, int64_t N, int sm_count);
 sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
                              const void* X2, const void* W2, int64_t r, const GemmArgs& args, cudaStream_t stream);
 // The same kernel with group-wise promotion (gK = 128): 256 weight rows x 128
-// tokens per pair tile, each K block's partial sum in one of three TMEM
-// accumulators and scaled into fp32 registers by its epilogue.
+// (or 112) tokens per pair tile, each K block's partial sum in one of three
+// (or four) TMEM accumulators and scaled into fp32 registers by its epilogue.
 bool pair_promote_applies(int64_t M, int64_t N, int64_t K, int64_t r);
+// Token tile of a group-wise pair launch (128, or 112 with four accumulators).
+int pair_promote_token_tile(int64_t M, int64_t N, int sm_count);
 sp24_status launch_pair_promote(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
                                 const GemmArgs& args, cudaStream_t stream);
 

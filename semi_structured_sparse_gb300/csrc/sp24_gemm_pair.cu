@@ -75,10 +75,13 @@ struct PairCfg {
   // tile's PN tokens then sw of this CTA's 128 channels (cp.async)
   static constexpr int SCL_OFF = LOAD_BYTES;
   static constexpr int STAGE = LOAD_BYTES + (PROMOTE ? KS * 1024 : 0);
-  static constexpr int NACC = PROMOTE ? 3 : 1;      // TMEM accumulators of PN columns
+  // TMEM accumulators of PN columns: promotion keeps one partial per K block in
+  // flight in each, three of 128 tokens or four of 112 beside the metadata ring
+  static constexpr int NACC = PROMOTE ? (PN <= 112 ? 4 : 3) : 1;
   // token chunk (warp half h holds chunks h, h + 2, ...): 32, or 24 when a
-  // warp's PN / 2 tokens are not a multiple of 32 (240-token tiles)
-  static constexpr int CHUNK = (PN / 2) % 32 == 0 ? 32 : 24;
+  // warp's PN / 2 tokens are not a multiple of 32 (240-token tiles); under
+  // promotion with 112-token tiles, the warp's 56 tokens in one chunk
+  static constexpr int CHUNK = (PN / 2) % 32 == 0 ? 32 : (PROMOTE ? PN / 2 : 24);
   // tokens per staged store pass (promotion stages the whole tile at once)
   static constexpr int OUT_TOKENS = PROMOTE ? PN : 2 * CHUNK;
   static constexpr int OUT_BYTES = OUT_TOKENS * BM * 2;
@@ -97,6 +100,7 @@ struct PairCfg {
   static_assert(STAGES >= 3 && STAGES <= MAX_STAGES, "pipeline depth");
   static_assert(SIDE ? (PN <= SIDE_COL && SIDE_COL + PN <= META_BASE) : NACC * PN <= META_COL0, "TMEM columns");
   static_assert(!PROMOTE || (!SIDE && PN + BM <= 256), "a scale slot holds PN + 128 floats");
+  static_assert(NACC <= 4, "four accumulator barriers");
   static_assert(NCHUNK * CHUNK == COLS && CHUNK % 8 == 0 && OUT_TOKENS * NPASS == PN, "epilogue chunks");
   static_assert(STAGES * STAGE >= PN * BM * 2, "the ring holds a whole output tile");
   static_assert(!SIDE || SIDE_W2_BYTES + SIDE_X2_BYTES <= STAGE, "the side operands fit one stage");
@@ -145,8 +149,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* full = bars;                  // [STAGES] leader: both CTAs' loads -> MMA
   uint64_t* empty = bars + MAX_STAGES;    // [STAGES] each CTA: MMA done with the stage -> its loads
   uint64_t* accf = bars + 2 * MAX_STAGES; // [NACC] each CTA: accumulator complete -> its epilogue
-  uint64_t* acce = accf + 3;              // [NACC] leader: both epilogues drained the accumulator -> MMA
-  uint64_t* sfull = acce + 3;             // [STAGES] promotion, each CTA: the stage's scales landed
+  uint64_t* acce = accf + 4;              // [NACC] leader: both epilogues drained the accumulator -> MMA
+  uint64_t* sfull = acce + 4;             // [STAGES] promotion, each CTA: the stage's scales landed
   uint64_t* drain = sfull + MAX_STAGES;   // leader: every MMA finished (before TMEM is freed)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
 
@@ -660,8 +664,20 @@ sp24_status launch_pair_gemm(const DeviceInfo* dev, const void* Xq, int64_t ldx,
   return launch_pair<256, false, false>(dev, Xq, ldx, Y, ldy, X2, W2, 0, args, stream);
 }
 
+// Token tile of a group-wise pair launch: 112 (four accumulators) where it
+// takes no more rounds of tiles over the SM pairs than 128 (three), counting
+// a 112-token round at the 0.93 of a 128-token one measured on the 152-SM part
+// (N 4096, M 2048: 52.6 against 56.9 us in four rounds each).
+int pair_promote_token_tile(int64_t M, int64_t N, int sm_count) {
+  const int64_t pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+  auto rounds = [&](int64_t pn) { return ((M + pn - 1) / pn * (N / 256) + pairs - 1) / pairs; };
+  return rounds(112) * 93 < rounds(128) * 100 ? 112 : 128;
+}
+
 sp24_status launch_pair_promote(const DeviceInfo* dev, const void* Xq, int64_t ldx, const void* Y, int64_t ldy,
                                 const GemmArgs& args, cudaStream_t stream) {
+  if (pair_promote_token_tile(args.M, args.N, dev->sm_count) == 112)
+    return launch_pair<112, false, true>(dev, Xq, ldx, Y, ldy, nullptr, nullptr, 0, args, stream);
   return launch_pair<128, false, true>(dev, Xq, ldx, Y, ldy, nullptr, nullptr, 0, args, stream);
 }
 

@@ -271,15 +271,30 @@ def test_pair_tiles_side_gemm(ora, sp24, M, N, K, r):
 @pytest.mark.parametrize("gM,gN", [(1, 128), (1, 1), (128, 128), (128, 1)])
 @pytest.mark.parametrize("M,N,K", [(65, 256, 256), (130, 512, 768), (300, 768, 1024), (2000, 1536, 512)])
 def test_pair_tiles_groupwise(ora, sp24, gM, gN, M, N, K):
-    """Group-wise promotion (gK = 128) on SM pairs: 256 x 128 tiles, each K
-    block's partial in one of three tensor-memory accumulators, scaled by its
-    own sx sw into fp32 registers.  Per-channel and 128-row block weight
-    scales, per-token and 128-token block activation scales, token tails in
-    either SM's half of a tile, a single stage, four stages per tile
-    (K = 1024), and more tiles than pairs (2000 x 1536: 16 token tiles x 6
-    weight-row tiles = 96)."""
+    """Group-wise promotion (gK = 128) on SM pairs: each K block's partial in
+    one of the tensor-memory accumulators, scaled by its own sx sw into fp32
+    registers.  These shapes take as many rounds of tiles with 112 tokens as
+    with 128, so they run the 112-token tiles (four accumulators).
+    Per-channel and 128-row block weight scales, per-token and 128-token
+    block activation scales, token tails in either SM's half of a tile, a
+    single stage, four stages per tile (K = 1024), and more tiles than pairs
+    (2000 x 1536: 18 token tiles x 6 weight-row tiles = 108)."""
     w = inputs.Workload("pairgw", M, N, K, gM=gM, gN=gN, gK=128, seed=M + N + K + gM + 3 * gN)
     _check_full(ora, sp24, w, "pair group-wise g=(%d,%d) M=%d N=%d K=%d" % (gM, gN, M, N, K))
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 4096, 256), (1000, 4096, 512), (513, 4096, 256), (1024, 14336, 256),
+                                   (1100, 14336, 256)])
+def test_pair_promote_token_tiles(ora, sp24, M, N, K):
+    """The group-wise pair kernel's token tile: 112 (four accumulators) where
+    it takes no more rounds of tiles over the SM pairs than 128 (three), else
+    128.  On a 152-SM part: 2048 x 4096 is four rounds either way, 1000 and
+    513 tokens (a 65-token last tile: 56 in the first SM's half, 9 in the
+    second) two, so those run 112; 1024 x 14336 is 6 rounds of 128 against 8
+    of 112, and 1100 tokens 7 against 8 (a 76-token last tile), so those run
+    128, the tile of the group-wise benchmark."""
+    w = inputs.Workload("pgwtile", M, N, K, gN=128, gK=128, seed=M + N + K + 9)
+    _check_full(ora, sp24, w, "group-wise pair token tile M=%d N=%d K=%d" % (M, N, K))
 
 
 def test_groupwise_odd_k_blocks_falls_back(ora, sp24):
