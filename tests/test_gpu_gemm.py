@@ -297,6 +297,15 @@ def test_pair_promote_token_tiles(ora, sp24, M, N, K):
     _check_full(ora, sp24, w, "group-wise pair token tile M=%d N=%d K=%d" % (M, N, K))
 
 
+@pytest.mark.parametrize("gM,gN", [(128, 128), (1, 1), (128, 1)])
+def test_pair_promote_128_token_tiles_granularities(ora, sp24, gM, gN):
+    """The 128-token group-wise tiles (the benchmark's) with the other scale
+    granularities: 128-token activation blocks and per-channel weight scales,
+    on 1100 x 14336 (7 rounds of 128-token tiles against 8 of 112)."""
+    w = inputs.Workload("pgw128", 1100, 14336, 256, gM=gM, gN=gN, gK=128, seed=gM + 5 * gN)
+    _check_full(ora, sp24, w, "group-wise 128-token tiles g=(%d,%d)" % (gM, gN))
+
+
 def test_groupwise_odd_k_blocks_falls_back(ora, sp24):
     """An odd number of 128-wide K blocks does not fill the pair kernel's
     two-block stages: such calls run on the one-CTA kernel, with the same result."""
