@@ -101,6 +101,7 @@ struct PairCfg {
   static_assert(SIDE ? (PN <= SIDE_COL && SIDE_COL + PN <= META_BASE) : NACC * PN <= META_COL0, "TMEM columns");
   static_assert(!PROMOTE || (!SIDE && PN + BM <= 256), "a scale slot holds PN + 128 floats");
   static_assert(NACC <= 4, "four accumulator barriers");
+  static_assert(SCL_OFF % 16 == 0, "scale slots start on a 16-byte boundary (read as float4)");
   static_assert(NCHUNK * CHUNK == COLS && CHUNK % 8 == 0 && OUT_TOKENS * NPASS == PN, "epilogue chunks");
   static_assert(STAGES * STAGE >= PN * BM * 2, "the ring holds a whole output tile");
   static_assert(!SIDE || SIDE_W2_BYTES + SIDE_X2_BYTES <= STAGE, "the side operands fit one stage");
