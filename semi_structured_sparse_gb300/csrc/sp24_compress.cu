@@ -295,7 +295,8 @@ __global__ void __launch_bounds__(256, 4) compress_rows_kernel(const uint16_t* _
 }
 
 // gN = 1, gK = K, K <= 4096: persistent warp pairs.  Pair p of the grid walks
-// rows p, p + P, p + 2P, ... (P pairs in all); warp h of a pair owns the
+// rows p, p + P, p + 2P, ... (P pairs in all; pair p is pair p / G of CTA
+// p mod G, G CTAs); warp h of a pair owns the
 // chunks c = h, h + 2, ... of a row, all held in registers, and loads its
 // chunks of the pair's next row before it packs the current one, so that
 // the loads of one row overlap the integer work of the previous (with every
@@ -342,7 +343,10 @@ __global__ void __launch_bounds__(64 * PAIRS, 1) compress_rows_pipe_kernel(const
       emit_row<false, 2, I8>(held, row, n, K, nchunks, h, lane, s, r, values, meta);
   };
   uint4 a[8], b[8];
-  int n = blockIdx.x * PAIRS + pr;
+  // pair pr of CTA c is pair pr G + c of the grid: when the rows do not divide
+  // evenly, the pairs with one row more are spread over all the SMs instead
+  // of filling the first CTAs (4096 rows: 448 of 1216 pairs take a fourth)
+  int n = pr * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
   if (n < N) load(n, a);
   // two rows per trip, so that the two row buffers keep their registers
   for (; n < N; n += 2 * stride) {
